@@ -1,0 +1,181 @@
+/*
+ * fa3.h -- C ABI of the GB300 (sm_103a) per-head INT8 attention-quantization
+ * library (libfa3.so).
+ *
+ * The library implements the data-parallel hot path of "FA3" activation
+ * quantization as described by msModelSlim's algorithm page
+ * ("FA3量化：Flash Attention 3激活量化算法说明", section 原理 / 算法流程) and used by
+ * MindIE ("FA3 quantization" and "Attention Quantization", Overview):
+ *   - per-head Recall-Window calibration with a running min/max,
+ *   - symmetric per-head INT8 parameters and quantize-on-append,
+ *   - decode-phase attention that reads the INT8 KV cache directly
+ *     (absorbed MLA with a bf16 RoPE key, and GQA with INT8 q/k/v).
+ *
+ * Conventions shared by every call:
+ *   - Array arguments are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or synchronizes; every call only enqueues work on
+ *     `stream` (a cudaStream_t passed as void*; NULL = the legacy default
+ *     stream) and returns.
+ *   - bf16 data is passed as uint16_t bit patterns.
+ *   - The return value is an fa3_status.  Host-side validation (null
+ *     pointers, sizes, alignment, options) happens before anything is
+ *     enqueued: on any error other than FA3_ECUDA nothing was enqueued.
+ *   - Errors that depend on device data (an append position, a context
+ *     length) cannot be seen on the host.  Kernels OR the FA3_DEVERR_* bits
+ *     into the optional caller-owned device word `dev_err` (int32, may be
+ *     NULL) and skip the offending row; the caller reads the word when it
+ *     likes.  Kernels never trap and every wait inside them is bounded.
+ *   - Calls on the same stream are ordered; calls that share a workspace
+ *     must not run concurrently on different streams.
+ */
+#ifndef FA3_H_
+#define FA3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum fa3_status {
+  FA3_OK = 0,
+  FA3_EINVAL = 1,       /* null pointer, non-positive size, bad option            */
+  FA3_ERANGE = 2,       /* a size or alignment outside what the kernels support    */
+  FA3_ECUDA = 3,        /* the CUDA runtime reported an error while enqueuing      */
+  FA3_EWORKSPACE = 4,   /* workspace pointer NULL or smaller than required         */
+  FA3_EDEVICE = 5       /* current device is not an sm_103 (GB300-class) GPU       */
+};
+
+/* Bits written into the optional device error word. */
+#define FA3_DEVERR_POS 1      /* append: pos[b] < 0 or pos[b] + T_new > T_max (row skipped)    */
+#define FA3_DEVERR_LENS 2     /* decode: lens[b] < 0 or lens[b] > T_max (output row set to 0) */
+#define FA3_DEVERR_TIMEOUT 4  /* a bounded wait inside a kernel gave up (output not valid)    */
+
+/* Human-readable name of a status code (static string). */
+const char* fa3_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int fa3_version(void);
+
+/* ------------------------------------------------------------------------
+ * Calibration -- msModelSlim FA3量化, 原理 / 算法流程 steps 1-3.
+ *
+ * Step 1: every head h collects the N = B*L values x[b, h, 0..L) of all b
+ *   (L = S*D for an activation of shape (B, H, S, D)).
+ * Step 2 (Recall Window): sort the N values, target_num = int(ratio * N)
+ *   (float64 product, truncated, at least 1), and among the windows
+ *   [sorted[i], sorted[i + target_num - 1]], i = 0 .. N - target_num, take
+ *   the narrowest (width computed in float64; ties -> smallest i).
+ * Step 3: min_io[h] = min(min_io[h], lo[h]), max_io[h] = max(max_io[h], hi[h]).
+ *   -0.0 orders before +0.0 in both the sort and the min/max.
+ *
+ * x        bf16 values; element (b, h, l) at x[b*stride_b + h*stride_h + l]
+ *          (strides in elements; l is contiguous).  Values must be finite.
+ * B, H, L  B >= 1, 1 <= H, L >= 1, B*L < 2^32.
+ * ratio    in (0, 1]; the pages' default is 0.9999.
+ * min_io, max_io  float[H], in/out.  Initialise to +inf / -inf before the
+ *          first batch; pass them back unchanged to accumulate more batches.
+ * workspace  device buffer of fa3_calibrate_workspace_size(H) bytes, 256-byte
+ *          aligned, ZERO-FILLED before its first use.  Every successful call
+ *          leaves it zero-filled again, so it can be reused without clearing.
+ *          (After an FA3_ECUDA error, zero it again.)
+ * Results are exact: the same bits as the sorted definition above.
+ * ------------------------------------------------------------------------ */
+size_t fa3_calibrate_workspace_size(int H);
+
+int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L,
+                          int64_t stride_b, int64_t stride_h, double ratio,
+                          float* min_io, float* max_io,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Quantization parameters -- msModelSlim FA3量化, 原理 / 算法流程 step 4:
+ *   abs_max[h] = max(|min[h]|, |max[h]|);  scale[h] = abs_max[h] / 127
+ * (one IEEE float32 division).  min, max, scale: float[H].
+ * ------------------------------------------------------------------------ */
+int fa3_qparams(const float* min_v, const float* max_v, float* scale, int H, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Quantize-on-append -- the input_scale step of MindIE "FA3 quantization" /
+ * "Attention Quantization" (Overview): activations become INT8 codes
+ *   q = clamp(round_half_even(x / scale[h]), -127, 127)     (scale 0 -> 0)
+ * with x / scale one IEEE float32 division.
+ *
+ * kv       bf16 [B][T_new][H][D] new rows.
+ * scale    float[H].
+ * cache    int8 [B][T_max][H][D]; row t of sequence b goes to position
+ *          pos[b] + t.  Other rows are untouched.
+ * pos      int32[B] device array.  A sequence with pos[b] < 0 or
+ *          pos[b] + T_new > T_max is skipped and FA3_DEVERR_POS is set.
+ * rope_src, rope_cache, Dr  optional pass-through of the unquantized RoPE key
+ *          of MLA ("FA3 quantization", Overview: the RoPE part of K is not
+ *          quantized): bf16 [B][T_new][Dr] copied to bf16 [B][T_max][Dr] at
+ *          the same positions.  Pass NULL, NULL, 0 to skip.
+ * Also used to quantize a GQA query: T_new = T_max = 1 and pos = 0.
+ * ------------------------------------------------------------------------ */
+int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* cache, const int32_t* pos,
+                        int B, int T_new, int H, int D, int T_max,
+                        const uint16_t* rope_src, uint16_t* rope_cache, int Dr,
+                        int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Absorbed-MLA decode attention over an INT8 latent cache -- MindIE
+ * "FA3 quantization", Overview (non-RoPE K quantized to 8 bits per head,
+ * RoPE K left unquantized; decode-phase attention reads the INT8 cache),
+ * with the per-head scales of msModelSlim FA3量化 step 4.
+ *
+ * For every sequence b and head h (one decoded query token):
+ *   q8[h]   = quantize(q[b, h, 0:Dl], q_scale[h])          (the latent query)
+ *   acc[j]  = sum_c q8[h, c] * ckv[b, j, c]                 (exact integer)
+ *   s[j]    = (acc[j] * q_scale[h] * kv_scale[0] + q[b, h, Dl:] . krope[b, j, :])
+ *             * softmax_scale,                  j < lens[b]
+ *   out[b, h, :] = kv_scale[0] * sum_j softmax(s)_j * ckv[b, j, :]
+ *
+ * q        bf16 [B][H][Dl + Dr] (latent part first).
+ * ckv      int8 [B][T_max][Dl] latent cache (shared K-nope / V), one KV head.
+ * krope    bf16 [B][T_max][Dr] RoPE key.
+ * q_scale  float[H];  kv_scale float[1].
+ * lens     int32[B]; 0 gives a zero row; < 0 or > T_max sets FA3_DEVERR_LENS.
+ * out      float32 [B][H][Dl].
+ * Supported: H <= 128, Dl in {64, 128, ..., 512} (multiple of 64),
+ *            Dr a multiple of 16 up to 64, T_max >= 1; ckv/krope rows 16-byte
+ *            aligned (Dl % 16 == 0, Dr % 8 == 0).
+ * workspace  fa3_mla_workspace_size(B, H, Dl, T_max) bytes (split-K partials).
+ * ------------------------------------------------------------------------ */
+size_t fa3_mla_workspace_size(int B, int H, int Dl, int T_max);
+
+int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint16_t* krope,
+                        const float* q_scale, const float* kv_scale, const int32_t* lens,
+                        float* out, int B, int H, int Dl, int Dr, int T_max, float softmax_scale,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * GQA decode attention with INT8 q, k and v -- MindIE "Attention
+ * Quantization", Overview, and MindIE Turbo "Attention量化" (q, k, v all
+ * 8-bit; deq_scale brings the result back to floating point).
+ *
+ * Query head h reads KV head g = h / (Hq / Hkv):
+ *   s[j] = (q[b, h] . k[b, j, g]) * q_scale[h] * k_scale[g] * softmax_scale
+ *   out[b, h, :] = bf16( v_scale[g] * sum_j softmax(s)_j * v[b, j, g, :] ),  j < lens[b]
+ *
+ * q        int8 [B][Hq][D];  k, v  int8 [B][T_max][Hkv][D].
+ * q_scale  float[Hq];  k_scale, v_scale  float[Hkv].
+ * lens     int32[B] (as for MLA).   out  bf16 [B][Hq][D].
+ * Supported: D = 128, 1 <= Hq / Hkv <= 8; 16-byte aligned rows.
+ * workspace  fa3_gqa_workspace_size(B, Hq, Hkv, D, T_max) bytes.
+ * ------------------------------------------------------------------------ */
+size_t fa3_gqa_workspace_size(int B, int Hq, int Hkv, int D, int T_max);
+
+int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v,
+                        const float* q_scale, const float* k_scale, const float* v_scale,
+                        const int32_t* lens, uint16_t* out, int B, int Hq, int Hkv, int D, int T_max,
+                        float softmax_scale, void* workspace, size_t workspace_bytes,
+                        int32_t* dev_err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA3_H_ */

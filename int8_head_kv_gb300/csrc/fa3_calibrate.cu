@@ -1,0 +1,292 @@
+// Per-head Recall-Window calibration.
+//
+// msModelSlim "FA3量化" page, 原理 / 算法流程:
+//   step 1  every head collects its N = B*S*D activation values;
+//   step 2  sort them, target_num = int(ratio*N), and keep the narrowest window
+//           [sorted[i], sorted[i+target_num-1]] over i = 0 .. N - target_num;
+//   step 3  running min/max of the window ends across calibration batches.
+//
+// GB300 design.  bf16 has only 65536 bit patterns, and a monotone 16-bit key
+// maps them onto the total order of their values (-0 before +0).  Counting
+// each key (a counting sort) therefore carries the whole sorted sequence, so
+// one pass over HBM replaces the sort:
+//   kernel 1  per (head, 65528-value chunk): a 65536-bin histogram of 16-bit
+//             counters packed two per word in 128 KB of shared memory (a chunk
+//             is shorter than 65536, so no counter can overflow), then the
+//             non-zero bins are added into the per-head u32 table in the
+//             workspace.
+//   kernel 2  per head: prefix sums over the 65536 bins; a window can only be
+//             narrowest if it starts at the first copy of a value, so each
+//             occupied bin v with start position P(v) <= N - target_num is a
+//             candidate whose window ends in the bin holding position
+//             P(v) + target_num - 1.  Width in float64, argmin with ties to the
+//             smallest start, then the running min/max update.  The kernel
+//             zeroes the bins it read, leaving the workspace clean.
+#include "fa3_common.cuh"
+
+namespace fa3 {
+namespace {
+
+constexpr int kBins = 65536;
+constexpr int kHistThreads = 1024;
+constexpr int kChunk = 65528;                       // values per histogram CTA (multiple of 8, < 65536)
+constexpr int kGroupsPerThread = (kChunk / 8 + kHistThreads - 1) / kHistThreads;   // 8
+constexpr int kScalarPerThread = (kChunk + kHistThreads - 1) / kHistThreads;       // 64
+constexpr int kWinThreads = 1024;
+constexpr int kBinsPerThread = kBins / kWinThreads;  // 64
+
+// Order-preserving key of a bf16 bit pattern: positive values get the top bit
+// set, negative values are bit-inverted, so key order == value order and
+// -0.0 (0x8000) maps just below +0.0 (0x0000).
+__device__ __forceinline__ uint32_t bf16_key(uint32_t bits) {
+  return (bits & 0x8000u) ? (~bits & 0xffffu) : (bits | 0x8000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  uint32_t bits = (key & 0x8000u) ? (key ^ 0x8000u) : (~key & 0xffffu);
+  return __uint_as_float(bits << 16);
+}
+
+__device__ __forceinline__ void count_key(uint32_t* bins, uint32_t key) {
+  // Warps whose 32 lanes all hold the same key (constant heads) add once.
+  const uint32_t lane0 = __shfl_sync(0xffffffffu, key, 0);
+  const bool same = __all_sync(0xffffffffu, key == lane0);
+  const uint32_t inc = (key & 1u) ? 0x10000u : 1u;
+  if (same) {
+    if ((threadIdx.x & 31) == 0) atomicAdd(&bins[key >> 1], inc * 32u);
+  } else {
+    atomicAdd(&bins[key >> 1], inc);
+  }
+}
+
+__global__ void __launch_bounds__(kHistThreads, 1)
+hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t N,
+            uint32_t* __restrict__ counts, int vec) {
+  extern __shared__ uint4 smem_hist[];
+  uint32_t* bins = reinterpret_cast<uint32_t*>(smem_hist);   // 32768 words = 65536 16-bit bins
+  const int h = blockIdx.y;
+  const int64_t n0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t n1 = min(n0 + (int64_t)kChunk, N);
+  const uint16_t* xh = x + (int64_t)h * stride_h;
+  const int tid = threadIdx.x;
+
+  if (vec) {
+    // Issue every load of the chunk first; their latency hides the clearing below.
+    uint4 v[kGroupsPerThread];
+#pragma unroll
+    for (int k = 0; k < kGroupsPerThread; ++k) {
+      v[k] = make_uint4(0, 0, 0, 0);
+      const int64_t n = n0 + 8 * (int64_t)(tid + k * kHistThreads);
+      if (n < n1) {
+        const int64_t b = n / L, l = n - b * L;
+        v[k] = __ldcs(reinterpret_cast<const uint4*>(xh + b * stride_b + l));
+      }
+    }
+    for (int i = tid; i < kBins / 8; i += kHistThreads) smem_hist[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kGroupsPerThread; ++k) {
+      const int64_t n = n0 + 8 * (int64_t)(tid + k * kHistThreads);
+      // Uniform per warp except on the chunk's last partial warp; the warp vote
+      // in count_key needs all lanes, so invalid lanes count nothing but vote.
+      const bool valid = n < n1;
+      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t bits = (w[j >> 1] >> (16 * (j & 1))) & 0xffffu;
+        if (__all_sync(0xffffffffu, valid)) {
+          count_key(bins, bf16_key(bits));
+        } else if (valid) {
+          atomicAdd(&bins[bf16_key(bits) >> 1], (bf16_key(bits) & 1u) ? 0x10000u : 1u);
+        }
+      }
+    }
+  } else {
+    for (int i = tid; i < kBins / 8; i += kHistThreads) smem_hist[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    for (int k = 0; k < kScalarPerThread; ++k) {
+      const int64_t n = n0 + tid + (int64_t)k * kHistThreads;
+      if (n < n1) {
+        const int64_t b = n / L, l = n - b * L;
+        const uint32_t key = bf16_key(xh[b * stride_b + l]);
+        atomicAdd(&bins[key >> 1], (key & 1u) ? 0x10000u : 1u);
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t* ch = counts + (int64_t)h * kBins;
+  for (int i = tid; i < kBins / 8; i += kHistThreads) {
+    const uint4 q = smem_hist[i];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = w[j] & 0xffffu, hi = w[j] >> 16;
+      if (lo) atomicAdd(&ch[8 * i + 2 * j], lo);
+      if (hi) atomicAdd(&ch[8 * i + 2 * j + 1], hi);
+    }
+  }
+}
+
+struct Cand {
+  double width;
+  uint32_t lo_key;
+  uint32_t hi_key;
+};
+
+__device__ __forceinline__ bool cand_less(const Cand& a, const Cand& b) {
+  return a.width < b.width || (a.width == b.width && a.lo_key < b.lo_key);
+}
+
+__device__ __forceinline__ bool tot_less(float a, float b) {
+  return a < b || (a == b && signbit(a) && !signbit(b));
+}
+
+__global__ void __launch_bounds__(kWinThreads, 1)
+window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long long t,
+              float* __restrict__ min_io, float* __restrict__ max_io) {
+  __shared__ unsigned long long base_s[kWinThreads + 1];
+  __shared__ unsigned long long warp_tot[kWinThreads / 32];
+  __shared__ Cand warp_best[kWinThreads / 32];
+  const int h = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* ch = counts + (int64_t)h * kBins;
+
+  // 64 consecutive bins per thread (re-read later from L2 rather than held in registers).
+  const uint4* src = reinterpret_cast<const uint4*>(ch + tid * kBinsPerThread);
+  unsigned long long sum = 0;
+  uint32_t any = 0;
+#pragma unroll 4
+  for (int i = 0; i < kBinsPerThread / 4; ++i) {
+    const uint4 q = src[i];
+    sum += (unsigned long long)q.x + q.y + q.z + q.w;
+    any |= q.x | q.y | q.z | q.w;
+  }
+
+  // Block-wide exclusive scan of the per-thread sums.
+  unsigned long long incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long wv = warp_tot[lane];
+    unsigned long long wi = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_tot[lane] = wi - wv;                      // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  const unsigned long long base = warp_tot[warp] + incl - sum;
+  base_s[tid] = base;
+  if (tid == kWinThreads - 1) base_s[kWinThreads] = base + sum;
+  __syncthreads();
+
+  // Candidate windows starting in this thread's bins.
+  Cand best{__longlong_as_double(0x7ff0000000000000LL), 0xffffffffu, 0xffffffffu};
+  unsigned long long P = base;
+  if (any != 0 && base + t <= N) {
+    for (int i = 0; i < kBinsPerThread; ++i) {
+      const uint32_t cnt = ch[tid * kBinsPerThread + i];
+      if (cnt != 0 && P + t <= N) {
+        const unsigned long long e = P + t - 1;     // position of the window's last value
+        int lo_s = 0, hi_s = kWinThreads - 1;       // largest segment s with base_s[s] <= e
+        while (lo_s < hi_s) {
+          const int mid = (lo_s + hi_s + 1) >> 1;
+          if (base_s[mid] <= e) lo_s = mid; else hi_s = mid - 1;
+        }
+        unsigned long long pos = base_s[lo_s];
+        uint32_t end_bin = lo_s * kBinsPerThread + kBinsPerThread - 1;
+        for (int j = 0; j < kBinsPerThread; ++j) {
+          pos += ch[lo_s * kBinsPerThread + j];
+          if (e < pos) { end_bin = lo_s * kBinsPerThread + j; break; }
+        }
+        const uint32_t start_bin = tid * kBinsPerThread + i;
+        const double w = (double)key_value(end_bin) - (double)key_value(start_bin);
+        const Cand cand{w, start_bin, end_bin};
+        if (cand_less(cand, best)) best = cand;
+      }
+      P += cnt;
+    }
+  }
+
+  // Block argmin (width, then start key).
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Cand other;
+    other.width = __shfl_xor_sync(0xffffffffu, best.width, o);
+    other.lo_key = __shfl_xor_sync(0xffffffffu, best.lo_key, o);
+    other.hi_key = __shfl_xor_sync(0xffffffffu, best.hi_key, o);
+    if (cand_less(other, best)) best = other;
+  }
+  if (lane == 0) warp_best[warp] = best;
+  __syncthreads();                                  // also: every read of ch[] is done
+  if (warp == 0) {
+    best = warp_best[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Cand other;
+      other.width = __shfl_xor_sync(0xffffffffu, best.width, o);
+      other.lo_key = __shfl_xor_sync(0xffffffffu, best.lo_key, o);
+      other.hi_key = __shfl_xor_sync(0xffffffffu, best.hi_key, o);
+      if (cand_less(other, best)) best = other;
+    }
+    if (lane == 0 && best.lo_key != 0xffffffffu) {
+      const float lo = key_value(best.lo_key), hi = key_value(best.hi_key);
+      if (tot_less(lo, min_io[h])) min_io[h] = lo;
+      if (tot_less(max_io[h], hi)) max_io[h] = hi;
+    }
+  }
+  // Leave the workspace zero-filled for the next call (only occupied bins are written).
+  if (any != 0) {
+    uint4* dst = reinterpret_cast<uint4*>(ch + tid * kBinsPerThread);
+    for (int i = 0; i < kBinsPerThread / 4; ++i) {
+      const uint4 q = dst[i];
+      if (q.x | q.y | q.z | q.w) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace fa3
+
+using namespace fa3;
+
+FA3_API size_t fa3_calibrate_workspace_size(int H) {
+  return H > 0 ? (size_t)H * kBins * sizeof(uint32_t) : 0;
+}
+
+FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L, int64_t stride_b,
+                                  int64_t stride_h, double ratio, float* min_io, float* max_io,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !min_io || !max_io) return FA3_EINVAL;
+  if (B <= 0 || H <= 0 || L <= 0 || stride_b < 0 || stride_h < 0) return FA3_EINVAL;
+  if (!(ratio > 0.0 && ratio <= 1.0)) return FA3_EINVAL;
+  const int64_t N = B * L;
+  if (N <= 0 || N >= (int64_t)1 << 32 || L > ((int64_t)1 << 40) / B) return FA3_ERANGE;
+  if (H > 65535) return FA3_ERANGE;
+  if (!workspace || workspace_bytes < fa3_calibrate_workspace_size(H) || !aligned16(workspace))
+    return FA3_EWORKSPACE;
+  int st = check_device(nullptr);
+  if (st != FA3_OK) return st;
+  // FA3量化 step 2: target_num = int(ratio * N), float64 product, truncation; at least 1.
+  int64_t t = (int64_t)(ratio * (double)N);
+  if (t < 1) t = 1;
+  if (t > N) t = N;
+  const int vec = (L % 8 == 0) && aligned16(x) && (stride_b % 8 == 0) && (stride_h % 8 == 0);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int smem = kBins * 2;   // 128 KB of 16-bit bins
+  if (cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return FA3_ECUDA;
+  dim3 grid((unsigned)((N + kChunk - 1) / kChunk), (unsigned)H);
+  uint32_t* counts = static_cast<uint32_t*>(workspace);
+  hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, counts, vec);
+  if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
+  window_kernel<<<H, kWinThreads, 0, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io);
+  return cuda_status(cudaGetLastError());
+}

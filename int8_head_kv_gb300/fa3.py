@@ -1,0 +1,236 @@
+"""Thin Python binding of libfa3.so (the C ABI declared in include/fa3.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  If the
+library has not been built, every call raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+FA3_DEVERR_POS = 1
+FA3_DEVERR_LENS = 2
+FA3_DEVERR_TIMEOUT = 4
+
+
+class FA3Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {lib().fa3_status_string(status).decode()} (status {status})")
+        self.status = status
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+_D = ctypes.c_double
+
+_SIGS = {
+    "fa3_status_string": (ctypes.c_char_p, [_I]),
+    "fa3_version": (_I, []),
+    "fa3_calibrate_workspace_size": (_SZ, [_I]),
+    "fa3_calibrate_perhead": (_I, [_P, _I64, _I, _I64, _I64, _I64, _D, _P, _P, _P, _SZ, _P]),
+    "fa3_qparams": (_I, [_P, _P, _P, _I, _P]),
+    "fa3_quantize_append": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
+    "fa3_mla_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "fa3_decode_attn_mla": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
+    "fa3_gqa_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa3_decode_attn_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libfa3.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libfa3.so is not built ({path}); run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise FA3Error(fn, status)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor of dtype {dtype}")
+
+
+def _need_contig(t: torch.Tensor, dtype, name: str):
+    _need(t, dtype, name)
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_ws_cache = {}
+
+
+def _workspace(key, nbytes: int, device, zero: bool = False) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    k = (key, device.index if device.index is not None else torch.cuda.current_device())
+    ws = _ws_cache.get(k)
+    if ws is None or ws.numel() < nbytes:
+        ws = (torch.zeros if zero else torch.empty)(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[k] = ws
+    return ws
+
+
+# --------------------------------------------------------------------- calls
+def calibrate_workspace_size(H: int) -> int:
+    return int(lib().fa3_calibrate_workspace_size(H))
+
+
+def calibrate_perhead(x: torch.Tensor, ratio: float, min_io: torch.Tensor, max_io: torch.Tensor,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Per-head Recall-Window calibration of one batch; updates min_io/max_io in place.
+
+    x: bf16 (B, H, S, D) with (S, D) contiguous, or (H, N) with N contiguous.
+    """
+    _need(x, torch.bfloat16, "x")
+    _need_contig(min_io, torch.float32, "min_io")
+    _need_contig(max_io, torch.float32, "max_io")
+    if x.dim() == 4:
+        B, H, S, D = x.shape
+        if x.stride(3) != 1 or x.stride(2) != D:
+            raise ValueError("x must have contiguous (S, D) planes")
+        L, sb, sh = S * D, x.stride(0), x.stride(1)
+    elif x.dim() == 2:
+        H, L = x.shape
+        if x.stride(1) != 1:
+            raise ValueError("x rows must be contiguous")
+        B, sb, sh = 1, 0, x.stride(0)
+    else:
+        raise ValueError("x must be (B, H, S, D) or (H, N)")
+    if min_io.numel() != H or max_io.numel() != H:
+        raise ValueError("min_io/max_io must hold H values")
+    nbytes = calibrate_workspace_size(H)
+    if workspace is None:
+        workspace = _workspace("calib", nbytes, x.device, zero=True)
+    st = lib().fa3_calibrate_perhead(_ptr(x), B, H, L, sb, sh, float(ratio), _ptr(min_io), _ptr(max_io),
+                                     _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("fa3_calibrate_perhead", st)
+
+
+def qparams(min_v: torch.Tensor, max_v: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
+    _need_contig(min_v, torch.float32, "min")
+    _need_contig(max_v, torch.float32, "max")
+    H = min_v.numel()
+    if out is None:
+        out = torch.empty(H, dtype=torch.float32, device=min_v.device)
+    st = lib().fa3_qparams(_ptr(min_v), _ptr(max_v), _ptr(out), H, _stream(stream))
+    _check("fa3_qparams", st)
+    return out
+
+
+def quantize_append(kv: torch.Tensor, scale: torch.Tensor, cache: torch.Tensor, pos: torch.Tensor,
+                    rope_src: Optional[torch.Tensor] = None, rope_cache: Optional[torch.Tensor] = None,
+                    dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """kv bf16 [B][T_new][H][D] -> cache int8 [B][T_max][H][D] at pos[b]."""
+    _need_contig(kv, torch.bfloat16, "kv")
+    _need_contig(scale, torch.float32, "scale")
+    _need_contig(cache, torch.int8, "cache")
+    _need_contig(pos, torch.int32, "pos")
+    B, T_new, H, D = kv.shape
+    if cache.dim() != 4 or cache.shape[0] != B or cache.shape[2] != H or cache.shape[3] != D:
+        raise ValueError("cache must be [B][T_max][H][D]")
+    Dr = 0
+    if rope_src is not None:
+        _need_contig(rope_src, torch.bfloat16, "rope_src")
+        _need_contig(rope_cache, torch.bfloat16, "rope_cache")
+        Dr = rope_src.shape[-1]
+    st = lib().fa3_quantize_append(_ptr(kv), _ptr(scale), _ptr(cache), _ptr(pos), B, T_new, H, D, cache.shape[1],
+                                   _ptr(rope_src), _ptr(rope_cache), Dr, _ptr(dev_err), _stream(stream))
+    _check("fa3_quantize_append", st)
+
+
+def mla_workspace_size(B: int, H: int, Dl: int, T_max: int) -> int:
+    return int(lib().fa3_mla_workspace_size(B, H, Dl, T_max))
+
+
+def decode_attn_mla(q: torch.Tensor, ckv: torch.Tensor, krope: torch.Tensor, q_scale: torch.Tensor,
+                    kv_scale: torch.Tensor, lens: torch.Tensor, softmax_scale: float,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Absorbed-MLA decode: q bf16 [B][H][Dl+Dr], ckv int8 [B][T_max][Dl], krope bf16 [B][T_max][Dr]."""
+    _need_contig(q, torch.bfloat16, "q")
+    _need_contig(ckv, torch.int8, "ckv")
+    _need_contig(krope, torch.bfloat16, "krope")
+    _need_contig(q_scale, torch.float32, "q_scale")
+    _need_contig(kv_scale, torch.float32, "kv_scale")
+    _need_contig(lens, torch.int32, "lens")
+    B, H, Dqk = q.shape
+    T_max, Dl = ckv.shape[1], ckv.shape[2]
+    Dr = krope.shape[2]
+    if Dqk != Dl + Dr:
+        raise ValueError("q last dim must be Dl + Dr")
+    if out is None:
+        out = torch.empty(B, H, Dl, dtype=torch.float32, device=q.device)
+    nbytes = mla_workspace_size(B, H, Dl, T_max)
+    if workspace is None:
+        workspace = _workspace("mla", nbytes, q.device)
+    st = lib().fa3_decode_attn_mla(_ptr(q), _ptr(ckv), _ptr(krope), _ptr(q_scale), _ptr(kv_scale), _ptr(lens),
+                                   _ptr(out), B, H, Dl, Dr, T_max, float(softmax_scale), _ptr(workspace),
+                                   0 if workspace is None else workspace.numel(), _ptr(dev_err), _stream(stream))
+    _check("fa3_decode_attn_mla", st)
+    return out
+
+
+def gqa_workspace_size(B: int, Hq: int, Hkv: int, D: int, T_max: int) -> int:
+    return int(lib().fa3_gqa_workspace_size(B, Hq, Hkv, D, T_max))
+
+
+def decode_attn_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: torch.Tensor,
+                    k_scale: torch.Tensor, v_scale: torch.Tensor, lens: torch.Tensor, softmax_scale: float,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """GQA decode: q int8 [B][Hq][D], k/v int8 [B][T_max][Hkv][D] -> bf16 [B][Hq][D]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need_contig(t, torch.int8, n)
+    for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need_contig(t, torch.float32, n)
+    _need_contig(lens, torch.int32, "lens")
+    B, Hq, D = q.shape
+    T_max, Hkv = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=q.device)
+    nbytes = gqa_workspace_size(B, Hq, Hkv, D, T_max)
+    if workspace is None:
+        workspace = _workspace("gqa", nbytes, q.device)
+    st = lib().fa3_decode_attn_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                   _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_max, float(softmax_scale),
+                                   _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                                   _ptr(dev_err), _stream(stream))
+    _check("fa3_decode_attn_gqa", st)
+    return out

@@ -1,0 +1,77 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every declared symbol,
+and its host-side validation rejects bad arguments before touching a GPU."""
+import ctypes
+
+import pytest
+
+from helpers import fa3, header_functions
+
+EINVAL, ERANGE, EWORKSPACE = 1, 2, 4
+FAKE = ctypes.c_void_p(4096)   # never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def L():
+    return fa3().lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    assert L.fa3_version() == 100
+    for s in range(6):
+        assert L.fa3_status_string(s).startswith(b"FA3")
+
+
+def test_calibrate_validation(L):
+    ws = L.fa3_calibrate_workspace_size(4)
+    assert ws == 4 * 65536 * 4
+    args = lambda **k: dict(dict(x=FAKE, B=2, H=4, L=64, sb=256, sh=64, ratio=0.9999, mn=FAKE, mx=FAKE,
+                                 ws=FAKE, wsb=ws), **k)
+    call = lambda a: L.fa3_calibrate_perhead(a["x"], a["B"], a["H"], a["L"], a["sb"], a["sh"], a["ratio"],
+                                             a["mn"], a["mx"], a["ws"], a["wsb"], None)
+    assert call(args(x=None)) == EINVAL
+    assert call(args(mn=None)) == EINVAL
+    for r in (0.0, -1.0, 1.5, float("nan")):
+        assert call(args(ratio=r)) == EINVAL
+    assert call(args(B=0)) == EINVAL
+    assert call(args(L=1 << 31, B=4)) == ERANGE        # N >= 2^32
+    assert call(args(wsb=ws - 1)) == EWORKSPACE
+    assert call(args(ws=None)) == EWORKSPACE
+
+
+def test_qparams_and_append_validation(L):
+    assert L.fa3_qparams(None, FAKE, FAKE, 4, None) == EINVAL
+    assert L.fa3_qparams(FAKE, FAKE, FAKE, 0, None) == EINVAL
+    q = lambda **k: L.fa3_quantize_append(k.get("kv", FAKE), FAKE, FAKE, FAKE, k.get("B", 2), k.get("T_new", 4), 1,
+                                          512, k.get("T_max", 16), k.get("rs", None), k.get("rc", None),
+                                          k.get("Dr", 0), None, None)
+    assert q(kv=None) == EINVAL
+    assert q(T_new=17) == EINVAL
+    assert q(rs=FAKE) == EINVAL                         # source without destination
+    assert q(rs=FAKE, rc=FAKE, Dr=0) == EINVAL
+
+
+def test_mla_validation(L):
+    call = lambda H=128, Dl=512, Dr=64, q=FAKE, sc=0.07: L.fa3_decode_attn_mla(
+        q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, H, Dl, Dr, 64, sc, FAKE, 1 << 30, None, None)
+    assert call(q=None) == EINVAL
+    assert call(sc=0.0) == EINVAL
+    assert call(H=129) == ERANGE
+    assert call(Dl=96) == ERANGE
+    assert call(Dr=24) == ERANGE
+    assert call(Dr=80) == ERANGE
+
+
+def test_gqa_validation(L):
+    call = lambda Hq=64, Hkv=8, D=128, k=FAKE: L.fa3_decode_attn_gqa(
+        FAKE, k, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, Hq, Hkv, D, 64, 0.09, FAKE, 1 << 30, None, None)
+    assert call(k=None) == EINVAL
+    assert call(Hq=60) == EINVAL          # not a multiple of Hkv
+    assert call(D=64) == ERANGE
+    assert call(Hq=128, Hkv=8) == ERANGE  # 16 query heads per KV head

@@ -1,0 +1,76 @@
+"""GPU parity of GQA decode attention (INT8 q/k/v, bf16 output) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from helpers import assert_attn_close, fa3
+from oracle import fa3_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(w, lens=None):
+    inp = W.gqa_inputs(w)
+    qs = O.qparams(*O.calibrate(inp.calib_q, w.ratio))
+    ks = O.qparams(*O.calibrate(inp.calib_k, w.ratio))
+    vs = O.qparams(*O.calibrate(inp.calib_v, w.ratio))
+    q8 = O.quantize(inp.q, qs[None, :, None])
+    k8 = O.quantize(inp.k, ks[None, None, :, None])
+    v8 = O.quantize(inp.v, vs[None, None, :, None])
+    lens = inp.lens if lens is None else np.asarray(lens, np.int32)
+    return inp, (q8, k8, v8, qs, ks, vs, lens)
+
+
+def _run(F, w, args, err=None):
+    q8, k8, v8, qs, ks, vs, lens = args
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = F.decode_attn_gqa(t(q8), t(k8), t(v8), t(qs), t(ks), t(vs), t(lens), w.softmax_scale, dev_err=err)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+def test_ragged_small():
+    F = fa3()
+    w = W.gqa_llama70b(B=4, T=300)
+    inp, args = _case(w, lens=[1, 37, 300, 129])
+    got = _run(F, w, args)
+    ref = O.gqa_decode(*args[:6], args[6], w.softmax_scale)
+    assert_attn_close(got, ref, bf16_out=True, what="gqa ragged")
+
+
+def test_edge_lengths_and_errors():
+    F = fa3()
+    w = W.gqa_llama70b(B=5, T=96)
+    inp, args = _case(w, lens=[0, 16, 15, 17, 96])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run(F, w, args, err)
+    ref = O.gqa_decode(*args[:6], args[6], w.softmax_scale)
+    assert_attn_close(got, ref, bf16_out=True, what="gqa edges")
+    assert np.all(got[0] == 0) and int(err.item()) == 0
+    bad = list(args)
+    bad[6] = np.array([97, 16, -1, 17, 96], np.int32)
+    got = _run(F, w, bad, err)
+    assert int(err.item()) & F.FA3_DEVERR_LENS
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+
+
+def test_fewer_query_heads_per_group():
+    F = fa3()
+    w = W.gqa_llama70b(B=2, T=200)
+    w.Hq, w.Hkv = 12, 4                   # 3 query heads per KV head
+    inp, args = _case(w, lens=[200, 77])
+    got = _run(F, w, args)
+    ref = O.gqa_decode(*args[:6], args[6], w.softmax_scale)
+    assert_attn_close(got, ref, bf16_out=True, what="gqa G=3")
+
+
+@pytest.mark.slow
+def test_llama70b_full_size():
+    F = fa3()
+    w = W.gqa_llama70b()
+    inp, args = _case(w)
+    got = _run(F, w, args)
+    ref = O.gqa_decode(*args[:6], args[6], w.softmax_scale)
+    max_abs, rrms = assert_attn_close(got, ref, bf16_out=True, what="gqa llama70b")
+    print(f"gqa full: max_abs(after bf16 slack)={max_abs:.3e} rel_rms={rrms:.3e}")

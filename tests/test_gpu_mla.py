@@ -1,0 +1,100 @@
+"""GPU parity of absorbed-MLA decode attention (INT8 latent, bf16 RoPE key) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from helpers import assert_attn_close, bf16_dev, fa3
+from oracle import fa3_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _prepare(w, lens=None):
+    inp = W.mla_inputs(w)
+    q_scale = O.qparams(*O.calibrate(inp.calib_q, w.ratio))
+    if q_scale.size != w.H:                       # calibration head count == query heads
+        raise AssertionError("calibration heads")
+    kv_scale = O.qparams(*O.calibrate(inp.calib_kv, w.ratio))
+    ckv8 = O.quantize(inp.ckv, kv_scale[0])
+    lens = inp.lens if lens is None else np.asarray(lens, np.int32)
+    return inp, q_scale, kv_scale, ckv8, lens
+
+
+def _run(F, w, inp, q_scale, kv_scale, ckv8, lens, err=None):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = F.decode_attn_mla(bf16_dev(inp.q), t(ckv8), bf16_dev(inp.krope), t(q_scale), t(kv_scale), t(lens),
+                            w.softmax_scale, dev_err=err)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _oracle(w, inp, q_scale, kv_scale, ckv8, lens, rows=None):
+    return O.mla_decode(inp.q, ckv8, inp.krope, q_scale, float(kv_scale[0]), lens, w.softmax_scale, rows=rows)
+
+
+def test_tiny_mla_full():
+    F = fa3()
+    w = W.mla_tiny()
+    args = _prepare(w)
+    got = _run(F, w, *args)
+    ref = _oracle(w, *args)
+    assert_attn_close(got, ref, what="tiny mla")
+
+
+def test_dsv3_shape_ragged():
+    F = fa3()
+    w = W.mla_dsv3(B=3, T=700)
+    args = _prepare(w, lens=[700, 333, 64])
+    got = _run(F, w, *args)
+    ref = _oracle(w, *args)
+    assert_attn_close(got, ref, what="dsv3 ragged")
+
+
+def test_edge_lengths_errors_and_small_shapes():
+    F = fa3()
+    w = W.mla_dsv3(B=6, T=130)
+    args = list(_prepare(w, lens=[0, 1, 63, 64, 65, 130]))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run(F, w, *args, err=err)
+    assert_attn_close(got, _oracle(w, *args), what="mla edges")
+    assert np.all(got[0] == 0) and int(err.item()) == 0
+    args[4] = np.array([131, 1, -5, 64, 65, 130], np.int32)
+    got = _run(F, w, *args, err=err)
+    assert int(err.item()) & F.FA3_DEVERR_LENS
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    # fewer heads, narrower latent, no RoPE
+    w2 = W.MLAWorkload(name="h16 dl128 dr0", B=2, H=16, Dl=128, Dr=0, T_max=300, softmax_scale=0.1, lens=[300, 200],
+                       calib_q_shape=(2, 16, 16, 128), calib_kv_shape=(1, 1, 256, 128))
+    a2 = _prepare(w2)
+    assert_attn_close(_run(F, w2, *a2), _oracle(w2, *a2), what="h16 dl128 dr0")
+    w3 = W.MLAWorkload(name="h128 dl256 dr32", B=2, H=128, Dl=256, Dr=32, T_max=200, softmax_scale=0.1,
+                       lens=[200, 129], calib_q_shape=(2, 128, 4, 256), calib_kv_shape=(1, 1, 256, 256))
+    a3 = _prepare(w3)
+    assert_attn_close(_run(F, w3, *a3), _oracle(w3, *a3), what="h128 dl256 dr32")
+
+
+@pytest.mark.slow
+def test_dsv3_full_size_sampled_rows():
+    F = fa3()
+    w = W.mla_dsv3()
+    args = _prepare(w)
+    got = _run(F, w, *args)
+    rng = np.random.default_rng(0)
+    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, w.B, 24), rng.integers(0, w.H, 24))]
+    ref = _oracle(w, *args, rows=rows)
+    bi = np.array([r[0] for r in rows]); hi = np.array([r[1] for r in rows])
+    max_abs, rrms = assert_attn_close(got[bi, hi], ref[bi, hi], what="dsv3 full sampled")
+    print(f"mla dsv3 full: max_abs={max_abs:.3e} rel_rms={rrms:.3e}")
+
+
+@pytest.mark.slow
+def test_long_context_variable_lengths_sampled_rows():
+    F = fa3()
+    w = W.mla_long()
+    args = _prepare(w)
+    got = _run(F, w, *args)
+    rows = [(b, h) for b in range(w.B) for h in (0, 77)]
+    ref = _oracle(w, *args, rows=rows)
+    bi = np.array([r[0] for r in rows]); hi = np.array([r[1] for r in rows])
+    assert_attn_close(got[bi, hi], ref[bi, hi], what="long mla sampled")
