@@ -79,7 +79,7 @@ constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;   // u32 TMEM base addres
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;         // u32 abort flag
 constexpr uint32_t OFF_SCHED = OFF_TMEM_SLOT + 8;         // 4 x int64: b_first, pre_first, x0, x1
 
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: normal waits last microseconds
 
 struct MlaParams {
   CUtensorMap tm_ckv;    // int8 [B][T_max][Dl], box {min(Dl/2,128), 64, 1}
@@ -169,7 +169,8 @@ __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* tm, int 
 }
 
 // Shared-memory matrix descriptor, no swizzle: core matrices of 8 rows x 16 bytes.
-// lbo / sbo: byte distances between core matrices along the leading / strided dimension.
+// K-major operand: lbo = byte stride between core matrices along K, sbo = along M/N.
+// MN-major operand: lbo = along K, sbo = along M/N as well (8-element MN groups).
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
@@ -228,17 +229,30 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
 }
 
-// Bounded wait: gives up after kWaitLimit polls or when another role aborted.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after kWaitNs nanoseconds of wall-clock time, or as
+// soon as another role of this CTA has given up.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                          int32_t* err, bool cluster_scope = false) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+  if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
     if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-    if ((it & 63u) == 63u && *abort_flag) return false;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitNs) break;
   }
   *abort_flag = 1u;
   set_dev_err(err, FA3_DEVERR_TIMEOUT);
   return false;
 }
+
+// Softmax warps run tcgen05.ld/st (warp-collective): keep their control flow warp-uniform.
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
 __device__ __forceinline__ int seq_tiles(const MlaParams& p, int b) {
   const int len = p.lens[b];
@@ -445,7 +459,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 #pragma unroll
         for (int kk = 0; kk < kTok / 16; ++kk) {
           const uint64_t a = sdesc(sbase + OFF_P + kk * 4096, 2048, 128);
-          const uint64_t bd = sdesc(sbase + OFF_C16 + cs * C16_BYTES + kk * 256, 1024, 128);
+          // MN-major, no swizzle: LBO strides the K (token) core groups, SBO the N (latent) ones.
+          const uint64_t bd = sdesc(sbase + OFF_C16 + cs * C16_BYTES + kk * 256, 128, 1024);
           mma_f16(tmem + TM_O, a, bd, id_pv, (first && kk == 0) ? 0u : 1u);
         }
         mma_commit(bar(B_PV_DONE));
@@ -533,7 +548,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       for (int tt = lo; tt < hi && ok; ++tt, ++it) {
         const uint32_t s = it & 1u, ph = (it >> 1) & 1u;
         const int nvalid = min(kTok, len - tt * kTok);
-        ok = wait_bar(bar(B_S_FULL + s), ph, abort_flag, p.err);
+        ok = warp_all(wait_bar(bar(B_S_FULL + s), ph, abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
         float part[64];
@@ -557,7 +572,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         mbar_arrive(bar(B_S_EMPTY + s));
 
         // ---- swap partial scores with the peer CTA
-        ok = wait_bar(bar(B_XE), (it & 1u) ^ 1u, abort_flag, p.err, true);
+        ok = warp_all(wait_bar(bar(B_XE), (it & 1u) ^ 1u, abort_flag, p.err, true));
         if (!ok) break;
 #pragma unroll
         for (int j4 = 0; j4 < 16; ++j4) {
@@ -566,7 +581,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                        "f"(part[4 * j4 + 1]), "f"(part[4 * j4 + 2]), "f"(part[4 * j4 + 3]) : "memory");
         }
         mbar_arrive_remote(peer_xf);
-        ok = wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true);
+        ok = warp_all(wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true));
         if (!ok) break;
         float mt = -CUDART_INF_F;
 #pragma unroll
@@ -602,10 +617,13 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         l = l * alpha + psum;
         if (tt > lo) {
           // P is single-buffered and O must hold P.C of the previous tile.
-          ok = wait_bar(bar(B_PV_DONE), (it - 1) & 1u, abort_flag, p.err);
+          ok = warp_all(wait_bar(bar(B_PV_DONE), (it - 1) & 1u, abort_flag, p.err));
           if (!ok) break;
           tc_fence_after();
-          if (rescale) {
+          // The rescale is decided per head (lane) but tcgen05.ld/st are warp-wide:
+          // the whole warp takes part, lanes that keep their reference scale by 1.
+          if (__any_sync(0xffffffffu, rescale)) {
+            if (!rescale) alpha = 1.f;
             for (int c0 = 0; c0 < DH; c0 += 32) {
               uint32_t v[32];
               FA3_TMEM_LD32(tmem + lane_base + TM_O + c0, v);
@@ -627,7 +645,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       }
       if (!ok) break;
       // ---- segment done: wait for the last P.C, then write the output (or a partial)
-      ok = wait_bar(bar(B_PV_DONE), (it - 1) & 1u, abort_flag, p.err);
+      ok = warp_all(wait_bar(bar(B_PV_DONE), (it - 1) & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
       const bool full = (lo == 0 && hi == tb);
@@ -696,10 +714,15 @@ __global__ void mla_combine_kernel(const MlaParams p, int64_t total_tiles_unused
   };
   const int c0 = owner(pre), c1 = owner(pre + tb - 1);
   if (c0 == c1) return;   // one cluster held the whole sequence and wrote it already
+  // Clusters between the two owners hold a segment of this sequence unless their
+  // range is empty (fewer tiles than clusters); empty ones wrote nothing.
+  auto holds = [&](int c) { return total * c / C < total * (c + 1) / C; };
   float M = -CUDART_INF_F;
-  for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.part_ml[(int64_t)(b + c) * kRows + h].x);
+  for (int c = c0; c <= c1; ++c)
+    if (holds(c)) M = fmaxf(M, p.part_ml[(int64_t)(b + c) * kRows + h].x);
   float L = 0.f;
   for (int c = c0; c <= c1; ++c) {
+    if (!holds(c)) continue;
     const float2 ml = p.part_ml[(int64_t)(b + c) * kRows + h];
     L += ml.y * exp2f(ml.x - M);
   }
@@ -708,6 +731,7 @@ __global__ void mla_combine_kernel(const MlaParams p, int64_t total_tiles_unused
     const int r = d / p.DH, dd = d - r * p.DH;
     float O = 0.f;
     for (int c = c0; c <= c1; ++c) {
+      if (!holds(c)) continue;
       const int64_t slot = b + c;
       O += p.part_o[((slot * 2 + r) * kRows + h) * p.DH + dd] * exp2f(p.part_ml[slot * kRows + h].x - M);
     }

@@ -98,3 +98,41 @@ def test_long_context_variable_lengths_sampled_rows():
     ref = _oracle(w, *args, rows=rows)
     bi = np.array([r[0] for r in rows]); hi = np.array([r[1] for r in rows])
     assert_attn_close(got[bi, hi], ref[bi, hi], what="long mla sampled")
+
+
+def test_poisoned_workspace_few_tiles():
+    # Fewer tiles than clusters: some clusters own nothing and must not be read back.
+    F = fa3()
+    w = W.mla_dsv3(B=2, T=256)
+    inp, q_scale, kv_scale, ckv8, lens = _prepare(w, lens=[256, 128])
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    ws = torch.full((F.mla_workspace_size(w.B, w.H, w.Dl, w.T_max),), 0xFF, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        out = F.decode_attn_mla(bf16_dev(inp.q), t(ckv8), bf16_dev(inp.krope), t(q_scale), t(kv_scale), t(lens),
+                                w.softmax_scale, workspace=ws)
+        assert_attn_close(out.cpu().numpy(), _oracle(w, inp, q_scale, kv_scale, ckv8, lens), what="poisoned ws")
+
+
+def test_multi_tile_segments():
+    # 256 tiles: every cluster walks several tiles, crosses a sequence boundary and
+    # hands split sequences to the combine kernel.
+    F = fa3()
+    w = W.mla_dsv3(B=2, T=8192)
+    args = _prepare(w, lens=[8192, 5000])
+    got = _run(F, w, *args)
+    assert_attn_close(got, _oracle(w, *args), what="multi-tile")
+
+
+def test_forced_rescales():
+    # RoPE keys aligned with each head's RoPE query and growing along the context:
+    # the running maximum jumps by more than the lazy-rescale threshold tile after tile.
+    F = fa3()
+    w = W.mla_dsv3(B=2, T=4096)
+    inp, q_scale, kv_scale, ckv8, lens = _prepare(w, lens=[4096, 3000])
+    qr = inp.q[:, :, w.Dl:]
+    ramp = (np.arange(w.T_max, dtype=np.float32) / 64.0) * 150.0          # about +10 (log2) per tile
+    k = qr.mean(axis=1, keepdims=True) / (np.linalg.norm(qr.mean(axis=1), axis=-1)[:, None, None] + 1e-6)
+    krope = W.bf16_round((k * ramp[None, :, None] + inp.krope * 0.1).astype(np.float32))
+    inp.krope = krope
+    got = _run(F, w, inp, q_scale, kv_scale, ckv8, lens)
+    assert_attn_close(got, _oracle(w, inp, q_scale, kv_scale, ckv8, lens), what="forced rescales")
