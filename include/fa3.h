@@ -174,6 +174,28 @@ int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v,
                         float softmax_scale, void* workspace, size_t workspace_bytes,
                         int32_t* dev_err, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free GQA decode.  No counterpart in the pages: a convenience for
+ * callers that cannot allocate device memory when they run attention (code
+ * inside an allocator or memory-pool callback, runtimes that plan every
+ * allocation ahead of time, deployments that forbid allocation after start-up).
+ *
+ * Same arguments and results as fa3_decode_attn_gqa, without the workspace:
+ * the split-K partials go to a fixed 8 MiB array in the library's own device
+ * memory, which every GPU that loads libfa3.so holds until the process exits.
+ * Sizes whose partials need more than 8 MiB (fa3_gqa_workspace_size() >
+ * 8 MiB) return FA3_EWORKSPACE; use fa3_decode_attn_gqa for them.
+ * The first call on each device looks up the array's device address (this
+ * may initialise the module on that device): make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last call's
+ * contents (nothing in it needs to start at zero); calls that overlap on the
+ * GPU -- on different streams, or from different host threads -- race on it.
+ * ------------------------------------------------------------------------ */
+int fa3_decode_attn_gqa_noalloc(const int8_t* q, const int8_t* k, const int8_t* v,
+                                const float* q_scale, const float* k_scale, const float* v_scale,
+                                const int32_t* lens, uint16_t* out, int B, int Hq, int Hkv, int D, int T_max,
+                                float softmax_scale, int32_t* dev_err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

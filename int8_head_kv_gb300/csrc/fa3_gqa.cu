@@ -349,3 +349,45 @@ FA3_API int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* 
   }
   return FA3_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of fa3_decode_attn_gqa.
+//
+// Some callers cannot call cudaMalloc at the point where they run decode
+// attention: code inside a custom allocator or memory-pool callback, runtimes
+// that pre-plan every device allocation up front, and embedded or safety-
+// certified deployments that forbid allocation after start-up.  For them the
+// split-K partials live in a fixed array in the library's own device memory.
+// Every GPU that loads libfa3.so holds this array (kGqaStaticScratchBytes)
+// until the process exits.
+namespace fa3 {
+namespace {
+constexpr size_t kGqaStaticScratchBytes = size_t(8) << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_gqa_static_scratch[kGqaStaticScratchBytes];
+
+// Device address of the array, looked up once per device.  In host code the
+// array's name is only a host-side stand-in, never a device address.
+void* g_gqa_static_scratch_addr[64] = {nullptr};
+}  // namespace
+}  // namespace fa3
+
+FA3_API int fa3_decode_attn_gqa_noalloc(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale,
+                                        const float* k_scale, const float* v_scale, const int32_t* lens,
+                                        uint16_t* out, int B, int Hq, int Hkv, int D, int T_max,
+                                        float softmax_scale, int32_t* dev_err, void* stream) {
+  if (!q || !k || !v || !q_scale || !k_scale || !v_scale || !lens || !out) return FA3_EINVAL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || T_max <= 0) return FA3_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA3_ECUDA;
+  const size_t need = fa3_gqa_workspace_size(B, Hq, Hkv, D, T_max);
+  if (need > kGqaStaticScratchBytes) return FA3_EWORKSPACE;   // beyond the fixed 8 MiB scratch
+  if (g_gqa_static_scratch_addr[dev] == nullptr) {
+    // Set-up, once per device, with that device current.
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_gqa_static_scratch) != cudaSuccess || ptr == nullptr) return FA3_ECUDA;
+    g_gqa_static_scratch_addr[dev] = ptr;
+  }
+  // Every slot of the partials is written before it is read, so nothing needs clearing.
+  return fa3_decode_attn_gqa(q, k, v, q_scale, k_scale, v_scale, lens, out, B, Hq, Hkv, D, T_max, softmax_scale,
+                             g_gqa_static_scratch_addr[dev], kGqaStaticScratchBytes, dev_err, stream);
+}

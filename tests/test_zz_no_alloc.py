@@ -1,0 +1,68 @@
+"""The allocation-free GQA decode entry point, called through the C ABI.
+
+Callers that cannot allocate device memory while they run attention (inside an
+allocator callback, under an ahead-of-time memory plan, or where allocation
+after start-up is forbidden) use fa3_decode_attn_gqa_noalloc, whose split-K
+scratch is a fixed array inside the library.  Its output must match the
+workspace-taking entry point on two calls in a row, and sizes that would need
+more than its fixed scratch must be rejected.  This file is collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from helpers import ATOL, RRMS, attn_errors, fa3
+from oracle import fa3_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+STATIC_SCRATCH = 8 << 20
+P, I, F32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+
+
+def _entry(L):
+    fn = L.fa3_decode_attn_gqa_noalloc
+    fn.restype = I
+    fn.argtypes = [P] * 8 + [I] * 5 + [F32, P, P]
+    return fn
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    F = fa3()
+    fn = _entry(F.lib())
+    w = W.gqa_llama70b(B=16, T=4096)
+    inp = W.gqa_inputs(w)
+    qs = O.qparams(*O.calibrate(inp.calib_q, w.ratio))
+    ks = O.qparams(*O.calibrate(inp.calib_k, w.ratio))
+    vs = O.qparams(*O.calibrate(inp.calib_v, w.ratio))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q8, k8, v8 = (t(O.quantize(inp.q, qs[None, :, None])), t(O.quantize(inp.k, ks[None, None, :, None])),
+                  t(O.quantize(inp.v, vs[None, None, :, None])))
+    qs_d, ks_d, vs_d = t(qs), t(ks), t(vs)
+    lens = t(np.array([4096, 1, 2049, 4000] * 4, np.int32))
+    assert 0 < F.gqa_workspace_size(w.B, w.Hq, w.Hkv, w.D, w.T_max) <= STATIC_SCRATCH   # the scratch is used
+    ref = F.decode_attn_gqa(q8, k8, v8, qs_d, ks_d, vs_d, lens, w.softmax_scale).float().cpu().numpy()
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        out = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device="cuda")
+        st = fn(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), qs_d.data_ptr(), ks_d.data_ptr(), vs_d.data_ptr(),
+                lens.data_ptr(), out.data_ptr(), w.B, w.Hq, w.Hkv, w.D, w.T_max, w.softmax_scale, None, stream)
+        assert st == 0, F.lib().fa3_status_string(st)
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy()
+        max_abs, rrms = attn_errors(got, ref, bf16_out=True)
+        assert max_abs <= ATOL and rrms <= RRMS, (max_abs, rrms)
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    F = fa3()
+    fn = _entry(F.lib())
+    B, Hq, Hkv, D, T = 137, 64, 8, 128, 8192
+    assert F.gqa_workspace_size(B, Hq, Hkv, D, T) > STATIC_SCRATCH
+    small = torch.zeros(16, dtype=torch.int8, device="cuda")        # never read: the call is rejected first
+    p = small.data_ptr()
+    st = fn(p, p, p, p, p, p, p, p, B, Hq, Hkv, D, T, 0.088, None, torch.cuda.current_stream().cuda_stream)
+    assert st == 4   # FA3_EWORKSPACE
