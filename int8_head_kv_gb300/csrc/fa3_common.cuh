@@ -29,6 +29,32 @@ __device__ __forceinline__ int quant_code(float x, float s) {
   return __float2int_rn(r);
 }
 
+// Approximate reciprocal (hardware rcp, flush-to-zero); only used to pick codes
+// where the decision cannot differ from the IEEE quotient's (see quant_code_fast).
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
+// Same code as quant_code(x, s), without a division in the common case.  With
+// rs = rcp_approx(s), y = x * rs is within 2.2e-4 of the correctly rounded
+// quotient whenever |x / s| < 200 (rcp error <= 2^-20, two roundings), so when y
+// is farther than 1e-3 from every half-integer its round-half-even is the
+// quotient's; beyond 127.01 both clamp to +-127.  Everything else (ties,
+// overflow, subnormal scales) takes the IEEE division.
+__device__ __forceinline__ int quant_code_fast(float x, float s, float rs) {
+  if (s == 0.0f) return 0;
+  const float y = x * rs;
+  const float a = fabsf(y);
+  if (a < 127.0f) {
+    if (fabsf(a - floorf(a) - 0.5f) >= 1e-3f) return __float2int_rn(y);
+  } else if (a >= 127.01f && a <= 3.0e38f) {
+    return y > 0.0f ? 127 : -127;
+  }
+  return quant_code(x, s);
+}
+
 __device__ __forceinline__ void set_dev_err(int32_t* err, int bit) {
   if (err) atomicOr(reinterpret_cast<int*>(err), bit);
 }

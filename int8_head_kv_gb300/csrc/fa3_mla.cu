@@ -53,6 +53,10 @@ constexpr int kRows = 128;        // heads (TMEM lanes)
 // Shared memory map (bytes from a 1024-byte aligned base).
 constexpr uint32_t OFF_Q = 0;             // fp16 latent query half, K-major core matrices (<= 64 KB)
 constexpr uint32_t OFF_QR = 65536;        // bf16 RoPE query half (<= 8 KB)
+// The query of every (sequence, latent half) is prepared once per call by
+// mla_prepare_q_kernel as an exact image of [OFF_Q, OFF_QR + 8 KB) and fetched
+// per segment with one bulk copy.
+constexpr uint32_t QIMG_BYTES = 65536 + 8192;
 constexpr uint32_t OFF_C16 = 73728;       // 2 x fp16 latent tile (<= 32 KB each)
 constexpr uint32_t C16_BYTES = 32768;
 constexpr uint32_t OFF_STG = 139264;      // 2 x int8 TMA staging tile (<= 16 KB each)
@@ -62,6 +66,7 @@ constexpr uint32_t ROPE_BYTES = 4096;
 constexpr uint32_t OFF_P = 180224;        // fp16 P, 128 x 64 (16 KB)
 constexpr uint32_t OFF_X = 196608;        // fp32 partial scores from the peer, 128 x 64 (32 KB)
 constexpr uint32_t OFF_BAR = 229376;
+constexpr uint32_t kXBytes = 128 * 64 * 4;   // one tile of fp32 partial scores, all heads
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
 
 // TMEM columns.
@@ -72,8 +77,8 @@ constexpr uint32_t TM_R = 384;    // 2 x 64 RoPE-score buffers
 // Barrier slots (8 bytes each) at OFF_BAR.
 enum {
   B_TILE_FULL = 0, B_STG_EMPTY = 2, B_ROPE_EMPTY = 4, B_C16_FULL = 6, B_C16_EMPTY = 8,
-  B_S_FULL = 10, B_S_EMPTY = 12, B_P_FULL = 14, B_PV_DONE = 15, B_Q_READY = 16,
-  B_XF = 17, B_XE = 18, B_DRAIN = 19, NBAR = 20
+  B_S_FULL = 10, B_S_EMPTY = 12, B_P_FULL = 14, B_PV_DONE = 15, B_Q_FULL = 16,
+  B_XF = 17, B_XE = 18, B_DRAIN = 19, B_QK_DONE = 20, NBAR = 21
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;   // u32 TMEM base address
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;         // u32 abort flag
@@ -91,6 +96,7 @@ struct MlaParams {
   float* out;
   float* part_o;         // [slot][2][128][Dl/2]
   float2* part_ml;       // [slot][128]
+  const uint8_t* q_img;  // [B][2][QIMG_BYTES] query images (fp16 latent codes, bf16 RoPE)
   int32_t* err;
   int B, H, Dl, Dr, T_max;
   int DH;                // Dl / 2
@@ -132,6 +138,16 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t a, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok) : "r"(a), "r"(parity) : "memory");
   return ok != 0;
+}
+// Asynchronous remote store; its bytes complete_tx on the destination CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(raddr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar) : "memory");
+}
+// Bulk asynchronous copy global -> this CTA's shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
 }
 __device__ __forceinline__ uint32_t mapa(uint32_t a, uint32_t rank) {
   uint32_t r;
@@ -280,8 +296,16 @@ struct SegWalk {
   }
 };
 
+template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ MlaParams p) {
+  // Compile-time geometry of this CTA's latent half.
+  constexpr int BOX_W = DH < 128 ? DH : 128;        // bytes per TMA box row (<= the 128-byte swizzle span)
+  constexpr int N_BOX = DH / BOX_W;
+  constexpr int CPB = BOX_W / 16;                   // 16-byte chunks per box row
+  constexpr uint32_t SWZ_MASK = BOX_W == 128 ? 7u : BOX_W == 64 ? 3u : 1u;
+  constexpr int LAT_CHUNKS = DH / 8;                // 8-wide fp16 chunks of the latent half
+  constexpr int CONV_UNITS = kTok * (DH / 16) / kConvThreads;   // 16-byte int8 chunks per converter thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -303,11 +327,13 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     mbar_init(bar(B_S_EMPTY), kRows); mbar_init(bar(B_S_EMPTY + 1), kRows);
     mbar_init(bar(B_P_FULL), kRows);
     mbar_init(bar(B_PV_DONE), 1);
-    mbar_init(bar(B_Q_READY), kRows);
-    mbar_init(bar(B_XF), kRows);
+    mbar_init(bar(B_Q_FULL), 1);
+    mbar_init(bar(B_QK_DONE), 1);
+    mbar_init(bar(B_XF), 1);          // armed with the expected bytes, filled by the peer's st.async
     mbar_init(bar(B_XE), kRows);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0u;
+    mbar_expect_tx(bar(B_XF), kXBytes);   // phase 0 of the partial-score exchange
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -373,8 +399,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
   const int64_t* sched = reinterpret_cast<const int64_t*>(smem + OFF_SCHED);
   SegWalk walk0{sched[2], sched[3], sched[1], (int)sched[0]};
-  const int DH = p.DH;
-  const int lat_chunks = DH / 8;                 // 16-byte fp16 chunks per row of the half
   const uint32_t tile_tx = (uint32_t)(kTok * DH) + (uint32_t)(kTok * 16 * p.rope_chunks);
 
   if (warp == kProducerWarp) {
@@ -391,9 +415,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                wait_bar(bar(B_ROPE_EMPTY + s), ph ^ 1u, abort_flag, p.err);
           if (!ok) break;
           mbar_expect_tx(bar(B_TILE_FULL + s), tile_tx);
-          for (int j = 0; j < p.n_box; ++j)
-            tma_3d(sbase + OFF_STG + s * STG_BYTES + (uint32_t)(j * kTok * p.box_w), &p.tm_ckv,
-                   (int)rank * DH + j * p.box_w, tt * kTok, b, bar(B_TILE_FULL + s));
+#pragma unroll
+          for (int j = 0; j < N_BOX; ++j)
+            tma_3d(sbase + OFF_STG + s * STG_BYTES + (uint32_t)(j * kTok * BOX_W), &p.tm_ckv,
+                   (int)rank * DH + j * BOX_W, tt * kTok, b, bar(B_TILE_FULL + s));
           if (p.rope_chunks > 0)
             tma_4d(sbase + OFF_ROPE + s * ROPE_BYTES, &p.tm_rope, 0, tt * kTok, (int)rank * p.rope_chunks, b,
                    bar(B_TILE_FULL + s));
@@ -410,9 +435,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     int b, lo, hi, tb;
     uint32_t it = 0;
     bool ok = true;
-    const int cpb = p.box_w / 16;            // 16-byte chunks per box row
-    const uint32_t swz_mask = p.box_w == 128 ? 7u : p.box_w == 64 ? 3u : 1u;
-    const int units = kTok * (DH / 16);      // (token, 16-byte chunk) units per tile
     while (ok && w.next(p, b, lo, hi, tb)) {
       for (int tt = lo; tt < hi && ok; ++tt, ++it) {
         const uint32_t s = it & 1u, ph = (it >> 1) & 1u;
@@ -421,18 +443,29 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         if (!ok) break;
         const uint8_t* stg = smem + OFF_STG + s * STG_BYTES;
         uint8_t* c16 = smem + OFF_C16 + s * C16_BYTES;
-        for (int u = ct; u < units; u += kConvThreads) {
+        // Unit u = (token n, 16-byte latent chunk cc); consecutive threads take
+        // consecutive tokens, so both the swizzled reads and the core-matrix
+        // writes are conflict-free.  All loads are issued before any convert.
+        uint4 v[CONV_UNITS];
+#pragma unroll
+        for (int i = 0; i < CONV_UNITS; ++i) {
+          const int u = ct + kConvThreads * i;
           const int n = u % kTok, cc = u / kTok;
-          const int j = cc / cpb, c = cc % cpb;
+          const int j = cc / CPB, c = cc % CPB;
           // TMA swizzle: the 16-byte chunk index is XORed with bits 7.. of the row address.
-          const uint32_t row_addr = (uint32_t)(n * p.box_w);
-          const uint32_t phys = ((uint32_t)c ^ ((row_addr >> 7) & swz_mask)) * 16u;
-          const uint4 v = *reinterpret_cast<const uint4*>(stg + j * kTok * p.box_w + row_addr + phys);
+          const uint32_t row_addr = (uint32_t)(n * BOX_W);
+          const uint32_t phys = ((uint32_t)c ^ ((row_addr >> 7) & SWZ_MASK)) * 16u;
+          v[i] = *reinterpret_cast<const uint4*>(stg + j * kTok * BOX_W + row_addr + phys);
+        }
+#pragma unroll
+        for (int i = 0; i < CONV_UNITS; ++i) {
+          const int u = ct + kConvThreads * i;
+          const int n = u % kTok, cc = u / kTok;
           uint4 o0, o1;
-          i8x4_to_f16x4(v.x, o0.x, o0.y);
-          i8x4_to_f16x4(v.y, o0.z, o0.w);
-          i8x4_to_f16x4(v.z, o1.x, o1.y);
-          i8x4_to_f16x4(v.w, o1.z, o1.w);
+          i8x4_to_f16x4(v[i].x, o0.x, o0.y);
+          i8x4_to_f16x4(v[i].y, o0.z, o0.w);
+          i8x4_to_f16x4(v[i].z, o1.x, o1.y);
+          i8x4_to_f16x4(v[i].w, o1.z, o1.w);
           const int kc = 2 * cc;             // 8-wide latent chunk of the first 8 values
           *reinterpret_cast<uint4*>(c16 + kc * 1024 + n * 16) = o0;
           *reinterpret_cast<uint4*>(c16 + (kc + 1) * 1024 + n * 16) = o1;
@@ -468,7 +501,18 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         return true;
       };
       while (ok && w.next(p, b, lo, hi, tb)) {
-        ok = wait_bar(bar(B_Q_READY), seg & 1u, abort_flag, p.err);
+        // This segment's query: wait until the previous segment's Q.C^T is done
+        // with the old one, then bulk-copy the prepared image.
+        if (seg > 0) ok = wait_bar(bar(B_QK_DONE), (seg - 1) & 1u, abort_flag, p.err);
+        if (!ok) break;
+        {
+          const uint8_t* img = p.q_img + ((size_t)b * 2 + rank) * QIMG_BYTES;
+          const uint32_t lat_bytes = (uint32_t)(DH / 8) * 2048u, rope_bytes = (uint32_t)(p.KR / 8) * 2048u;
+          mbar_expect_tx(bar(B_Q_FULL), lat_bytes + rope_bytes);
+          bulk_g2s(sbase + OFF_Q, img, lat_bytes, bar(B_Q_FULL));
+          if (rope_bytes) bulk_g2s(sbase + OFF_QR, img + 65536, rope_bytes, bar(B_Q_FULL));
+        }
+        ok = wait_bar(bar(B_Q_FULL), seg & 1u, abort_flag, p.err);
         ++seg;
         for (int tt = lo; tt < hi && ok; ++tt, ++it) {
           const uint32_t s = it & 1u, ph = (it >> 1) & 1u;
@@ -489,6 +533,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           }
           mma_commit(bar(B_S_FULL + s));
           mma_commit(bar(B_ROPE_EMPTY + s));
+          if (tt == hi - 1) mma_commit(bar(B_QK_DONE));   // the query may be replaced
           // P.C of the previous tile of this segment overlaps the softmax of this one.
           if (tt > lo) ok = issue_pv(it - 1, tt - 1 == lo);
           if (ok && tt == hi - 1) ok = issue_pv(it, tt == lo);
@@ -512,37 +557,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     uint32_t it = 0;
     bool ok = true;
     while (ok && w.next(p, b, lo, hi, tb)) {
-      // ---- query of this sequence: quantize the latent half, copy the RoPE half
       const float qs = h < p.H ? p.q_scale[h] : 0.f;
       const float c_lat = qs * kvs * p.sm_log2;
-      {
-        const uint16_t* qrow = p.q + ((int64_t)b * p.H + h) * (p.Dl + p.Dr);
-        for (int k = 0; k < lat_chunks; ++k) {
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (h < p.H) {
-            const uint4 v = *reinterpret_cast<const uint4*>(qrow + rank * DH + 8 * k);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            uint32_t r4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float c0 = (float)quant_code(bf16_to_float(wv[e] & 0xffffu), qs);
-              const float c1 = (float)quant_code(bf16_to_float(wv[e] >> 16), qs);
-              r4[e] = pack_f16x2(c0, c1);
-            }
-            o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
-          }
-          *reinterpret_cast<uint4*>(smem + OFF_Q + k * 2048 + (h >> 3) * 128 + (h & 7) * 16) = o;
-        }
-        for (int k = 0; k < p.KR / 8; ++k) {
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (h < p.H && k < p.rope_chunks)
-            o = *reinterpret_cast<const uint4*>(qrow + p.Dl + rank * (p.Dr / 2) + 8 * k);
-          *reinterpret_cast<uint4*>(smem + OFF_QR + k * 2048 + (h >> 3) * 128 + (h & 7) * 16) = o;
-        }
-      }
-      fence_proxy_async();
-      mbar_arrive(bar(B_Q_READY));
-
       const int len = p.lens[b];
       float m_ref = -CUDART_INF_F, l = 0.f;
       for (int tt = lo; tt < hi && ok; ++tt, ++it) {
@@ -575,12 +591,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         ok = warp_all(wait_bar(bar(B_XE), (it & 1u) ^ 1u, abort_flag, p.err, true));
         if (!ok) break;
 #pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4) {
-          const uint32_t dst = peer_x + (uint32_t)((j4 * kRows + h) * 16);
-          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(part[4 * j4]),
-                       "f"(part[4 * j4 + 1]), "f"(part[4 * j4 + 2]), "f"(part[4 * j4 + 3]) : "memory");
-        }
-        mbar_arrive_remote(peer_xf);
+        for (int j4 = 0; j4 < 16; ++j4)
+          st_async_v4(peer_x + (uint32_t)((j4 * kRows + h) * 16), part[4 * j4], part[4 * j4 + 1], part[4 * j4 + 2],
+                      part[4 * j4 + 3], peer_xf);
         ok = warp_all(wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true));
         if (!ok) break;
         float mt = -CUDART_INF_F;
@@ -596,6 +609,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             mt = fmaxf(mt, part[j]);
           }
         }
+        // Re-arm for the next tile before telling the peer that its buffer is free.
+        if (h == 0) mbar_expect_tx(bar(B_XF), kXBytes);
         mbar_arrive_remote(peer_xe);
 
         // ---- online softmax with a lazily moved reference maximum
@@ -651,6 +666,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const bool full = (lo == 0 && hi == tb);
       const float inv = (full && l > 0.f) ? kvs / l : 0.f;
       const int slot = b + cluster;
+#pragma unroll 1
       for (int c0 = 0; c0 < DH; c0 += 32) {
         uint32_t v[32];
         FA3_TMEM_LD32(tmem + lane_base + TM_O + c0, v);
@@ -678,6 +694,51 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   cluster_sync();     // the peer no longer writes into this CTA's shared memory
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+  }
+}
+
+// Quantizes every latent query once per call (per-head static scale, exact
+// codes as fp16) and lays it out, with the RoPE query, as the shared-memory
+// image the decode kernel copies: K-major core matrices of 8 heads x 8 values.
+// One thread per 8 values of one (sequence, head).
+__global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
+  const int chunks_lat = p.Dl / 8, chunks_rope = p.Dr / 8;
+  const int per_row = chunks_lat + chunks_rope;
+  const int64_t n = (int64_t)p.B * kRows * per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % per_row);
+    const int64_t bh = i / per_row;
+    const int h = (int)(bh % kRows), b = (int)(bh / kRows);
+    uint4 o = make_uint4(0, 0, 0, 0);
+    int r, k;
+    uint32_t region;
+    if (c < chunks_lat) {
+      r = c / (p.DH / 8);
+      k = c % (p.DH / 8);
+      region = 0;
+      if (h < p.H) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.H + h) * (p.Dl + p.Dr) + 8 * c);
+        const float qs = p.q_scale[h], rqs = rcp_approx(qs);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        uint32_t r4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          r4[e] = pack_f16x2((float)quant_code_fast(bf16_to_float(wv[e] & 0xffffu), qs, rqs),
+                             (float)quant_code_fast(bf16_to_float(wv[e] >> 16), qs, rqs));
+        o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+      }
+    } else {
+      const int cr = c - chunks_lat;
+      r = cr / p.rope_chunks;
+      k = cr % p.rope_chunks;
+      region = 65536;
+      if (h < p.H) o = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.H + h) * (p.Dl + p.Dr) + 8 * c);
+    }
+    uint8_t* img = const_cast<uint8_t*>(p.q_img) + ((size_t)b * 2 + r) * QIMG_BYTES + region;
+    *reinterpret_cast<uint4*>(img + k * 2048 + (h >> 3) * 128 + (h & 7) * 16) = o;
+    // RoPE contraction padding (KR > Dr/2): the extra 8-wide chunk is zero.
+    if (c >= chunks_lat && k == p.rope_chunks - 1 && p.KR / 8 > p.rope_chunks)
+      *reinterpret_cast<uint4*>(img + (k + 1) * 2048 + (h >> 3) * 128 + (h & 7) * 16) = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -739,6 +800,13 @@ __global__ void mla_combine_kernel(const MlaParams p, int64_t total_tiles_unused
   }
 }
 
+template <int DH>
+cudaError_t launch_mla(cudaLaunchConfig_t cfg, const MlaParams& prm) {
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<DH>, prm);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -758,7 +826,7 @@ int max_clusters() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+  if (cudaFuncSetAttribute(mla_decode_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -771,7 +839,8 @@ int max_clusters() {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg) != cudaSuccess || n <= 0) return 0;
+  // Every width instantiation has the same block size and shared memory, hence the same residency.
+  if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<256>, &cfg) != cudaSuccess || n <= 0) return 0;
   if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
 }
@@ -792,7 +861,8 @@ FA3_API size_t fa3_mla_workspace_size(int B, int H, int Dl, int T_max) {
   if (check_device(nullptr) == FA3_OK) C = max_clusters();
   if (C <= 0) C = 128;
   const size_t slots = (size_t)B + (size_t)C;
-  return slots * 2 * kRows * (size_t)(Dl / 2) * sizeof(float) + slots * kRows * sizeof(float2) + 256;
+  return slots * 2 * kRows * (size_t)(Dl / 2) * sizeof(float) + slots * kRows * sizeof(float2) + 256 +
+         (size_t)B * 2 * QIMG_BYTES;
 }
 
 FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint16_t* krope, const float* q_scale,
@@ -848,12 +918,24 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   const size_t slots = (size_t)B + (size_t)C;
   prm.part_o = static_cast<float*>(workspace);
   prm.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + slots * 2 * kRows * prm.DH * sizeof(float));
+  {
+    size_t off = slots * 2 * kRows * prm.DH * sizeof(float) + slots * kRows * sizeof(float2);
+    off = (off + 255) & ~size_t(255);
+    prm.q_img = static_cast<const uint8_t*>(workspace) + off;
+  }
   prm.err = dev_err;
   prm.B = B; prm.H = H; prm.Dl = Dl; prm.Dr = Dr; prm.T_max = T_max;
   prm.num_clusters = C;
   prm.sm_log2 = softmax_scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    const int64_t n = (int64_t)B * kRows * ((Dl + Dr) / 8);
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    mla_prepare_q_kernel<<<(unsigned)blocks, 256, 0, s>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -864,7 +946,14 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla_decode_kernel, prm) != cudaSuccess) return FA3_ECUDA;
+  cudaError_t le = cudaErrorInvalidValue;
+  switch (prm.DH) {
+    case 32: le = launch_mla<32>(cfg, prm); break;
+    case 64: le = launch_mla<64>(cfg, prm); break;
+    case 128: le = launch_mla<128>(cfg, prm); break;
+    case 256: le = launch_mla<256>(cfg, prm); break;
+  }
+  if (le != cudaSuccess) return FA3_ECUDA;
   mla_combine_kernel<<<dim3(kRows, B), 256, 0, s>>>(prm, 0);
   return cuda_status(cudaGetLastError());
 }

@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(256) quantize_append_vec_kernel(
         continue;
       }
       uint4 v = kv[gi];
-      float s = scale[h];
+      const float s = scale[h];
+      const float rs = rcp_approx(s);
       uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t packed[2];
 #pragma unroll
@@ -63,8 +64,8 @@ __global__ void __launch_bounds__(256) quantize_append_vec_kernel(
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           uint32_t word = w[2 * i + j];
-          int c0 = quant_code(bf16_to_float(word & 0xffffu), s);
-          int c1 = quant_code(bf16_to_float(word >> 16), s);
+          const int c0 = quant_code_fast(bf16_to_float(word & 0xffffu), s, rs);
+          const int c1 = quant_code_fast(bf16_to_float(word >> 16), s, rs);
           acc |= ((uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8)) << (16 * j);
         }
         packed[i] = acc;

@@ -96,3 +96,21 @@ def test_query_quantization_as_append():
     F.quantize_append(bf16_dev(inp.q[:, None]), torch.from_numpy(qs).cuda(), q8,
                       torch.zeros(w.B, dtype=torch.int32, device="cuda"))
     assert np.array_equal(q8.cpu().numpy()[:, 0], O.quantize(inp.q, qs[None, :, None]))
+
+
+def test_codes_near_rounding_boundaries():
+    # Quotients x/scale on or next to half-integers (exact ties for power-of-two
+    # scales, near-ties otherwise): codes must equal the IEEE float32 division's.
+    F = fa3()
+    rng = np.random.default_rng(11)
+    scales = np.array([1.0 / 64, 0.25, 2.0, 0.0173, 0.31, 1.0 / 3.0, 2.5e-3, 7.7], np.float32)
+    for s in scales:
+        k = rng.integers(-130, 131, 4096).astype(np.float32)
+        x = ((k + 0.5) * s).astype(np.float32)
+        x = np.concatenate([x, np.nextafter(x, np.float32(np.inf)), np.nextafter(x, np.float32(-np.inf)),
+                            (k * s).astype(np.float32)])
+        x = W.bf16_round(x)[None, None, None, :]                          # [B=1][T_new=1][H=1][D]
+        cache = torch.zeros(1, 1, 1, x.shape[-1], dtype=torch.int8, device="cuda")
+        F.quantize_append(bf16_dev(x), torch.tensor([s], device="cuda"), cache,
+                          torch.zeros(1, dtype=torch.int32, device="cuda"))
+        assert np.array_equal(cache.cpu().numpy()[0, 0, 0], O.quantize(x[0, 0, 0], s)), s
