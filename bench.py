@@ -334,6 +334,60 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_kernel(args):
+    """Runs one kernel alone (for ncu captures): prints its mean time per call."""
+    import torch
+    import __graft_entry__ as G
+    from int8_head_kv_gb300 import fa3 as F
+    G.build()
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    k = args.kernel
+    if k == "mla":
+        ckv = torch.randint(-127, 128, (B, T, DL), dtype=torch.int8, device=dev, generator=g)
+        kr = torch.randn(B, T, DR, device=dev, generator=g).to(torch.bfloat16)
+        q = torch.randn(B, H, DL + DR, device=dev, generator=g).to(torch.bfloat16)
+        qs, kvs = torch.full((H,), 0.03, device=dev), torch.full((1,), 0.02, device=dev)
+        lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+        out = torch.empty(B, H, DL, device=dev)
+        ws = torch.empty(F.mla_workspace_size(B, H, DL, T), dtype=torch.uint8, device=dev)
+        fn = lambda: F.decode_attn_mla(q, ckv, kr, qs, kvs, lens, SOFTMAX_SCALE, out=out, workspace=ws)
+        unit = ("KV GB/s", kv_bytes_per_step())
+    elif k == "gqa":
+        Bq, Hq, Hkv, D, Tq = 16, 64, 8, 128, 4096
+        kc = torch.randint(-127, 128, (Bq, Tq, Hkv, D), dtype=torch.int8, device=dev, generator=g)
+        vc = torch.randint(-127, 128, (Bq, Tq, Hkv, D), dtype=torch.int8, device=dev, generator=g)
+        q8 = torch.randint(-127, 128, (Bq, Hq, D), dtype=torch.int8, device=dev, generator=g)
+        s1, s2 = torch.full((Hq,), 0.01, device=dev), torch.full((Hkv,), 0.01, device=dev)
+        lens = torch.full((Bq,), Tq, dtype=torch.int32, device=dev)
+        fn = lambda: F.decode_attn_gqa(q8, kc, vc, s1, s2, s2, lens, 1 / math.sqrt(128))
+        unit = ("KV GB/s", Bq * Tq * Hkv * D * 2)
+    elif k == "calib":
+        x = (torch.randn(4, H, 2048, 192, device=dev, generator=g) * 2).to(torch.bfloat16)
+        mn, mx = torch.full((H,), float("inf"), device=dev), torch.full((H,), float("-inf"), device=dev)
+        fn = lambda: F.calibrate_perhead(x, 0.9999, mn, mx)
+        unit = ("GB/s", x.numel() * 2)
+    else:
+        kv = torch.randn(32, 64, 1, 512, device=dev, generator=g).to(torch.bfloat16)
+        cache = torch.zeros(32, 1024, 1, 512, dtype=torch.int8, device=dev)
+        pos = torch.zeros(32, dtype=torch.int32, device=dev)
+        sc = torch.full((1,), 0.02, device=dev)
+        fn = lambda: F.quantize_append(kv, sc, cache, pos)
+        unit = ("GB/s", kv.numel() * 3)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"kernel": k, "us_per_call": ms * 1e3, unit[0]: unit[1] / (ms / 1e3) / 1e9}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -342,8 +396,12 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--kernel", choices=["mla", "gqa", "calib", "append"],
+                    help="run one kernel alone (for profiling) instead of the benchmark step")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.kernel:
+        run_kernel(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
