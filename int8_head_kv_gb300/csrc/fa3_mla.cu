@@ -5,26 +5,27 @@
 // RoPE part of K stays in floating point; the decode-phase attention operator
 // reads the INT8 cache.  Scales are the symmetric per-head ones of msModelSlim
 // "FA3量化" 原理 / 算法流程 step 4; the latent query is quantized with its static
-// per-head scale so that the score contraction is an integer one.
+// per-head scale so that the latent score is an integer contraction.
 //
 //   s[h, j] = (sum_c q8[h, c] ckv[j, c]) * q_scale[h] * kv_scale + q_rope[h] . k_rope[j]
 //   out[h]  = kv_scale * sum_j softmax(s * softmax_scale)_j * ckv[j, :]
 //
 // GB300 design (tcgen05 has no int8 MMA kind on sm_103a):
-//   * int8 codes are exact in fp16, and every partial sum of products of two
-//     codes over <= 256 terms stays below 2^24, so a kind::f16 MMA with fp32
-//     accumulation returns the exact integer latent score;
-//   * the fp32 output accumulator of 128 heads x 512 latent is 256 KB -- all of
-//     one SM's TMEM -- so a 2-CTA cluster splits the latent in halves: CTA r
-//     owns latent columns [r*Dl/2, (r+1)*Dl/2) (and half of the RoPE dims),
-//     TMA-loads only that half of each 64-token tile, converts it to fp16 in
-//     shared memory, and computes a partial score over its half;
-//   * the two CTAs swap their fp32 partial scores through distributed shared
-//     memory and both run the same online softmax (fp32 addition commutes, so
-//     both see bit-identical scores, maxima and P);
-//   * P (fp16) . C_r accumulates the CTA's half of O in TMEM; the same fp16
-//     tile serves as the K-major B operand of Q.C^T and the MN-major B operand
-//     of P.C;
+//   * int8 codes are exact in fp16 and a 256-term sum of their products stays
+//     below 2^24, so kind::f16 MMAs with fp32 accumulation give the exact
+//     integer latent score;
+//   * the fp32 accumulator of 128 heads x 512 latent is all of one SM's TMEM, so
+//     a 2-CTA cluster splits the latent in halves: CTA r owns latent columns
+//     [r*Dl/2, (r+1)*Dl/2), TMA-loads only that half of each 64-token tile,
+//     converts it to fp16 core matrices in shared memory (one buffer is the
+//     K-major B operand of Q.C^T and the MN-major B operand of P.C) and keeps
+//     its O half in TMEM;
+//   * the quantized latent query lives in TMEM as the A operand of Q.C^T; the
+//     RoPE term is computed over all RoPE dims in both CTAs (it is small), so
+//     only the exact integer latent partial crosses the cluster, packed in 24
+//     bits (|partial| <= 256*127*127 < 2^23) by st.async into the peer's shared
+//     memory; both CTAs then hold bit-identical scores and run the same online
+//     softmax (lazy rescale when the max grows by more than 8 in log2 units);
 //   * warp roles: 4 softmax warps (one TMEM lane = one head each), 1 TMA
 //     producer, 1 MMA issuer, 4 int8->fp16 converter warps;
 //   * split-K: the tiles of all sequences are dealt out evenly to the clusters
@@ -49,46 +50,49 @@ constexpr int kMmaWarp = 5;
 constexpr int kConvWarp0 = 6;
 constexpr int kConvThreads = 128;
 constexpr int kRows = 128;        // heads (TMEM lanes)
+constexpr int NS = 3;             // TMA staging depth (int8 latent tile + RoPE key tile)
+constexpr int NC = 2;             // fp16 latent tile buffers
 
 // Shared memory map (bytes from a 1024-byte aligned base).
-constexpr uint32_t OFF_Q = 0;             // fp16 latent query half, K-major core matrices (<= 64 KB)
-constexpr uint32_t OFF_QR = 65536;        // bf16 RoPE query half (<= 8 KB)
-// The query of every (sequence, latent half) is prepared once per call by
-// mla_prepare_q_kernel as an exact image of [OFF_Q, OFF_QR + 8 KB) and fetched
-// per segment with one bulk copy.
-constexpr uint32_t QIMG_BYTES = 65536 + 8192;
-constexpr uint32_t OFF_C16 = 73728;       // 2 x fp16 latent tile (<= 32 KB each)
+constexpr uint32_t OFF_QR = 0;                                   // bf16 RoPE query, all Dr dims (<= 16 KB)
+constexpr uint32_t QR_BYTES = 16384;
+constexpr uint32_t OFF_C16 = OFF_QR + QR_BYTES;                  // NC x fp16 latent tile half (<= 32 KB)
 constexpr uint32_t C16_BYTES = 32768;
-constexpr uint32_t OFF_STG = 139264;      // 2 x int8 TMA staging tile (<= 16 KB each)
+constexpr uint32_t OFF_STG = OFF_C16 + NC * C16_BYTES;           // NS x int8 TMA staging (<= 16 KB)
 constexpr uint32_t STG_BYTES = 16384;
-constexpr uint32_t OFF_ROPE = 172032;     // 2 x bf16 RoPE key tile (<= 4 KB each)
-constexpr uint32_t ROPE_BYTES = 4096;
-constexpr uint32_t OFF_P = 180224;        // fp16 P, 128 x 64 (16 KB)
-constexpr uint32_t OFF_X = 196608;        // fp32 partial scores from the peer, 128 x 64 (32 KB)
-constexpr uint32_t OFF_BAR = 229376;
-constexpr uint32_t kXBytes = 128 * 64 * 4;   // one tile of fp32 partial scores, all heads
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;
+constexpr uint32_t OFF_ROPE = OFF_STG + NS * STG_BYTES;          // NS x bf16 RoPE key tile (<= 8 KB)
+constexpr uint32_t ROPE_BYTES = 8192;
+constexpr uint32_t OFF_P = OFF_ROPE + NS * ROPE_BYTES;           // fp16 P, 128 x 64 (16 KB)
+constexpr uint32_t OFF_X = OFF_P + 16384;                        // peer's packed latent partials
+constexpr uint32_t kXChunks = 12;                                // 64 values x 24 bits = 12 x 16 bytes per head
+constexpr uint32_t kXBytes = kXChunks * kRows * 16;
+constexpr uint32_t OFF_BAR = OFF_X + kXBytes;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
 
 // TMEM columns.
 constexpr uint32_t TM_O = 0;      // fp32 O half: Dl/2 columns
-constexpr uint32_t TM_S = 256;    // 2 x 64 latent-score buffers
-constexpr uint32_t TM_R = 384;    // 2 x 64 RoPE-score buffers
+constexpr uint32_t TM_QA = 256;   // fp16 latent query half as the A operand: Dl/4 columns
+constexpr uint32_t TM_S = 384;    // latent partial scores, 64 columns
+constexpr uint32_t TM_R = 448;    // RoPE scores, 64 columns
 
 // Barrier slots (8 bytes each) at OFF_BAR.
 enum {
-  B_TILE_FULL = 0, B_STG_EMPTY = 2, B_ROPE_EMPTY = 4, B_C16_FULL = 6, B_C16_EMPTY = 8,
-  B_S_FULL = 10, B_S_EMPTY = 12, B_P_FULL = 14, B_PV_DONE = 15, B_Q_FULL = 16,
-  B_XF = 17, B_XE = 18, B_DRAIN = 19, B_QK_DONE = 20, NBAR = 21
+  B_TILE_FULL = 0, B_STG_EMPTY = B_TILE_FULL + NS, B_ROPE_EMPTY = B_STG_EMPTY + NS,
+  B_C16_FULL = B_ROPE_EMPTY + NS, B_C16_EMPTY = B_C16_FULL + NC,
+  B_S_FULL = B_C16_EMPTY + NC, B_S_EMPTY, B_R_EMPTY, B_P_FULL, B_PV_DONE, B_Q_READY, B_QR_FULL, B_QK_DONE,
+  B_XF, B_XE, B_DRAIN, NBAR
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;   // u32 TMEM base address
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;         // u32 abort flag
 constexpr uint32_t OFF_SCHED = OFF_TMEM_SLOT + 8;         // 4 x int64: b_first, pre_first, x0, x1
+static_assert(OFF_SCHED + 32 <= OFF_BAR + 512, "barrier area");
 
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: normal waits last microseconds
+constexpr int kMaxSeg = 256;                   // clusters a sequence can span (>= resident clusters)
 
 struct MlaParams {
   CUtensorMap tm_ckv;    // int8 [B][T_max][Dl], box {min(Dl/2,128), 64, 1}
-  CUtensorMap tm_rope;   // bf16 viewed as (8, T_max, Dr/8, B), box {8, 64, Dr/16, 1}
+  CUtensorMap tm_rope;   // bf16 viewed as (8, T_max, Dr/8, B), box {8, 64, Dr/8, 1}
   const uint16_t* q;
   const float* q_scale;
   const float* kv_scale;
@@ -96,14 +100,13 @@ struct MlaParams {
   float* out;
   float* part_o;         // [slot][2][128][Dl/2]
   float2* part_ml;       // [slot][128]
-  const uint8_t* q_img;  // [B][2][QIMG_BYTES] query images (fp16 latent codes, bf16 RoPE)
+  uint16_t* q_lat;       // [B][2][128][Dl/2] fp16 latent query codes (prepared per call)
+  uint8_t* q_rope;       // [B][QR_BYTES] bf16 RoPE query in core-matrix layout (prepared per call)
+  int* seg_n;            // [B] segments of each sequence: -1 one cluster wrote it, 0 empty, else count
+  int* seg_slot;         // [B][kMaxSeg] partial slots of each split sequence
   int32_t* err;
   int B, H, Dl, Dr, T_max;
   int DH;                // Dl / 2
-  int box_w;             // bytes per TMA box row of the latent (<= 128)
-  int n_box;             // boxes per latent half
-  int rope_chunks;       // 8-wide RoPE chunks per CTA (Dr / 16)
-  int KR;                // RoPE contraction per CTA padded to a multiple of 16 (0 if Dr == 0)
   int num_clusters;
   float sm_log2;         // softmax_scale * log2(e)
 };
@@ -138,11 +141,6 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t a, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok) : "r"(a), "r"(parity) : "memory");
   return ok != 0;
-}
-// Asynchronous remote store; its bytes complete_tx on the destination CTA's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d, uint32_t rbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
-               ::"r"(raddr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar) : "memory");
 }
 // Bulk asynchronous copy global -> this CTA's shared memory, completing on an mbarrier.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -270,6 +268,36 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Softmax warps run tcgen05.ld/st (warp-collective): keep their control flow warp-uniform.
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
+
+// tcgen05.mma with the A operand in TMEM.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void st_async_u4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(raddr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar) : "memory");
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Four integers in [-2^23, 2^23) <-> three 32-bit words.
+__device__ __forceinline__ void pack24(int a, int b, int c, int d, uint32_t& w0, uint32_t& w1, uint32_t& w2) {
+  w0 = ((uint32_t)a & 0xffffffu) | ((uint32_t)b << 24);
+  w1 = (((uint32_t)b >> 8) & 0xffffu) | ((uint32_t)c << 16);
+  w2 = (((uint32_t)c >> 16) & 0xffu) | ((uint32_t)d << 8);
+}
+__device__ __forceinline__ void unpack24(uint32_t w0, uint32_t w1, uint32_t w2, int& a, int& b, int& c, int& d) {
+  a = (int)(w0 << 8) >> 8;
+  b = (int)(((w0 >> 24) | (w1 << 8)) << 8) >> 8;
+  c = (int)(((w1 >> 16) | (w2 << 16)) << 8) >> 8;
+  d = (int)w2 >> 8;
+}
+
 __device__ __forceinline__ int seq_tiles(const MlaParams& p, int b) {
   const int len = p.lens[b];
   if (len < 0 || len > p.T_max) return 0;
@@ -304,8 +332,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   constexpr int N_BOX = DH / BOX_W;
   constexpr int CPB = BOX_W / 16;                   // 16-byte chunks per box row
   constexpr uint32_t SWZ_MASK = BOX_W == 128 ? 7u : BOX_W == 64 ? 3u : 1u;
-  constexpr int LAT_CHUNKS = DH / 8;                // 8-wide fp16 chunks of the latent half
   constexpr int CONV_UNITS = kTok * (DH / 16) / kConvThreads;   // 16-byte int8 chunks per converter thread
+  constexpr int QA_WORDS = DH / 2;                  // 32-bit TMEM columns of one head's fp16 query half
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -315,19 +344,26 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   const int cluster = blockIdx.x >> 1;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * (uint32_t)i; };
+  const int rope_chunks = p.Dr / 8;                 // 8-wide RoPE chunks (all of them, in both CTAs)
 
-  // ---- set-up: barriers, TMEM, zero padding, schedule
+  // ---- set-up: barriers, TMEM, schedule
   if (tid == 0) {
-    mbar_init(bar(B_TILE_FULL), 1); mbar_init(bar(B_TILE_FULL + 1), 1);
-    mbar_init(bar(B_STG_EMPTY), kConvThreads); mbar_init(bar(B_STG_EMPTY + 1), kConvThreads);
-    mbar_init(bar(B_ROPE_EMPTY), 1); mbar_init(bar(B_ROPE_EMPTY + 1), 1);
-    mbar_init(bar(B_C16_FULL), kConvThreads); mbar_init(bar(B_C16_FULL + 1), kConvThreads);
-    mbar_init(bar(B_C16_EMPTY), 1); mbar_init(bar(B_C16_EMPTY + 1), 1);
-    mbar_init(bar(B_S_FULL), 1); mbar_init(bar(B_S_FULL + 1), 1);
-    mbar_init(bar(B_S_EMPTY), kRows); mbar_init(bar(B_S_EMPTY + 1), kRows);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(bar(B_TILE_FULL + i), 1);
+      mbar_init(bar(B_STG_EMPTY + i), kConvThreads);
+      mbar_init(bar(B_ROPE_EMPTY + i), 1);
+    }
+    for (int i = 0; i < NC; ++i) {
+      mbar_init(bar(B_C16_FULL + i), kConvThreads);
+      mbar_init(bar(B_C16_EMPTY + i), 1);
+    }
+    mbar_init(bar(B_S_FULL), 1);
+    mbar_init(bar(B_S_EMPTY), kRows);     // latent scores read
+    mbar_init(bar(B_R_EMPTY), kRows);     // RoPE scores read
     mbar_init(bar(B_P_FULL), kRows);
     mbar_init(bar(B_PV_DONE), 1);
-    mbar_init(bar(B_Q_FULL), 1);
+    mbar_init(bar(B_Q_READY), kRows);
+    mbar_init(bar(B_QR_FULL), 1);
     mbar_init(bar(B_QK_DONE), 1);
     mbar_init(bar(B_XF), 1);          // armed with the expected bytes, filled by the peer's st.async
     mbar_init(bar(B_XE), kRows);
@@ -341,23 +377,14 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                  ::"r"(sbase + OFF_TMEM_SLOT), "r"(512) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (warp >= kConvWarp0 && p.KR > 0) {
-    // RoPE key chunks beyond this CTA's share stay zero (contraction padding).
-    for (int s = 0; s < 2; ++s)
-      for (uint32_t off = (uint32_t)p.rope_chunks * 1024u + (uint32_t)(tid - kConvWarp0 * 32) * 16u;
-           off < (uint32_t)(p.KR / 8) * 1024u; off += kConvThreads * 16u)
-        *reinterpret_cast<uint4*>(smem + OFF_ROPE + s * ROPE_BYTES + off) = make_uint4(0, 0, 0, 0);
-  }
   if (warp == 0) {
     // Even split of all tiles over the clusters; find this cluster's first sequence.
     int64_t total = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       int t = (b0 + lane < p.B) ? seq_tiles(p, b0 + lane) : 0;
-      if (lane == 0 && rank == 0 && cluster == 0) {
-        for (int bb = b0; bb < min(b0 + 32, p.B); ++bb) {
-          const int len = p.lens[bb];
-          if (len < 0 || len > p.T_max) set_dev_err(p.err, FA3_DEVERR_LENS);
-        }
+      if (rank == 0 && cluster == 0 && b0 + lane < p.B) {
+        const int len = p.lens[b0 + lane];
+        if (len < 0 || len > p.T_max) set_dev_err(p.err, FA3_DEVERR_LENS);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
@@ -399,7 +426,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
   const int64_t* sched = reinterpret_cast<const int64_t*>(smem + OFF_SCHED);
   SegWalk walk0{sched[2], sched[3], sched[1], (int)sched[0]};
-  const uint32_t tile_tx = (uint32_t)(kTok * DH) + (uint32_t)(kTok * 16 * p.rope_chunks);
+  const uint32_t tile_tx = (uint32_t)(kTok * DH) + (uint32_t)(kTok * 2 * p.Dr);
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -410,23 +437,22 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       bool ok = true;
       while (ok && w.next(p, b, lo, hi, tb)) {
         for (int tt = lo; tt < hi && ok; ++tt, ++it) {
-          const uint32_t s = it & 1u, ph = (it >> 1) & 1u;
-          ok = wait_bar(bar(B_STG_EMPTY + s), ph ^ 1u, abort_flag, p.err) &&
-               wait_bar(bar(B_ROPE_EMPTY + s), ph ^ 1u, abort_flag, p.err);
+          const uint32_t st = it % NS, ph = (it / NS) & 1u;
+          ok = wait_bar(bar(B_STG_EMPTY + st), ph ^ 1u, abort_flag, p.err) &&
+               wait_bar(bar(B_ROPE_EMPTY + st), ph ^ 1u, abort_flag, p.err);
           if (!ok) break;
-          mbar_expect_tx(bar(B_TILE_FULL + s), tile_tx);
+          mbar_expect_tx(bar(B_TILE_FULL + st), tile_tx);
 #pragma unroll
           for (int j = 0; j < N_BOX; ++j)
-            tma_3d(sbase + OFF_STG + s * STG_BYTES + (uint32_t)(j * kTok * BOX_W), &p.tm_ckv,
-                   (int)rank * DH + j * BOX_W, tt * kTok, b, bar(B_TILE_FULL + s));
-          if (p.rope_chunks > 0)
-            tma_4d(sbase + OFF_ROPE + s * ROPE_BYTES, &p.tm_rope, 0, tt * kTok, (int)rank * p.rope_chunks, b,
-                   bar(B_TILE_FULL + s));
+            tma_3d(sbase + OFF_STG + st * STG_BYTES + (uint32_t)(j * kTok * BOX_W), &p.tm_ckv,
+                   (int)rank * DH + j * BOX_W, tt * kTok, b, bar(B_TILE_FULL + st));
+          if (rope_chunks > 0)
+            tma_4d(sbase + OFF_ROPE + st * ROPE_BYTES, &p.tm_rope, 0, tt * kTok, 0, b, bar(B_TILE_FULL + st));
         }
       }
       // Drain: every issued copy must land before the CTA may exit.
-      for (uint32_t k = (it >= 2 ? it - 2 : 0); k < it; ++k)
-        wait_bar(bar(B_TILE_FULL + (k & 1u)), (k >> 1) & 1u, abort_flag, p.err);
+      for (uint32_t k = (it >= NS ? it - NS : 0); k < it; ++k)
+        wait_bar(bar(B_TILE_FULL + k % NS), (k / NS) & 1u, abort_flag, p.err);
     }
   } else if (warp >= kConvWarp0) {
     // ------------------------------------------------------ int8 -> fp16 converters
@@ -437,12 +463,12 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     bool ok = true;
     while (ok && w.next(p, b, lo, hi, tb)) {
       for (int tt = lo; tt < hi && ok; ++tt, ++it) {
-        const uint32_t s = it & 1u, ph = (it >> 1) & 1u;
-        ok = wait_bar(bar(B_TILE_FULL + s), ph, abort_flag, p.err) &&
-             wait_bar(bar(B_C16_EMPTY + s), ph ^ 1u, abort_flag, p.err);
+        const uint32_t st = it % NS, cs = it % NC;
+        ok = wait_bar(bar(B_TILE_FULL + st), (it / NS) & 1u, abort_flag, p.err) &&
+             wait_bar(bar(B_C16_EMPTY + cs), ((it / NC) & 1u) ^ 1u, abort_flag, p.err);
         if (!ok) break;
-        const uint8_t* stg = smem + OFF_STG + s * STG_BYTES;
-        uint8_t* c16 = smem + OFF_C16 + s * C16_BYTES;
+        const uint8_t* stg = smem + OFF_STG + st * STG_BYTES;
+        uint8_t* c16 = smem + OFF_C16 + cs * C16_BYTES;
         // Unit u = (token n, 16-byte latent chunk cc); consecutive threads take
         // consecutive tokens, so both the swizzled reads and the core-matrix
         // writes are conflict-free.  All loads are issued before any convert.
@@ -471,8 +497,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           *reinterpret_cast<uint4*>(c16 + (kc + 1) * 1024 + n * 16) = o1;
         }
         fence_proxy_async();
-        mbar_arrive(bar(B_C16_FULL + s));
-        mbar_arrive(bar(B_STG_EMPTY + s));
+        mbar_arrive(bar(B_C16_FULL + cs));
+        mbar_arrive(bar(B_STG_EMPTY + st));
       }
     }
   } else if (warp == kMmaWarp) {
@@ -481,6 +507,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const uint32_t id_qk = idesc_f16(128, kTok, false, false);
       const uint32_t id_rope = idesc_f16(128, kTok, true, false);
       const uint32_t id_pv = idesc_f16(128, DH, false, true);
+      const uint32_t qr_bytes = (uint32_t)rope_chunks * 2048u;
       SegWalk w = walk0;
       int b, lo, hi, tb;
       uint32_t it = 0, seg = 0;
@@ -488,7 +515,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       auto issue_pv = [&](uint32_t j, bool first) -> bool {
         if (!wait_bar(bar(B_P_FULL), j & 1u, abort_flag, p.err)) return false;
         tc_fence_after();
-        const uint32_t cs = j & 1u;
+        const uint32_t cs = j % NC;
 #pragma unroll
         for (int kk = 0; kk < kTok / 16; ++kk) {
           const uint64_t a = sdesc(sbase + OFF_P + kk * 4096, 2048, 128);
@@ -501,39 +528,44 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         return true;
       };
       while (ok && w.next(p, b, lo, hi, tb)) {
-        // This segment's query: wait until the previous segment's Q.C^T is done
-        // with the old one, then bulk-copy the prepared image.
+        // The RoPE query image of this sequence replaces the previous one once the
+        // previous segment's scores are done with it.
         if (seg > 0) ok = wait_bar(bar(B_QK_DONE), (seg - 1) & 1u, abort_flag, p.err);
         if (!ok) break;
-        {
-          const uint8_t* img = p.q_img + ((size_t)b * 2 + rank) * QIMG_BYTES;
-          const uint32_t lat_bytes = (uint32_t)(DH / 8) * 2048u, rope_bytes = (uint32_t)(p.KR / 8) * 2048u;
-          mbar_expect_tx(bar(B_Q_FULL), lat_bytes + rope_bytes);
-          bulk_g2s(sbase + OFF_Q, img, lat_bytes, bar(B_Q_FULL));
-          if (rope_bytes) bulk_g2s(sbase + OFF_QR, img + 65536, rope_bytes, bar(B_Q_FULL));
+        if (qr_bytes) {
+          mbar_expect_tx(bar(B_QR_FULL), qr_bytes);
+          bulk_g2s(sbase + OFF_QR, p.q_rope + (size_t)b * QR_BYTES, qr_bytes, bar(B_QR_FULL));
+          ok = wait_bar(bar(B_QR_FULL), seg & 1u, abort_flag, p.err);
         }
-        ok = wait_bar(bar(B_Q_FULL), seg & 1u, abort_flag, p.err);
+        ok = ok && wait_bar(bar(B_Q_READY), seg & 1u, abort_flag, p.err);   // latent query in TMEM
         ++seg;
         for (int tt = lo; tt < hi && ok; ++tt, ++it) {
-          const uint32_t s = it & 1u, ph = (it >> 1) & 1u;
-          ok = wait_bar(bar(B_TILE_FULL + s), ph, abort_flag, p.err) &&
-               wait_bar(bar(B_C16_FULL + s), ph, abort_flag, p.err) &&
-               wait_bar(bar(B_S_EMPTY + s), ph ^ 1u, abort_flag, p.err);
+          const uint32_t st = it % NS, cs = it % NC;
+          ok = wait_bar(bar(B_TILE_FULL + st), (it / NS) & 1u, abort_flag, p.err) &&
+               wait_bar(bar(B_C16_FULL + cs), (it / NC) & 1u, abort_flag, p.err) &&
+               wait_bar(bar(B_S_EMPTY), (it & 1u) ^ 1u, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
+          // Latent scores first: the softmax releases them as soon as it has read them,
+          // the RoPE scores only after the partial-score exchange.
+#pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint64_t a = sdesc(sbase + OFF_Q + kk * 4096, 2048, 128);
-            const uint64_t bd = sdesc(sbase + OFF_C16 + s * C16_BYTES + kk * 2048, 1024, 128);
-            mma_f16(tmem + TM_S + s * 64, a, bd, id_qk, kk > 0 ? 1u : 0u);
+            const uint64_t bd = sdesc(sbase + OFF_C16 + cs * C16_BYTES + kk * 2048, 1024, 128);
+            mma_f16_ts(tmem + TM_S, tmem + TM_QA + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
           }
-          for (int kk = 0; kk < p.KR / 16; ++kk) {
+          if (p.Dr > 0) {
+            ok = wait_bar(bar(B_R_EMPTY), (it & 1u) ^ 1u, abort_flag, p.err);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          for (int kk = 0; kk < p.Dr / 16; ++kk) {
             const uint64_t a = sdesc(sbase + OFF_QR + kk * 4096, 2048, 128);
-            const uint64_t bd = sdesc(sbase + OFF_ROPE + s * ROPE_BYTES + kk * 2048, 1024, 128);
-            mma_f16(tmem + TM_R + s * 64, a, bd, id_rope, kk > 0 ? 1u : 0u);
+            const uint64_t bd = sdesc(sbase + OFF_ROPE + st * ROPE_BYTES + kk * 2048, 1024, 128);
+            mma_f16(tmem + TM_R, a, bd, id_rope, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(B_S_FULL + s));
-          mma_commit(bar(B_ROPE_EMPTY + s));
-          if (tt == hi - 1) mma_commit(bar(B_QK_DONE));   // the query may be replaced
+          mma_commit(bar(B_S_FULL));
+          mma_commit(bar(B_ROPE_EMPTY + st));
+          if (tt == hi - 1) mma_commit(bar(B_QK_DONE));   // both query operands may be replaced
           // P.C of the previous tile of this segment overlaps the softmax of this one.
           if (tt > lo) ok = issue_pv(it - 1, tt - 1 == lo);
           if (ok && tt == hi - 1) ok = issue_pv(it, tt == lo);
@@ -549,6 +581,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float kvs = p.kv_scale[0];
     const float c_rope = p.sm_log2;
+    const float c_lat = (h < p.H ? p.q_scale[h] : 0.f) * kvs * p.sm_log2;
     const uint32_t peer_x = mapa(sbase + OFF_X, peer);
     const uint32_t peer_xf = mapa(bar(B_XF), peer);
     const uint32_t peer_xe = mapa(bar(B_XE), peer);
@@ -557,78 +590,132 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     uint32_t it = 0;
     bool ok = true;
     while (ok && w.next(p, b, lo, hi, tb)) {
-      const float qs = h < p.H ? p.q_scale[h] : 0.f;
-      const float c_lat = qs * kvs * p.sm_log2;
+      // ---- latent query of this sequence into TMEM (the previous segment's last
+      //      Q.C^T has completed: this thread consumed its scores)
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + (((size_t)b * 2 + rank) * kRows + h) * DH);
+#pragma unroll
+        for (int c0 = 0; c0 < QA_WORDS; c0 += 32) {
+          uint4 v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = src[c0 / 4 + i];
+          uint32_t r[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            r[4 * i] = v[i].x; r[4 * i + 1] = v[i].y; r[4 * i + 2] = v[i].z; r[4 * i + 3] = v[i].w;
+          }
+          FA3_TMEM_ST32(tmem + lane_base + TM_QA + c0, r);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_Q_READY));
+
       const int len = p.lens[b];
       float m_ref = -CUDART_INF_F, l = 0.f;
       for (int tt = lo; tt < hi && ok; ++tt, ++it) {
-        const uint32_t s = it & 1u, ph = (it >> 1) & 1u;
         const int nvalid = min(kTok, len - tt * kTok);
-        ok = warp_all(wait_bar(bar(B_S_FULL + s), ph, abort_flag, p.err));
+        ok = warp_all(wait_bar(bar(B_S_FULL), it & 1u, abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
-        float part[64];
+        // ---- own latent partial: exact integers in fp32
+        int li[64];
         {
-          uint32_t v[32], r[32];
+          uint32_t v[32];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            FA3_TMEM_LD32(tmem + lane_base + TM_S + s * 64 + half * 32, v);
-            if (p.KR > 0) {
-              FA3_TMEM_LD32(tmem + lane_base + TM_R + s * 64 + half * 32, r);
-            }
+            FA3_TMEM_LD32(tmem + lane_base + TM_S + half * 32, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float rr = p.KR > 0 ? __uint_as_float(r[j]) : 0.f;
-              part[half * 32 + j] = fmaf(__uint_as_float(v[j]), c_lat, rr * c_rope);
-            }
+            for (int j = 0; j < 32; ++j) li[half * 32 + j] = __float2int_rn(__uint_as_float(v[j]));
           }
         }
         tc_fence_before();
-        mbar_arrive(bar(B_S_EMPTY + s));
-
-        // ---- swap partial scores with the peer CTA
+        mbar_arrive(bar(B_S_EMPTY));
+        // ---- swap latent partials with the peer CTA (24 bits each)
         ok = warp_all(wait_bar(bar(B_XE), (it & 1u) ^ 1u, abort_flag, p.err, true));
         if (!ok) break;
+        // 16 values -> 12 packed words -> 3 chunks of 16 bytes (chunk c holds words 4c..4c+3)
 #pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4)
-          st_async_v4(peer_x + (uint32_t)((j4 * kRows + h) * 16), part[4 * j4], part[4 * j4 + 1], part[4 * j4 + 2],
-                      part[4 * j4 + 3], peer_xf);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t wv[12];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int v0 = 16 * q + 4 * g;
+            pack24(li[v0], li[v0 + 1], li[v0 + 2], li[v0 + 3], wv[3 * g], wv[3 * g + 1], wv[3 * g + 2]);
+          }
+#pragma unroll
+          for (int c = 0; c < 3; ++c)
+            st_async_u4(peer_x + (uint32_t)(((3 * q + c) * kRows + h) * 16), wv[4 * c], wv[4 * c + 1], wv[4 * c + 2],
+                        wv[4 * c + 3], peer_xf);
+        }
         ok = warp_all(wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true));
         if (!ok) break;
-        float mt = -CUDART_INF_F;
+        {
+          uint32_t pw[48];
 #pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4) {
-          const float4 o = *reinterpret_cast<const float4*>(smem + OFF_X + (j4 * kRows + h) * 16);
-          const float ov[4] = {o.x, o.y, o.z, o.w};
+          for (int c = 0; c < (int)kXChunks; ++c) {
+            const uint4 o = *reinterpret_cast<const uint4*>(smem + OFF_X + (c * kRows + h) * 16);
+            pw[4 * c] = o.x; pw[4 * c + 1] = o.y; pw[4 * c + 2] = o.z; pw[4 * c + 3] = o.w;
+          }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 4 * j4 + e;
-            const float sc = part[j] + ov[e];
-            part[j] = j < nvalid ? sc : -CUDART_INF_F;
-            mt = fmaxf(mt, part[j]);
+          for (int g = 0; g < 16; ++g) {
+            int a0, a1, a2, a3;
+            unpack24(pw[3 * g], pw[3 * g + 1], pw[3 * g + 2], a0, a1, a2, a3);
+            li[4 * g] += a0; li[4 * g + 1] += a1; li[4 * g + 2] += a2; li[4 * g + 3] += a3;
           }
         }
         // Re-arm for the next tile before telling the peer that its buffer is free.
         if (h == 0) mbar_expect_tx(bar(B_XF), kXBytes);
         mbar_arrive_remote(peer_xe);
 
+        // ---- scores: exact latent sum, RoPE term computed identically in both CTAs
+        float part[64];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            if (p.Dr > 0) {
+              FA3_TMEM_LD32(tmem + lane_base + TM_R + half * 32, r);
+              tmem_wait_ld();
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int jj = half * 32 + j;
+              const float rr = p.Dr > 0 ? __uint_as_float(r[j]) * c_rope : 0.f;
+              const float sc = fmaf((float)li[jj], c_lat, rr);
+              part[jj] = jj < nvalid ? sc : -CUDART_INF_F;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_R_EMPTY));
+        // tile maximum as a tree (short dependency chains)
+        float mx[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          mx[q] = fmaxf(fmaxf(fmaxf(part[8 * q], part[8 * q + 1]), fmaxf(part[8 * q + 2], part[8 * q + 3])),
+                        fmaxf(fmaxf(part[8 * q + 4], part[8 * q + 5]), fmaxf(part[8 * q + 6], part[8 * q + 7])));
+        }
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+
         // ---- online softmax with a lazily moved reference maximum
         float alpha = 1.f;
         bool rescale = false;
         if (mt > m_ref + 8.f) {
-          alpha = (m_ref == -CUDART_INF_F) ? 0.f : exp2f(m_ref - mt);
+          alpha = (m_ref == -CUDART_INF_F) ? 0.f : ex2_approx(m_ref - mt);
           rescale = tt > lo;
           m_ref = mt;
         }
         uint32_t pk[32];
-        float psum = 0.f;
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          pk[j] = pack_f16x2(exp2f(part[2 * j] - m_ref), exp2f(part[2 * j + 1] - m_ref));
-          const float2 f = unpack_f16x2(pk[j]);
-          psum += f.x + f.y;
+          const float e0 = ex2_approx(part[2 * j] - m_ref), e1 = ex2_approx(part[2 * j + 1] - m_ref);
+          pk[j] = pack_f16x2(e0, e1);
+          ps[j & 7] += e0 + e1;
         }
+        const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         l = l * alpha + psum;
         if (tt > lo) {
           // P is single-buffered and O must hold P.C of the previous tile.
@@ -698,10 +785,58 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 }
 
 // Quantizes every latent query once per call (per-head static scale, exact
-// codes as fp16) and lays it out, with the RoPE query, as the shared-memory
-// image the decode kernel copies: K-major core matrices of 8 heads x 8 values.
-// One thread per 8 values of one (sequence, head).
+// codes stored as fp16, row-major per (sequence, latent half, head) for the
+// TMEM A operand) and lays out the RoPE query of each sequence as the
+// shared-memory image of K-major core matrices (8 heads x 8 values).
+// One thread per 8 values of one (sequence, head); heads >= H are zero.
 __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
+  if (blockIdx.x == 0 && threadIdx.x < 32) {
+    // Segments of every sequence under the decode kernel's even split of tiles over
+    // clusters (cluster c covers tile positions [total*c/C, total*(c+1)/C)).
+    const int lane = threadIdx.x;
+    const int C = p.num_clusters;
+    int64_t total = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      int t = b0 + lane < p.B ? seq_tiles(p, b0 + lane) : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      total += t;
+    }
+    auto owner = [&](int64_t x) {   // the largest c with floor(total*c/C) <= x
+      int lo = 0, hi = C - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (total * mid / C <= x) lo = mid; else hi = mid - 1;
+      }
+      return lo;
+    };
+    int64_t pre = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int bb = b0 + lane;
+      const int t = bb < p.B ? seq_tiles(p, bb) : 0;
+      int incl = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (bb < p.B) {
+        const int64_t start = pre + incl - t;
+        int n = 0;
+        if (t > 0) {
+          const int c0 = owner(start), c1 = owner(start + t - 1);
+          if (c0 == c1) {
+            n = -1;
+          } else {
+            for (int c = c0; c <= c1; ++c)
+              if (total * c / C < total * (c + 1) / C && n < kMaxSeg) p.seg_slot[(int64_t)bb * kMaxSeg + n++] = bb + c;
+          }
+        }
+        p.seg_n[bb] = n;
+      }
+      pre += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
   const int chunks_lat = p.Dl / 8, chunks_rope = p.Dr / 8;
   const int per_row = chunks_lat + chunks_rope;
   const int64_t n = (int64_t)p.B * kRows * per_row;
@@ -709,15 +844,11 @@ __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
     const int c = (int)(i % per_row);
     const int64_t bh = i / per_row;
     const int h = (int)(bh % kRows), b = (int)(bh / kRows);
+    const uint16_t* qrow = p.q + ((int64_t)b * p.H + h) * (p.Dl + p.Dr);
     uint4 o = make_uint4(0, 0, 0, 0);
-    int r, k;
-    uint32_t region;
     if (c < chunks_lat) {
-      r = c / (p.DH / 8);
-      k = c % (p.DH / 8);
-      region = 0;
       if (h < p.H) {
-        const uint4 v = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.H + h) * (p.Dl + p.Dr) + 8 * c);
+        const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * c);
         const float qs = p.q_scale[h], rqs = rcp_approx(qs);
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
         uint32_t r4[4];
@@ -727,84 +858,50 @@ __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
                              (float)quant_code_fast(bf16_to_float(wv[e] >> 16), qs, rqs));
         o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
       }
+      const int r = c / (p.DH / 8), k = c % (p.DH / 8);
+      *reinterpret_cast<uint4*>(p.q_lat + (((int64_t)b * 2 + r) * kRows + h) * p.DH + 8 * k) = o;
     } else {
-      const int cr = c - chunks_lat;
-      r = cr / p.rope_chunks;
-      k = cr % p.rope_chunks;
-      region = 65536;
-      if (h < p.H) o = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.H + h) * (p.Dl + p.Dr) + 8 * c);
+      const int k = c - chunks_lat;
+      if (h < p.H) o = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+      *reinterpret_cast<uint4*>(p.q_rope + (int64_t)b * QR_BYTES + k * 2048 + (h >> 3) * 128 + (h & 7) * 16) = o;
     }
-    uint8_t* img = const_cast<uint8_t*>(p.q_img) + ((size_t)b * 2 + r) * QIMG_BYTES + region;
-    *reinterpret_cast<uint4*>(img + k * 2048 + (h >> 3) * 128 + (h & 7) * 16) = o;
-    // RoPE contraction padding (KR > Dr/2): the extra 8-wide chunk is zero.
-    if (c >= chunks_lat && k == p.rope_chunks - 1 && p.KR / 8 > p.rope_chunks)
-      *reinterpret_cast<uint4*>(img + (k + 1) * 2048 + (h >> 3) * 128 + (h & 7) * 16) = make_uint4(0, 0, 0, 0);
   }
 }
 
-// Merges the split segments of each sequence; writes zero rows for empty sequences.
-__global__ void mla_combine_kernel(const MlaParams p, int64_t total_tiles_unused) {
+// Merges the split segments of each sequence (listed by the pre-pass kernel) with
+// log-sum-exp weights; writes zero rows for empty sequences.  One block per
+// (head, sequence), Dl/4 threads, four outputs per thread.
+__global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p) {
   const int h = blockIdx.x, b = blockIdx.y;
-  __shared__ int64_t s_info[3];
-  if (threadIdx.x == 0) {
-    int64_t total = 0, pre = 0;
-    for (int bb = 0; bb < p.B; ++bb) {
-      const int t = seq_tiles(p, bb);
-      if (bb < b) pre += t;
-      total += t;
-    }
-    s_info[0] = total; s_info[1] = pre; s_info[2] = seq_tiles(p, b);
-  }
-  __syncthreads();
-  const int64_t total = s_info[0], pre = s_info[1], tb = s_info[2];
-  const int C = p.num_clusters;
   if (h >= p.H) return;
-  float* dst = p.out + ((int64_t)b * p.H + h) * p.Dl;
-  if (tb == 0) {
-    for (int c = threadIdx.x; c < p.Dl; c += blockDim.x) dst[c] = 0.f;
+  const int n = p.seg_n[b];
+  if (n < 0) return;                                   // one cluster held the sequence
+  const int e = 4 * threadIdx.x;
+  float4* dst = reinterpret_cast<float4*>(p.out + ((int64_t)b * p.H + h) * p.Dl + e);
+  if (n == 0) {
+    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  // owner cluster of tile position x: the largest c with floor(total*c/C) <= x
-  auto owner = [&](int64_t x) {
-    int lo = 0, hi = C - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (total * mid / C <= x) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-  };
-  const int c0 = owner(pre), c1 = owner(pre + tb - 1);
-  if (c0 == c1) return;   // one cluster held the whole sequence and wrote it already
-  // Clusters between the two owners hold a segment of this sequence unless their
-  // range is empty (fewer tiles than clusters); empty ones wrote nothing.
-  auto holds = [&](int c) { return total * c / C < total * (c + 1) / C; };
+  const int* slots = p.seg_slot + (int64_t)b * kMaxSeg;
   float M = -CUDART_INF_F;
-  for (int c = c0; c <= c1; ++c)
-    if (holds(c)) M = fmaxf(M, p.part_ml[(int64_t)(b + c) * kRows + h].x);
+  for (int k = 0; k < n; ++k) M = fmaxf(M, p.part_ml[(int64_t)slots[k] * kRows + h].x);
+  const int r = e / p.DH, dd = e - r * p.DH;
+  const int64_t off = ((int64_t)r * kRows + h) * p.DH + dd;
+  const int64_t slot_stride = (int64_t)2 * kRows * p.DH;
   float L = 0.f;
-  for (int c = c0; c <= c1; ++c) {
-    if (!holds(c)) continue;
-    const float2 ml = p.part_ml[(int64_t)(b + c) * kRows + h];
-    L += ml.y * exp2f(ml.x - M);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int k = 0; k < n; ++k) {
+    const int64_t sl = slots[k];
+    const float2 ml = p.part_ml[sl * kRows + h];
+    const float w = exp2f(ml.x - M);
+    const float4 v = *reinterpret_cast<const float4*>(p.part_o + sl * slot_stride + off);
+    L += ml.y * w;
+    acc.x = fmaf(v.x, w, acc.x); acc.y = fmaf(v.y, w, acc.y);
+    acc.z = fmaf(v.z, w, acc.z); acc.w = fmaf(v.w, w, acc.w);
   }
-  const float kvs = p.kv_scale[0];
-  for (int d = threadIdx.x; d < p.Dl; d += blockDim.x) {
-    const int r = d / p.DH, dd = d - r * p.DH;
-    float O = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-      if (!holds(c)) continue;
-      const int64_t slot = b + c;
-      O += p.part_o[((slot * 2 + r) * kRows + h) * p.DH + dd] * exp2f(p.part_ml[slot * kRows + h].x - M);
-    }
-    dst[d] = L > 0.f ? kvs * (O / L) : 0.f;
-  }
-}
-
-template <int DH>
-cudaError_t launch_mla(cudaLaunchConfig_t cfg, const MlaParams& prm) {
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<DH>, prm);
+  const float sc = L > 0.f ? p.kv_scale[0] / L : 0.f;
+  *dst = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -850,19 +947,44 @@ bool mla_shape_ok(int H, int Dl, int Dr) {
   return H >= 1 && H <= kRows && dl_ok && Dr >= 0 && Dr <= 64 && Dr % 16 == 0;
 }
 
+
+template <int DH>
+cudaError_t launch_mla(cudaLaunchConfig_t cfg, const MlaParams& prm) {
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<DH>, prm);
+}
+
 }  // namespace
 }  // namespace fa3
 
 using namespace fa3;
+
+namespace {
+size_t mla_ws_parts(int B, int Dl, int C, size_t* off_ml, size_t* off_qlat, size_t* off_qrope) {
+  const size_t slots = (size_t)B + (size_t)C;
+  size_t off = slots * 2 * kRows * (size_t)(Dl / 2) * sizeof(float);
+  *off_ml = off;
+  off += slots * kRows * sizeof(float2);
+  off = (off + 255) & ~size_t(255);
+  *off_qlat = off;
+  off += (size_t)B * kRows * (size_t)Dl * sizeof(uint16_t);
+  off = (off + 255) & ~size_t(255);
+  *off_qrope = off;
+  off += (size_t)B * QR_BYTES;
+  off = (off + 255) & ~size_t(255);
+  off += (size_t)B * (kMaxSeg + 1) * sizeof(int);      // segment lists
+  return off + 256;
+}
+}  // namespace
 
 FA3_API size_t fa3_mla_workspace_size(int B, int H, int Dl, int T_max) {
   if (B <= 0 || H <= 0 || Dl <= 0 || T_max <= 0) return 0;
   int C = 0;
   if (check_device(nullptr) == FA3_OK) C = max_clusters();
   if (C <= 0) C = 128;
-  const size_t slots = (size_t)B + (size_t)C;
-  return slots * 2 * kRows * (size_t)(Dl / 2) * sizeof(float) + slots * kRows * sizeof(float2) + 256 +
-         (size_t)B * 2 * QIMG_BYTES;
+  size_t a, b2, c;
+  return mla_ws_parts(B, Dl, C, &a, &b2, &c);
 }
 
 FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint16_t* krope, const float* q_scale,
@@ -879,7 +1001,8 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   if (st != FA3_OK) return st;
   const int C = max_clusters();
   if (C <= 0) return FA3_ECUDA;
-  const size_t need = fa3_mla_workspace_size(B, H, Dl, T_max);
+  size_t off_ml, off_qlat, off_qrope;
+  const size_t need = mla_ws_parts(B, Dl, C, &off_ml, &off_qlat, &off_qrope);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FA3_EWORKSPACE;
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
   if (!encode) return FA3_ECUDA;
@@ -887,41 +1010,41 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   MlaParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.DH = Dl / 2;
-  prm.box_w = prm.DH < 128 ? prm.DH : 128;
-  prm.n_box = prm.DH / prm.box_w;
   {
+    const int box_w = prm.DH < 128 ? prm.DH : 128;
     const cuuint64_t dims[3] = {(cuuint64_t)Dl, (cuuint64_t)T_max, (cuuint64_t)B};
     const cuuint64_t strides[2] = {(cuuint64_t)Dl, (cuuint64_t)Dl * T_max};
-    const cuuint32_t box[3] = {(cuuint32_t)prm.box_w, (cuuint32_t)kTok, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)kTok, 1};
     const cuuint32_t es[3] = {1, 1, 1};
-    const CUtensorMapSwizzle sw = prm.box_w == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : prm.box_w == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                                    : CU_TENSOR_MAP_SWIZZLE_32B;
+    const CUtensorMapSwizzle sw = box_w == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : box_w == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_32B;
     if (encode(&prm.tm_ckv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t*>(ckv), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return FA3_ECUDA;
   }
   if (Dr > 0) {
-    prm.rope_chunks = Dr / 16;
-    prm.KR = ((Dr / 2 + 15) / 16) * 16;
+    // (8 values, token, 8-wide chunk, sequence): one box lands as K-major core matrices.
     const cuuint64_t dims[4] = {8, (cuuint64_t)T_max, (cuuint64_t)(Dr / 8), (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)Dr * 2, 16, (cuuint64_t)Dr * 2 * T_max};
-    const cuuint32_t box[4] = {8, (cuuint32_t)kTok, (cuuint32_t)prm.rope_chunks, 1};
+    const cuuint32_t box[4] = {8, (cuuint32_t)kTok, (cuuint32_t)(Dr / 8), 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     if (encode(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(krope), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return FA3_ECUDA;
   }
+  char* ws = static_cast<char*>(workspace);
   prm.q = q; prm.q_scale = q_scale; prm.kv_scale = kv_scale; prm.lens = lens; prm.out = out;
-  const size_t slots = (size_t)B + (size_t)C;
-  prm.part_o = static_cast<float*>(workspace);
-  prm.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + slots * 2 * kRows * prm.DH * sizeof(float));
+  prm.part_o = reinterpret_cast<float*>(ws);
+  prm.part_ml = reinterpret_cast<float2*>(ws + off_ml);
+  prm.q_lat = reinterpret_cast<uint16_t*>(ws + off_qlat);
+  prm.q_rope = reinterpret_cast<uint8_t*>(ws + off_qrope);
   {
-    size_t off = slots * 2 * kRows * prm.DH * sizeof(float) + slots * kRows * sizeof(float2);
-    off = (off + 255) & ~size_t(255);
-    prm.q_img = static_cast<const uint8_t*>(workspace) + off;
+    size_t off_seg = (off_qrope + (size_t)B * QR_BYTES + 255) & ~size_t(255);
+    prm.seg_n = reinterpret_cast<int*>(ws + off_seg);
+    prm.seg_slot = prm.seg_n + B;
   }
   prm.err = dev_err;
   prm.B = B; prm.H = H; prm.Dl = Dl; prm.Dr = Dr; prm.T_max = T_max;
@@ -954,6 +1077,6 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
     case 256: le = launch_mla<256>(cfg, prm); break;
   }
   if (le != cudaSuccess) return FA3_ECUDA;
-  mla_combine_kernel<<<dim3(kRows, B), 256, 0, s>>>(prm, 0);
+  mla_combine_kernel<<<dim3(H, B), Dl / 4, 0, s>>>(prm);
   return cuda_status(cudaGetLastError());
 }
