@@ -10,11 +10,11 @@
 // maps them onto the total order of their values (-0 before +0).  Counting
 // each key (a counting sort) therefore carries the whole sorted sequence, so
 // one pass over HBM replaces the sort:
-//   kernel 1  per (head, 65528-value chunk): a 65536-bin histogram of 16-bit
-//             counters packed two per word in 128 KB of shared memory (a chunk
-//             is shorter than 65536, so no counter can overflow), then the
-//             non-zero bins are added into the per-head u32 table in the
-//             workspace.
+//   kernel 1  persistent CTAs walk (head, 65528-value chunk) pairs: a 65536-bin
+//             histogram of 16-bit counters packed two per word in 128 KB of
+//             shared memory (a chunk is shorter than 65536, so no counter can
+//             overflow), then the non-zero bins are added into the per-head u32
+//             table in the workspace and cleared, while the next chunk loads.
 //   kernel 2  per head: prefix sums over the 65536 bins; a window can only be
 //             narrowest if it starts at the first copy of a value, so each
 //             occupied bin v with start position P(v) <= N - target_num is a
@@ -35,44 +35,69 @@ constexpr int kScalarPerThread = (kChunk + kHistThreads - 1) / kHistThreads;    
 constexpr int kWinThreads = 1024;
 constexpr int kBinsPerThread = kBins / kWinThreads;  // 64
 
-// Order-preserving key of a bf16 bit pattern: positive values get the top bit
-// set, negative values are bit-inverted, so key order == value order and
-// -0.0 (0x8000) maps just below +0.0 (0x0000).
-__device__ __forceinline__ uint32_t bf16_key(uint32_t bits) {
-  return (bits & 0x8000u) ? (~bits & 0xffffu) : (bits | 0x8000u);
-}
-
+// Order-preserving 16-bit key of a bf16 value: positive values get the top bit
+// set, negative values are bit-inverted, so key order == value order and -0.0
+// (0x8000) maps just below +0.0 (0x0000).  key_value is the inverse.
 __device__ __forceinline__ float key_value(uint32_t key) {
   uint32_t bits = (key & 0x8000u) ? (key ^ 0x8000u) : (~key & 0xffffu);
   return __uint_as_float(bits << 16);
 }
 
-__device__ __forceinline__ void count_key(uint32_t* bins, uint32_t key) {
-  // Warps whose 32 lanes all hold the same key (constant heads) add once.
-  const uint32_t lane0 = __shfl_sync(0xffffffffu, key, 0);
-  const bool same = __all_sync(0xffffffffu, key == lane0);
-  const uint32_t inc = (key & 1u) ? 0x10000u : 1u;
-  if (same) {
-    if ((threadIdx.x & 31) == 0) atomicAdd(&bins[key >> 1], inc * 32u);
-  } else {
-    atomicAdd(&bins[key >> 1], inc);
+// Two order-preserving keys from one 32-bit word holding two bf16 values:
+// negative halves are inverted, positive halves get their top bit set.
+__device__ __forceinline__ uint32_t bf16x2_keys(uint32_t w) {
+  const uint32_t neg = (w >> 15) & 0x00010001u;            // sign bit of each half, at bit 0 / 16
+  return w ^ ((neg * 0x7fffu) | 0x80008000u);
+}
+
+// Adds one count for the 16-bit key `key` (two 16-bit counters per shared word).
+__device__ __forceinline__ void count16(uint32_t* bins, uint32_t key) {
+  atomicAdd(&bins[key >> 1], 1u << ((key & 1u) << 4));
+}
+
+// Counts the 8 values of one 16-byte group.  When the whole warp holds one and the
+// same 16 bytes made of a single repeated value (a constant head), one lane adds
+// 256 at once instead of 256 conflicting atomics.
+__device__ __forceinline__ void count_group(uint32_t* bins, const uint4 v, bool valid) {
+  const uint32_t w0 = __shfl_sync(0xffffffffu, v.x, 0);
+  const bool uniform = __all_sync(0xffffffffu, valid && v.x == w0 && v.y == w0 && v.z == w0 && v.w == w0 &&
+                                                   (w0 >> 16) == (w0 & 0xffffu));
+  if (uniform) {
+    if ((threadIdx.x & 31) == 0) {
+      const uint32_t key = bf16x2_keys(w0) & 0xffffu;
+      atomicAdd(&bins[key >> 1], 256u << ((key & 1u) << 4));
+    }
+    return;
+  }
+  if (!valid) return;
+  const uint32_t k[4] = {bf16x2_keys(v.x), bf16x2_keys(v.y), bf16x2_keys(v.z), bf16x2_keys(v.w)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    count16(bins, k[i] & 0xffffu);
+    count16(bins, k[i] >> 16);
   }
 }
 
+// Persistent: CTA g walks chunks g, g + gridDim.x, ... of the (head, chunk) list.
+// While the histogram of one chunk is flushed (and re-zeroed in the same pass),
+// the loads of the next chunk are already in flight.
 __global__ void __launch_bounds__(kHistThreads, 1)
 hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t N,
-            uint32_t* __restrict__ counts, int vec) {
+            int chunks_per_head, int total_chunks, uint32_t* __restrict__ counts, int vec) {
   extern __shared__ uint4 smem_hist[];
   uint32_t* bins = reinterpret_cast<uint32_t*>(smem_hist);   // 32768 words = 65536 16-bit bins
-  const int h = blockIdx.y;
-  const int64_t n0 = (int64_t)blockIdx.x * kChunk;
-  const int64_t n1 = min(n0 + (int64_t)kChunk, N);
-  const uint16_t* xh = x + (int64_t)h * stride_h;
   const int tid = threadIdx.x;
+  for (int i = tid; i < kBins / 8; i += kHistThreads) smem_hist[i] = make_uint4(0, 0, 0, 0);
 
-  if (vec) {
-    // Issue every load of the chunk first; their latency hides the clearing below.
-    uint4 v[kGroupsPerThread];
+  auto chunk_span = [&](int ci, int& h, int64_t& n0, int64_t& n1) {
+    h = ci / chunks_per_head;
+    n0 = (int64_t)(ci - h * chunks_per_head) * kChunk;
+    n1 = min(n0 + (int64_t)kChunk, N);
+  };
+  auto load_chunk = [&](int ci, uint4 (&v)[kGroupsPerThread]) {
+    int h; int64_t n0, n1;
+    chunk_span(ci, h, n0, n1);
+    const uint16_t* xh = x + (int64_t)h * stride_h;
 #pragma unroll
     for (int k = 0; k < kGroupsPerThread; ++k) {
       v[k] = make_uint4(0, 0, 0, 0);
@@ -82,48 +107,48 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
         v[k] = __ldcs(reinterpret_cast<const uint4*>(xh + b * stride_b + l));
       }
     }
-    for (int i = tid; i < kBins / 8; i += kHistThreads) smem_hist[i] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
+  };
+
+  uint4 v[kGroupsPerThread];
+  int ci = blockIdx.x;
+  if (vec && ci < total_chunks) load_chunk(ci, v);
+  __syncthreads();
+  for (; ci < total_chunks; ci += gridDim.x) {
+    int h; int64_t n0, n1;
+    chunk_span(ci, h, n0, n1);
+    if (vec) {
 #pragma unroll
-    for (int k = 0; k < kGroupsPerThread; ++k) {
-      const int64_t n = n0 + 8 * (int64_t)(tid + k * kHistThreads);
-      // Uniform per warp except on the chunk's last partial warp; the warp vote
-      // in count_key needs all lanes, so invalid lanes count nothing but vote.
-      const bool valid = n < n1;
-      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t bits = (w[j >> 1] >> (16 * (j & 1))) & 0xffffu;
-        if (__all_sync(0xffffffffu, valid)) {
-          count_key(bins, bf16_key(bits));
-        } else if (valid) {
-          atomicAdd(&bins[bf16_key(bits) >> 1], (bf16_key(bits) & 1u) ? 0x10000u : 1u);
+      for (int k = 0; k < kGroupsPerThread; ++k) {
+        const int64_t n = n0 + 8 * (int64_t)(tid + k * kHistThreads);
+        count_group(bins, v[k], n < n1);
+      }
+    } else {
+      const uint16_t* xh = x + (int64_t)h * stride_h;
+      for (int k = 0; k < kScalarPerThread; ++k) {
+        const int64_t n = n0 + tid + (int64_t)k * kHistThreads;
+        if (n < n1) {
+          const int64_t b = n / L, l = n - b * L;
+          count16(bins, bf16x2_keys(xh[b * stride_b + l]) & 0xffffu);
         }
       }
     }
-  } else {
-    for (int i = tid; i < kBins / 8; i += kHistThreads) smem_hist[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
-    for (int k = 0; k < kScalarPerThread; ++k) {
-      const int64_t n = n0 + tid + (int64_t)k * kHistThreads;
-      if (n < n1) {
-        const int64_t b = n / L, l = n - b * L;
-        const uint32_t key = bf16_key(xh[b * stride_b + l]);
-        atomicAdd(&bins[key >> 1], (key & 1u) ? 0x10000u : 1u);
-      }
-    }
-  }
-  __syncthreads();
-  uint32_t* ch = counts + (int64_t)h * kBins;
-  for (int i = tid; i < kBins / 8; i += kHistThreads) {
-    const uint4 q = smem_hist[i];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    if (vec && ci + (int)gridDim.x < total_chunks) load_chunk(ci + gridDim.x, v);
+    // flush the non-zero counters into the head's table and clear them
+    uint32_t* ch = counts + (int64_t)h * kBins;
+    for (int i = tid; i < kBins / 8; i += kHistThreads) {
+      const uint4 q = smem_hist[i];
+      if ((q.x | q.y | q.z | q.w) == 0u) continue;
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t lo = w[j] & 0xffffu, hi = w[j] >> 16;
-      if (lo) atomicAdd(&ch[8 * i + 2 * j], lo);
-      if (hi) atomicAdd(&ch[8 * i + 2 * j + 1], hi);
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = w[j] & 0xffffu, hi = w[j] >> 16;
+        if (lo) atomicAdd(&ch[8 * i + 2 * j], lo);
+        if (hi) atomicAdd(&ch[8 * i + 2 * j + 1], hi);
+      }
+      smem_hist[i] = make_uint4(0, 0, 0, 0);
     }
+    __syncthreads();
   }
 }
 
@@ -283,9 +308,19 @@ FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L
   const int smem = kBins * 2;   // 128 KB of 16-bit bins
   if (cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return FA3_ECUDA;
-  dim3 grid((unsigned)((N + kChunk - 1) / kChunk), (unsigned)H);
+  const int chunks_per_head = (int)((N + kChunk - 1) / kChunk);
+  const int64_t total_chunks = (int64_t)chunks_per_head * H;
+  if (total_chunks > (int64_t)1 << 30) return FA3_ERANGE;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess || sms <= 0) sms = 148;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  const unsigned grid = (unsigned)(total_chunks < sms ? total_chunks : sms);
   uint32_t* counts = static_cast<uint32_t*>(workspace);
-  hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, counts, vec);
+  hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, chunks_per_head, (int)total_chunks,
+                                                counts, vec);
   if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
   window_kernel<<<H, kWinThreads, 0, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io);
   return cuda_status(cudaGetLastError());

@@ -24,6 +24,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+
 namespace fa3 {
 namespace {
 
@@ -285,16 +287,39 @@ __global__ void __launch_bounds__(kD) gqa_combine_kernel(const GqaArgs p) {
   p.out[((int64_t)b * p.Hq + h) * kD + d] = __float2bfloat16_rn(val);
 }
 
-// Split-K plan: chunk is a multiple of 64 tokens, chosen so that about eight
-// CTAs per SM cover the largest possible context.
+int gqa_blocks_per_sm();
+
+// Split-K plan: the (split, KV head, sequence) grid is sized to a whole number of
+// waves of resident CTAs, with chunks of at least 64 tokens.
 void gqa_plan(int B, int Hkv, int T_max, int num_sms, int* splits, int* chunk) {
-  const int64_t want_ctas = (int64_t)num_sms * 8;
-  int64_t per = ((int64_t)T_max * B * Hkv + want_ctas - 1) / want_ctas;
-  per = ((per + 63) / 64) * 64;
-  if (per < 64) per = 64;
-  if (per > T_max) per = ((T_max + 15) / 16) * 16;
+  const int64_t units = (int64_t)B * Hkv;
+  const int64_t wave = (int64_t)num_sms * gqa_blocks_per_sm();
+  int best_s = 1;
+  double best_cost = 1e30;
+  const int max_s = (int)std::max<int64_t>(1, (T_max + 63) / 64);
+  for (int sp = 1; sp <= max_s && sp <= 64; ++sp) {
+    const int64_t ctas = units * sp;
+    const int64_t waves = (ctas + wave - 1) / wave;
+    const int64_t per = ((int64_t)T_max + sp - 1) / sp;
+    // time ~ waves x tokens per CTA, plus a fixed per-CTA cost worth ~32 tokens
+    const double cost = (double)waves * (double)(per + 32);
+    if (cost < best_cost - 1e-9) { best_cost = cost; best_s = sp; }
+  }
+  int64_t per = ((int64_t)T_max + best_s - 1) / best_s;
+  per = ((per + 15) / 16) * 16;
   *chunk = (int)per;
   *splits = (int)((T_max + per - 1) / per);
+}
+
+int gqa_blocks_per_sm() {
+  static int cached = 0;
+  if (cached <= 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel, kThreads, 0) != cudaSuccess || n <= 0)
+      n = 3;
+    cached = n;
+  }
+  return cached;
 }
 
 }  // namespace
