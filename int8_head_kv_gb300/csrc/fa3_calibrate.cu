@@ -34,6 +34,7 @@ constexpr int kGroupsPerThread = (kChunk / 8 + kHistThreads - 1) / kHistThreads;
 constexpr int kScalarPerThread = (kChunk + kHistThreads - 1) / kHistThreads;       // 64
 constexpr int kWinThreads = 1024;
 constexpr int kBinsPerThread = kBins / kWinThreads;  // 64
+constexpr int kCandCap = 16384;     // window starts the fast search can table (N - t + 1 <= kCandCap)
 
 // Order-preserving 16-bit key of a bf16 value: positive values get the top bit
 // set, negative values are bit-inverted, so key order == value order and -0.0
@@ -212,10 +213,54 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
   if (tid == kWinThreads - 1) base_s[kWinThreads] = base + sum;
   __syncthreads();
 
-  // Candidate windows starting in this thread's bins.
   Cand best{__longlong_as_double(0x7ff0000000000000LL), 0xffffffffu, 0xffffffffu};
   unsigned long long P = base;
-  if (any != 0 && base + t <= N) {
+  if (N - t + 1 <= (unsigned long long)kCandCap) {
+    // Few window starts (ratio near 1): table the first position of every value that
+    // can start a window, cand[position] = its bin; then each bin w looks up the
+    // starts whose window ends inside w: start position = end position - (t - 1).
+    extern __shared__ uint32_t cand[];
+    const uint32_t span = (uint32_t)(N - t + 1);
+    for (uint32_t i = tid; i < span; i += kWinThreads) cand[i] = 0xffffffffu;
+    __syncthreads();
+    unsigned long long pos = base;
+    if (any != 0 && base < span) {
+      for (int q = 0; q < kBinsPerThread / 4; ++q) {
+        const uint4 c4 = src[q];
+        const uint32_t c[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (c[j] != 0 && pos < span) cand[pos] = (uint32_t)(tid * kBinsPerThread + 4 * q + j);
+          pos += c[j];
+        }
+        if (pos >= span) break;
+      }
+    }
+    __syncthreads();
+    // end positions live in [t - 1, N); this thread's bins cover [base, base + sum)
+    pos = base;
+    if (any != 0 && base + sum > t - 1) {
+      for (int q = 0; q < kBinsPerThread / 4; ++q) {
+        const uint4 c4 = src[q];
+        const uint32_t c[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const unsigned long long lo_e = pos > t - 1 ? pos : t - 1, hi_e = pos + c[j];
+          for (unsigned long long e = lo_e; e < hi_e; ++e) {
+            const uint32_t v = cand[e - (t - 1)];
+            if (v != 0xffffffffu) {
+              const uint32_t end_bin = (uint32_t)(tid * kBinsPerThread + 4 * q + j);
+              const double w = (double)key_value(end_bin) - (double)key_value(v);
+              const Cand cd{w, v, end_bin};
+              if (cand_less(cd, best)) best = cd;
+            }
+          }
+          pos = hi_e;
+        }
+      }
+    }
+  } else if (any != 0 && base + t <= N) {
+    // Candidate windows starting in this thread's bins.
     for (int i = 0; i < kBinsPerThread; ++i) {
       const uint32_t cnt = ch[tid * kBinsPerThread + i];
       if (cnt != 0 && P + t <= N) {
@@ -322,6 +367,11 @@ FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L
   hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, chunks_per_head, (int)total_chunks,
                                                 counts, vec);
   if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
-  window_kernel<<<H, kWinThreads, 0, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io);
+  const bool fast = (uint64_t)(N - t + 1) <= (uint64_t)kCandCap;
+  const int wsmem = fast ? (int)((N - t + 1) * sizeof(uint32_t)) : 0;
+  if (wsmem > 48 * 1024 &&
+      cudaFuncSetAttribute(window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem) != cudaSuccess)
+    return FA3_ECUDA;
+  window_kernel<<<H, kWinThreads, wsmem, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io);
   return cuda_status(cudaGetLastError());
 }
