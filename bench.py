@@ -50,25 +50,32 @@ def flops_per_step():
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    """Samples nvidia-smi clocks and throttle reasons around the timed region.
 
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    Started before the timed region (and confirmed producing samples), stopped
+    after it; samples whose timestamps fall within 50 ms of the region are kept.
+    """
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.samples = []
-        self._stop = threading.Event()
         self._proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self._proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "10"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            deadline = time.time() + 3.0
+            while not self.samples and time.time() < deadline:
+                time.sleep(0.01)
         except Exception:
             self._proc = None
         return self
@@ -76,8 +83,15 @@ class ClockSampler:
     def _read(self):
         for line in self._proc.stdout:
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 7:
-                self.samples.append(parts)
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts[1:]))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(0.05)
 
     def __exit__(self, *a):
         if self._proc is not None:
@@ -88,14 +102,33 @@ class ClockSampler:
                 self._proc.kill()
 
     def summary(self):
-        if not self.samples:
+        if self.t0 is None or self.t1 is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        win = [s for t, s in self.samples if self.t0 - 0.05 <= t <= self.t1 + 0.05]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        num = lambda x: float(x) if x.replace(".", "", 1).isdigit() else None
+        sm = [num(s[0]) for s in win if num(s[0]) is not None]
+        mx = [num(s[1]) for s in win if num(s[1]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[3 + i].lower() == "active"})
+        reasons = sorted({names[i] for s in win for i in range(4) if s[3 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+                "reasons": reasons, "samples": len(win),
+                "window_ms": round((self.t1 - self.t0) * 1e3, 1)}
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of mla_decode_kernel from the committed ncu record,
+    or None when the kernel source has changed since that capture."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["mla_decode_kernel"]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != rec["sha256"]:
+            return None
+        return rec["dram_bytes_per_launch"]
+    except Exception:
+        return None
 
 
 # ------------------------------------------------------------------ CPU oracle arm
@@ -242,12 +275,14 @@ def run_gpu(args):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        clk.mark_start()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
             step(i, mla_ev[i])
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
         if world > 1:
             dist.barrier()
     ms_total = t0.elapsed_time(t1)
@@ -299,7 +334,7 @@ def run_gpu(args):
     value = tokens / (ms_step / 1e3)
     kv_gbs = kv_bytes_per_step() / (mla_ms / 1e3) / 1e9
     tflops = flops_per_step() / (mla_ms / 1e3) / 1e12
-    traffic = None
+    traffic = recorded_traffic()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         rate, n, el = oracle_sample(seconds_hint=args.cpu_seconds)
@@ -317,7 +352,8 @@ def run_gpu(args):
         "kv_gbs": kv_gbs, "kv_hbm_frac_of_measured": kv_gbs / hbm,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s",
                      "frac": tflops / bf16, "traffic": traffic,
-                     "kernel": "mla_decode_kernel + mla_combine_kernel (CUDA events around the decode call)",
+                     "kernel": "fa3_decode_attn_mla call = query pre-pass + mla_decode_kernel + combine "
+                               "(CUDA events around the call); traffic: mla_decode_kernel alone, from ncu",
                      "peak_source": "measured bf16 dense (burst), MEASURED_PEAKS.json; f16 runs at the bf16 rate"},
         "hbm_roofline": {"achieved": kv_gbs, "peak": hbm, "unit": "GB/s", "frac": kv_gbs / hbm},
         "calibration": {"workload": "B=4 H=128 S=2048 D=192 bf16, ratio 0.9999", "ms_per_batch": cal_ms,
@@ -325,7 +361,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,   # per step: quantize-append, query pre-pass, decode, combine
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -391,7 +427,7 @@ def run_kernel(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true")
