@@ -44,14 +44,15 @@ namespace fa3 {
 namespace {
 
 constexpr int kTok = 64;          // tokens per tile
-constexpr int kThreads = 320;     // 10 warps
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kConvWarp0 = 6;
-constexpr int kConvThreads = 128;
+constexpr int kThreads = 384;     // 12 warps
+constexpr int kSmWarps = 8;       // softmax: two warps per TMEM lane quarter, one per half of the tile's tokens
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kConvWarp0 = 10;
+constexpr int kConvThreads = 64;
 constexpr int kRows = 128;        // heads (TMEM lanes)
-constexpr int NS = 3;             // TMA staging depth (int8 latent tile + RoPE key tile)
-constexpr int NC = 2;             // fp16 latent tile buffers
+constexpr int NS = 2;             // TMA staging depth (int8 latent tile + RoPE key tile)
+constexpr int NC = 3;             // fp16 latent tile buffers (Q.C^T runs two tiles ahead of P.C)
 
 // Shared memory map (bytes from a 1024-byte aligned base).
 constexpr uint32_t OFF_QR = 0;                                   // bf16 RoPE query, all Dr dims (<= 16 KB)
@@ -66,8 +67,11 @@ constexpr uint32_t OFF_P = OFF_ROPE + NS * ROPE_BYTES;           // fp16 P, 128 
 constexpr uint32_t OFF_X = OFF_P + 16384;                        // peer's packed latent partials
 constexpr uint32_t kXChunks = 12;                                // 64 values x 24 bits = 12 x 16 bytes per head
 constexpr uint32_t kXBytes = kXChunks * kRows * 16;
-constexpr uint32_t OFF_BAR = OFF_X + kXBytes;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+constexpr uint32_t OFF_Y = OFF_X + kXBytes;                      // own packed latent partials (same layout)
+constexpr uint32_t OFF_BAR = OFF_Y + kXBytes;
+constexpr uint32_t OFF_MX = OFF_BAR + 512;                       // float [2][128]: per-half row maxima / sums
+constexpr uint32_t SMEM_BYTES = OFF_MX + 1024 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 // TMEM columns.
 constexpr uint32_t TM_O = 0;      // fp32 O half: Dl/2 columns
@@ -79,8 +83,8 @@ constexpr uint32_t TM_R = 448;    // RoPE scores, 64 columns
 enum {
   B_TILE_FULL = 0, B_STG_EMPTY = B_TILE_FULL + NS, B_ROPE_EMPTY = B_STG_EMPTY + NS,
   B_C16_FULL = B_ROPE_EMPTY + NS, B_C16_EMPTY = B_C16_FULL + NC,
-  B_S_FULL = B_C16_EMPTY + NC, B_S_EMPTY, B_R_EMPTY, B_P_FULL, B_PV_DONE, B_Q_READY, B_QR_FULL, B_QK_DONE,
-  B_XF, B_XE, B_DRAIN, NBAR
+  B_S_FULL = B_C16_EMPTY + NC, B_S_EMPTY, B_R_FULL, B_R_EMPTY, B_P_FULL, B_PV_DONE, B_Q_READY, B_QR_FULL, B_QK_DONE,
+  B_XF, B_XE, B_DRAIN, B_YRDY, B_PAIR_W, B_PAIR_R = B_PAIR_W + 4, NBAR = B_PAIR_R + 4
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;   // u32 TMEM base address
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;         // u32 abort flag
@@ -125,7 +129,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t tx) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(tx) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   uint32_t ok;
@@ -222,6 +226,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),         \
         "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]))
 
+#define FA3_TMEM_LD16(taddr, v)                                                                                   \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];" \
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),  \
+                 "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),        \
+                 "=r"(v[15])                                                                                     \
+               : "r"(taddr))
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -275,29 +286,35 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
       ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
-__device__ __forceinline__ void st_async_u4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t rbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-               ::"r"(raddr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar) : "memory");
-}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// Four integers in [-2^23, 2^23) <-> three 32-bit words.
-__device__ __forceinline__ void pack24(int a, int b, int c, int d, uint32_t& w0, uint32_t& w1, uint32_t& w2) {
-  w0 = ((uint32_t)a & 0xffffffu) | ((uint32_t)b << 24);
-  w1 = (((uint32_t)b >> 8) & 0xffffu) | ((uint32_t)c << 16);
-  w2 = (((uint32_t)c >> 16) & 0xffu) | ((uint32_t)d << 8);
+// Exact integer-valued floats v with |v| < 2^22 <-> 24-bit fields.  x = v + 1.5*2^23
+// is exact, its exponent byte is 0x4B and its low 24 bits are v + 2^22, so four
+// values pack into three words and come back as x by restoring the exponent byte.
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+__device__ __forceinline__ void pack_fields(float v0, float v1, float v2, float v3, uint32_t& w0, uint32_t& w1,
+                                            uint32_t& w2) {
+  const uint32_t f0 = __float_as_uint(v0 + kMagic), f1 = __float_as_uint(v1 + kMagic);
+  const uint32_t f2 = __float_as_uint(v2 + kMagic), f3 = __float_as_uint(v3 + kMagic);
+  w0 = __byte_perm(f0, f1, 0x4210);   // f0 bytes 0-2, f1 byte 0
+  w1 = __byte_perm(f1, f2, 0x5421);   // f1 bytes 1-2, f2 bytes 0-1
+  w2 = __byte_perm(f2, f3, 0x6542);   // f2 byte 2, f3 bytes 0-2
 }
-__device__ __forceinline__ void unpack24(uint32_t w0, uint32_t w1, uint32_t w2, int& a, int& b, int& c, int& d) {
-  a = (int)(w0 << 8) >> 8;
-  b = (int)(((w0 >> 24) | (w1 << 8)) << 8) >> 8;
-  c = (int)(((w1 >> 16) | (w2 << 16)) << 8) >> 8;
-  d = (int)w2 >> 8;
+__device__ __forceinline__ void unpack_fields(uint32_t w0, uint32_t w1, uint32_t w2, float (&x)[4]) {
+  constexpr uint32_t kExp = 0x4B000000u;
+  x[0] = __uint_as_float(__byte_perm(w0, kExp, 0x7210));
+  x[1] = __uint_as_float((__byte_perm(w0, w1, 0x5543) & 0x00FFFFFFu) | kExp);
+  x[2] = __uint_as_float((__byte_perm(w1, w2, 0x4432) & 0x00FFFFFFu) | kExp);
+  x[3] = __uint_as_float(__byte_perm(w2, kExp, 0x7321));
 }
-
+// Bulk copy from this CTA's shared memory into a cluster peer's, completing on the peer's barrier.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster) : "memory");
+}
 __device__ __forceinline__ int seq_tiles(const MlaParams& p, int b) {
   const int len = p.lens[b];
   if (len < 0 || len > p.T_max) return 0;
@@ -358,16 +375,22 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       mbar_init(bar(B_C16_EMPTY + i), 1);
     }
     mbar_init(bar(B_S_FULL), 1);
-    mbar_init(bar(B_S_EMPTY), kRows);     // latent scores read
-    mbar_init(bar(B_R_EMPTY), kRows);     // RoPE scores read
-    mbar_init(bar(B_P_FULL), kRows);
+    mbar_init(bar(B_S_EMPTY), kSmWarps);     // latent scores read
+    mbar_init(bar(B_R_FULL), 1);
+    mbar_init(bar(B_R_EMPTY), kSmWarps);     // RoPE scores read
+    mbar_init(bar(B_P_FULL), kSmWarps);
     mbar_init(bar(B_PV_DONE), 1);
-    mbar_init(bar(B_Q_READY), kRows);
+    mbar_init(bar(B_Q_READY), kSmWarps);
     mbar_init(bar(B_QR_FULL), 1);
     mbar_init(bar(B_QK_DONE), 1);
     mbar_init(bar(B_XF), 1);          // armed with the expected bytes, filled by the peer's st.async
-    mbar_init(bar(B_XE), kRows);
+    mbar_init(bar(B_XE), kSmWarps);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_YRDY), kSmWarps);     // own partial written to Y by every softmax warp
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(B_PAIR_W + i), 2);    // both warps of a lane quarter wrote their value
+      mbar_init(bar(B_PAIR_R + i), 2);    // both warps of a lane quarter read the other's value
+    }
     *abort_flag = 0u;
     mbar_expect_tx(bar(B_XF), kXBytes);   // phase 0 of the partial-score exchange
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -527,6 +550,38 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         mma_commit(bar(B_C16_EMPTY + cs));
         return true;
       };
+      // Q.C^T of tile j into S (latent partial scores).
+      auto issue_qk = [&](uint32_t j) -> bool {
+        const uint32_t cs = j % NC;
+        if (!(wait_bar(bar(B_C16_FULL + cs), (j / NC) & 1u, abort_flag, p.err) &&
+              wait_bar(bar(B_S_EMPTY), (j & 1u) ^ 1u, abort_flag, p.err)))
+          return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint64_t bd = sdesc(sbase + OFF_C16 + cs * C16_BYTES + kk * 2048, 1024, 128);
+          mma_f16_ts(tmem + TM_S, tmem + TM_QA + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_S_FULL));
+        return true;
+      };
+      // RoPE scores of tile j into R; the last tile of a segment also releases both query operands.
+      auto issue_rope = [&](uint32_t j, bool last) -> bool {
+        const uint32_t st = j % NS;
+        if (!(wait_bar(bar(B_TILE_FULL + st), (j / NS) & 1u, abort_flag, p.err) &&
+              wait_bar(bar(B_R_EMPTY), (j & 1u) ^ 1u, abort_flag, p.err)))
+          return false;
+        tc_fence_after();
+        for (int kk = 0; kk < p.Dr / 16; ++kk) {
+          const uint64_t a = sdesc(sbase + OFF_QR + kk * 4096, 2048, 128);
+          const uint64_t bd = sdesc(sbase + OFF_ROPE + st * ROPE_BYTES + kk * 2048, 1024, 128);
+          mma_f16(tmem + TM_R, a, bd, id_rope, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_R_FULL));
+        mma_commit(bar(B_ROPE_EMPTY + st));
+        if (last) mma_commit(bar(B_QK_DONE));
+        return true;
+      };
       while (ok && w.next(p, b, lo, hi, tb)) {
         // The RoPE query image of this sequence replaces the previous one once the
         // previous segment's scores are done with it.
@@ -539,37 +594,17 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         }
         ok = ok && wait_bar(bar(B_Q_READY), seg & 1u, abort_flag, p.err);   // latent query in TMEM
         ++seg;
-        for (int tt = lo; tt < hi && ok; ++tt, ++it) {
-          const uint32_t st = it % NS, cs = it % NC;
-          ok = wait_bar(bar(B_TILE_FULL + st), (it / NS) & 1u, abort_flag, p.err) &&
-               wait_bar(bar(B_C16_FULL + cs), (it / NC) & 1u, abort_flag, p.err) &&
-               wait_bar(bar(B_S_EMPTY), (it & 1u) ^ 1u, abort_flag, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          // Latent scores first: the softmax releases them as soon as it has read them,
-          // the RoPE scores only after the partial-score exchange.
-#pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint64_t bd = sdesc(sbase + OFF_C16 + cs * C16_BYTES + kk * 2048, 1024, 128);
-            mma_f16_ts(tmem + TM_S, tmem + TM_QA + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
-          }
-          if (p.Dr > 0) {
-            ok = wait_bar(bar(B_R_EMPTY), (it & 1u) ^ 1u, abort_flag, p.err);
-            if (!ok) break;
-            tc_fence_after();
-          }
-          for (int kk = 0; kk < p.Dr / 16; ++kk) {
-            const uint64_t a = sdesc(sbase + OFF_QR + kk * 4096, 2048, 128);
-            const uint64_t bd = sdesc(sbase + OFF_ROPE + st * ROPE_BYTES + kk * 2048, 1024, 128);
-            mma_f16(tmem + TM_R, a, bd, id_rope, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(B_S_FULL));
-          mma_commit(bar(B_ROPE_EMPTY + st));
-          if (tt == hi - 1) mma_commit(bar(B_QK_DONE));   // both query operands may be replaced
-          // P.C of the previous tile of this segment overlaps the softmax of this one.
-          if (tt > lo) ok = issue_pv(it - 1, tt - 1 == lo);
-          if (ok && tt == hi - 1) ok = issue_pv(it, tt == lo);
+        // Order on the tensor pipe: Q.C^T runs two tiles and the RoPE term one tile
+        // ahead of P.C, so that the softmax finds the next tile's partial scores
+        // ready while it works on the current one.
+        const uint32_t n = (uint32_t)(hi - lo), base = it;
+        ok = ok && issue_qk(base) && issue_rope(base, n == 1) && (n < 2 || issue_qk(base + 1));
+        for (uint32_t k = 0; k < n && ok; ++k) {
+          if (k + 1 < n) ok = issue_rope(base + k + 1, k + 2 == n);
+          if (ok && k + 2 < n) ok = issue_qk(base + k + 2);
+          if (ok) ok = issue_pv(base + k, k == 0);
         }
+        it = base + n;
       }
       // Drain every MMA this thread issued before the CTA may release TMEM.
       mma_commit(bar(B_DRAIN));
@@ -577,14 +612,80 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int h = tid;                                   // head == TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // Warp w handles heads 32*(w%4) .. +31 (its TMEM lane quarter) and the tile's
+    // tokens 32*(w/4) .. +31; the two warps of a quarter agree on the row maximum
+    // through shared memory and each keeps its own part of the row sum.
+    const int qd = warp & 3, hf = warp >> 2;
+    const int h = qd * 32 + lane;                          // head == TMEM lane
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    float* mx_own = reinterpret_cast<float*>(smem + OFF_MX) + hf * kRows + h;
+    const float* mx_oth = reinterpret_cast<const float*>(smem + OFF_MX) + (hf ^ 1) * kRows + h;
     const float kvs = p.kv_scale[0];
     const float c_rope = p.sm_log2;
     const float c_lat = (h < p.H ? p.q_scale[h] : 0.f) * kvs * p.sm_log2;
     const uint32_t peer_x = mapa(sbase + OFF_X, peer);
     const uint32_t peer_xf = mapa(bar(B_XF), peer);
     const uint32_t peer_xe = mapa(bar(B_XE), peer);
+    // Column ranges of O (fp32 words) and of the fp16 query (32-bit words) this warp handles.
+    constexpr int O_PER = DH >= 64 ? DH / 2 : DH;
+    constexpr int QW = DH / 2, QW_PER = QW >= 16 ? QW / 2 : QW;
+    const int o_lo = hf * O_PER, o_hi = min(DH, o_lo + O_PER);
+    const int q_lo = hf * QW_PER, q_hi = min(QW, q_lo + QW_PER);
+    uint32_t n_pair = 0, n_send = 0;
+    // One arrival per softmax warp (the warp-collective waits and __syncwarp order
+    // every lane's work before it).
+    auto warp_arrive = [&](int which) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(which));
+    };
+    // Own latent partial of tile j -> Y as 24-bit fields (this warp's 32 tokens),
+    // then one bulk copy of Y into the peer's X that completes on the peer's XF.
+    auto send_partial = [&](uint32_t j) -> bool {
+      // XE: the peer has consumed tile j-1, so the previous copy out of Y is complete.
+      if (!warp_all(wait_bar(bar(B_S_FULL), j & 1u, abort_flag, p.err)) ||
+          !warp_all(wait_bar(bar(B_XE), (j & 1u) ^ 1u, abort_flag, p.err, true)))
+        return false;
+      tc_fence_after();
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const int q = 2 * hf + qq;                         // 16-token group of the tile
+        uint32_t v[16];
+        FA3_TMEM_LD16(tmem + lane_base + TM_S + q * 16, v);
+        tmem_wait_ld();
+        uint32_t wv[12];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          pack_fields(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                      __uint_as_float(v[4 * g + 3]), wv[3 * g], wv[3 * g + 1], wv[3 * g + 2]);
+#pragma unroll
+        for (int c = 0; c < 3; ++c)
+          *reinterpret_cast<uint4*>(smem + OFF_Y + ((3 * q + c) * kRows + h) * 16) =
+              make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
+      }
+      tc_fence_before();
+      warp_arrive(B_S_EMPTY);
+      fence_proxy_async();                                  // Y is read by the bulk-copy engine
+      warp_arrive(B_YRDY);
+      bool sent = true;
+      if (warp == 0) {
+        sent = warp_all(wait_bar(bar(B_YRDY), n_send & 1u, abort_flag, p.err));
+        if (sent && lane == 0) bulk_s2cluster(peer_x, sbase + OFF_Y, kXBytes, peer_xf);
+      }
+      ++n_send;
+      return sent;
+    };
+    // Swaps one float per head with the other warp of this lane quarter.
+    auto pair_swap = [&](float mine, float& other) -> bool {
+      if (n_pair > 0 && !warp_all(wait_bar(bar(B_PAIR_R + qd), (n_pair - 1) & 1u, abort_flag, p.err)))
+        return false;                                       // the other warp still reads the previous value
+      *mx_own = mine;
+      warp_arrive(B_PAIR_W + qd);
+      if (!warp_all(wait_bar(bar(B_PAIR_W + qd), n_pair & 1u, abort_flag, p.err))) return false;
+      other = *mx_oth;
+      warp_arrive(B_PAIR_R + qd);
+      ++n_pair;
+      return true;
+    };
     SegWalk w = walk0;
     int b, lo, hi, tb;
     uint32_t it = 0;
@@ -594,112 +695,92 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       //      Q.C^T has completed: this thread consumed its scores)
       {
         const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + (((size_t)b * 2 + rank) * kRows + h) * DH);
-#pragma unroll
-        for (int c0 = 0; c0 < QA_WORDS; c0 += 32) {
-          uint4 v[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = src[c0 / 4 + i];
-          uint32_t r[32];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            r[4 * i] = v[i].x; r[4 * i + 1] = v[i].y; r[4 * i + 2] = v[i].z; r[4 * i + 3] = v[i].w;
-          }
-          FA3_TMEM_ST32(tmem + lane_base + TM_QA + c0, r);
+#pragma unroll 1
+        for (int c0 = q_lo; c0 < q_hi; c0 += 8) {
+          const uint4 v0 = src[c0 / 4], v1 = src[c0 / 4 + 1];
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                       ::"r"(tmem + lane_base + TM_QA + c0), "r"(v0.x), "r"(v0.y), "r"(v0.z), "r"(v0.w), "r"(v1.x),
+                         "r"(v1.y), "r"(v1.z), "r"(v1.w));
         }
         tmem_wait_st();
       }
       tc_fence_before();
-      mbar_arrive(bar(B_Q_READY));
+      warp_arrive(B_Q_READY);
 
       const int len = p.lens[b];
       float m_ref = -CUDART_INF_F, l = 0.f;
+      // The own partial of the next tile goes out right after this tile's scores,
+      // so the cluster copy overlaps this tile's softmax.
+      ok = send_partial(it);
       for (int tt = lo; tt < hi && ok; ++tt, ++it) {
-        const int nvalid = min(kTok, len - tt * kTok);
-        ok = warp_all(wait_bar(bar(B_S_FULL), it & 1u, abort_flag, p.err));
+        const int nvalid = min(kTok, len - tt * kTok) - hf * 32;   // valid tokens in this warp's half
+        ok = warp_all(wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true)) &&
+             warp_all(wait_bar(bar(B_R_FULL), it & 1u, abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
-        // ---- own latent partial: exact integers in fp32
-        int li[64];
-        {
-          uint32_t v[32];
+        // ---- scores: exact latent sum (own + peer partial) and the RoPE term, which
+        //      both CTAs compute identically, so both hold bit-identical scores
+        float part[32];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            FA3_TMEM_LD32(tmem + lane_base + TM_S + half * 32, v);
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q = 2 * hf + qq;
+          uint32_t r[16];
+          if (p.Dr > 0) {
+            FA3_TMEM_LD16(tmem + lane_base + TM_R + q * 16, r);
             tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) li[half * 32 + j] = __float2int_rn(__uint_as_float(v[j]));
           }
-        }
-        tc_fence_before();
-        mbar_arrive(bar(B_S_EMPTY));
-        // ---- swap latent partials with the peer CTA (24 bits each)
-        ok = warp_all(wait_bar(bar(B_XE), (it & 1u) ^ 1u, abort_flag, p.err, true));
-        if (!ok) break;
-        // 16 values -> 12 packed words -> 3 chunks of 16 bytes (chunk c holds words 4c..4c+3)
+          uint32_t xw[12], yw[12];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t wv[12];
+          for (int c = 0; c < 3; ++c) {
+            const uint32_t off = ((3 * q + c) * kRows + h) * 16;
+            const uint4 xo = *reinterpret_cast<const uint4*>(smem + OFF_X + off);
+            const uint4 yo = *reinterpret_cast<const uint4*>(smem + OFF_Y + off);
+            xw[4 * c] = xo.x; xw[4 * c + 1] = xo.y; xw[4 * c + 2] = xo.z; xw[4 * c + 3] = xo.w;
+            yw[4 * c] = yo.x; yw[4 * c + 1] = yo.y; yw[4 * c + 2] = yo.z; yw[4 * c + 3] = yo.w;
+          }
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            const int v0 = 16 * q + 4 * g;
-            pack24(li[v0], li[v0 + 1], li[v0 + 2], li[v0 + 3], wv[3 * g], wv[3 * g + 1], wv[3 * g + 2]);
-          }
+            float xp[4], xs[4];
+            unpack_fields(xw[3 * g], xw[3 * g + 1], xw[3 * g + 2], xp);
+            unpack_fields(yw[3 * g], yw[3 * g + 1], yw[3 * g + 2], xs);
 #pragma unroll
-          for (int c = 0; c < 3; ++c)
-            st_async_u4(peer_x + (uint32_t)(((3 * q + c) * kRows + h) * 16), wv[4 * c], wv[4 * c + 1], wv[4 * c + 2],
-                        wv[4 * c + 3], peer_xf);
-        }
-        ok = warp_all(wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true));
-        if (!ok) break;
-        {
-          uint32_t pw[48];
-#pragma unroll
-          for (int c = 0; c < (int)kXChunks; ++c) {
-            const uint4 o = *reinterpret_cast<const uint4*>(smem + OFF_X + (c * kRows + h) * 16);
-            pw[4 * c] = o.x; pw[4 * c + 1] = o.y; pw[4 * c + 2] = o.z; pw[4 * c + 3] = o.w;
-          }
-#pragma unroll
-          for (int g = 0; g < 16; ++g) {
-            int a0, a1, a2, a3;
-            unpack24(pw[3 * g], pw[3 * g + 1], pw[3 * g + 2], a0, a1, a2, a3);
-            li[4 * g] += a0; li[4 * g + 1] += a1; li[4 * g + 2] += a2; li[4 * g + 3] += a3;
-          }
-        }
-        // Re-arm for the next tile before telling the peer that its buffer is free.
-        if (h == 0) mbar_expect_tx(bar(B_XF), kXBytes);
-        mbar_arrive_remote(peer_xe);
-
-        // ---- scores: exact latent sum, RoPE term computed identically in both CTAs
-        float part[64];
-        {
-          uint32_t r[32];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            if (p.Dr > 0) {
-              FA3_TMEM_LD32(tmem + lane_base + TM_R + half * 32, r);
-              tmem_wait_ld();
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int jj = half * 32 + j;
-              const float rr = p.Dr > 0 ? __uint_as_float(r[j]) * c_rope : 0.f;
-              const float sc = fmaf((float)li[jj], c_lat, rr);
-              part[jj] = jj < nvalid ? sc : -CUDART_INF_F;
+            for (int i = 0; i < 4; ++i) {
+              // (M + v_own) + (M + v_peer - 2M): every step exact, the result is v_own + v_peer
+              const float lat = xs[i] + (xp[i] - 2.f * kMagic);
+              const float rr = p.Dr > 0 ? __uint_as_float(r[4 * g + i]) * c_rope : 0.f;
+              part[16 * qq + 4 * g + i] = fmaf(lat, c_lat, rr);
             }
           }
+        }
+        if (nvalid < 32) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) part[jj] = jj < nvalid ? part[jj] : -CUDART_INF_F;
         }
         tc_fence_before();
-        mbar_arrive(bar(B_R_EMPTY));
-        // tile maximum as a tree (short dependency chains)
-        float mx[8];
+        warp_arrive(B_R_EMPTY);
+        // Re-arm for the next tile before telling the peer that its buffer is free.
+        if (tid == 0) mbar_expect_tx(bar(B_XF), kXBytes);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(peer_xe);
+        if (tt + 1 < hi) {
+          ok = send_partial(it + 1);
+          if (!ok) break;
+        }
+        // tile maximum as a tree (short dependency chains), then across the pair
+        float mx[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 4; ++q) {
           mx[q] = fmaxf(fmaxf(fmaxf(part[8 * q], part[8 * q + 1]), fmaxf(part[8 * q + 2], part[8 * q + 3])),
                         fmaxf(fmaxf(part[8 * q + 4], part[8 * q + 5]), fmaxf(part[8 * q + 6], part[8 * q + 7])));
         }
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        float mo;
+        ok = pair_swap(mh, mo);
+        if (!ok) break;
+        const float mt = fmaxf(mh, mo);
 
-        // ---- online softmax with a lazily moved reference maximum
+        // ---- online softmax with a lazily moved reference maximum (both warps of
+        //      the pair take the same decisions from the same tile maximum)
         float alpha = 1.f;
         bool rescale = false;
         if (mt > m_ref + 8.f) {
@@ -707,54 +788,59 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           rescale = tt > lo;
           m_ref = mt;
         }
-        uint32_t pk[32];
-        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[16];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 16; ++j) {
           const float e0 = ex2_approx(part[2 * j] - m_ref), e1 = ex2_approx(part[2 * j + 1] - m_ref);
           pk[j] = pack_f16x2(e0, e1);
-          ps[j & 7] += e0 + e1;
+          ps[j & 3] += e0 + e1;
         }
-        const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        l = l * alpha + psum;
+        l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+        // P is single-buffered and O must hold P.C of the previous tile.
         if (tt > lo) {
-          // P is single-buffered and O must hold P.C of the previous tile.
           ok = warp_all(wait_bar(bar(B_PV_DONE), (it - 1) & 1u, abort_flag, p.err));
           if (!ok) break;
           tc_fence_after();
-          // The rescale is decided per head (lane) but tcgen05.ld/st are warp-wide:
-          // the whole warp takes part, lanes that keep their reference scale by 1.
-          if (__any_sync(0xffffffffu, rescale)) {
-            if (!rescale) alpha = 1.f;
-            for (int c0 = 0; c0 < DH; c0 += 32) {
-              uint32_t v[32];
-              FA3_TMEM_LD32(tmem + lane_base + TM_O + c0, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-              FA3_TMEM_ST32(tmem + lane_base + TM_O + c0, v);
-            }
-            tmem_wait_st();
-          }
         }
 #pragma unroll
-        for (int kc = 0; kc < 8; ++kc)
-          *reinterpret_cast<uint4*>(smem + OFF_P + kc * 2048 + (h >> 3) * 128 + (h & 7) * 16) =
+        for (int kc = 0; kc < 4; ++kc)
+          *reinterpret_cast<uint4*>(smem + OFF_P + (4 * hf + kc) * 2048 + (h >> 3) * 128 + (h & 7) * 16) =
               make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
+        // The rescale is decided per head (lane) but tcgen05.ld/st are warp-wide:
+        // the whole warp takes part, lanes that keep their reference scale by 1.
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (!rescale) alpha = 1.f;
+#pragma unroll 1
+          for (int c0 = o_lo; c0 < o_hi; c0 += 32) {
+            uint32_t v[32];
+            FA3_TMEM_LD32(tmem + lane_base + TM_O + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            FA3_TMEM_ST32(tmem + lane_base + TM_O + c0, v);
+          }
+          tmem_wait_st();
+        }
         fence_proxy_async();
         tc_fence_before();
-        mbar_arrive(bar(B_P_FULL));
+        warp_arrive(B_P_FULL);
       }
       if (!ok) break;
-      // ---- segment done: wait for the last P.C, then write the output (or a partial)
+      // ---- segment done: the row sum over both halves, then wait for the last
+      //      P.C and write the output (or a partial)
+      float lo_sum;
+      ok = pair_swap(l, lo_sum);
+      if (!ok) break;
+      const float l_row = hf == 0 ? l + lo_sum : lo_sum + l;   // the same order in both warps
       ok = warp_all(wait_bar(bar(B_PV_DONE), (it - 1) & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
       const bool full = (lo == 0 && hi == tb);
-      const float inv = (full && l > 0.f) ? kvs / l : 0.f;
+      const float inv = (full && l_row > 0.f) ? kvs / l_row : 0.f;
       const int slot = b + cluster;
 #pragma unroll 1
-      for (int c0 = 0; c0 < DH; c0 += 32) {
+      for (int c0 = o_lo; c0 < o_hi; c0 += 32) {
         uint32_t v[32];
         FA3_TMEM_LD32(tmem + lane_base + TM_O + c0, v);
         tmem_wait_ld();
@@ -769,7 +855,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                             __uint_as_float(v[j + 2]) * f, __uint_as_float(v[j + 3]) * f);
         }
       }
-      if (!full && rank == 0 && h < p.H) p.part_ml[(int64_t)slot * kRows + h] = make_float2(m_ref, l);
+      if (!full && rank == 0 && hf == 0 && h < p.H) p.part_ml[(int64_t)slot * kRows + h] = make_float2(m_ref, l_row);
       tc_fence_before();
     }
   }
