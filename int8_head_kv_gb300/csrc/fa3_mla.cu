@@ -84,12 +84,13 @@ enum {
   B_TILE_FULL = 0, B_STG_EMPTY = B_TILE_FULL + NS, B_ROPE_EMPTY = B_STG_EMPTY + NS,
   B_C16_FULL = B_ROPE_EMPTY + NS, B_C16_EMPTY = B_C16_FULL + NC,
   B_S_FULL = B_C16_EMPTY + NC, B_S_EMPTY, B_R_FULL, B_R_EMPTY, B_P_FULL, B_PV_DONE, B_Q_READY, B_QR_FULL, B_QK_DONE,
-  B_XF, B_XE, B_DRAIN, B_YRDY, B_PAIR_W, B_PAIR_R = B_PAIR_W + 4, NBAR = B_PAIR_R + 4
+  B_XF, B_XE, B_DRAIN, B_PAIR_W, B_PAIR_R = B_PAIR_W + 4, NBAR = B_PAIR_R + 4
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;   // u32 TMEM base address
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;         // u32 abort flag
 constexpr uint32_t OFF_SCHED = OFF_TMEM_SLOT + 8;         // 4 x int64: b_first, pre_first, x0, x1
-static_assert(OFF_SCHED + 32 <= OFF_BAR + 512, "barrier area");
+constexpr uint32_t OFF_YCNT = OFF_SCHED + 32;             // u32: softmax warps done writing Y (mod 8)
+static_assert(OFF_YCNT + 4 <= OFF_BAR + 512, "barrier area");
 
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: normal waits last microseconds
 constexpr int kMaxSeg = 256;                   // clusters a sequence can span (>= resident clusters)
@@ -291,14 +292,35 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Paired fp32 arithmetic (one instruction for two lanes of data) and a three-input max.
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n.reg .b64 x, y, z;\nmov.b64 x, {%2, %3};\nmov.b64 y, {%4, %5};\nadd.rn.f32x2 z, x, y;\nmov.b64 {%0, %1}, z;\n}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n.reg .b64 x, y, z;\nmov.b64 x, {%2, %3};\nmov.b64 y, {%4, %5};\nmul.rn.f32x2 z, x, y;\nmov.b64 {%0, %1}, z;\n}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+  asm("{\n.reg .b64 x, y, z, w;\nmov.b64 x, {%2, %3};\nmov.b64 y, {%4, %5};\nmov.b64 z, {%6, %7};\n"
+      "fma.rn.f32x2 w, x, y, z;\nmov.b64 {%0, %1}, w;\n}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 // Exact integer-valued floats v with |v| < 2^22 <-> 24-bit fields.  x = v + 1.5*2^23
 // is exact, its exponent byte is 0x4B and its low 24 bits are v + 2^22, so four
 // values pack into three words and come back as x by restoring the exponent byte.
 constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
 __device__ __forceinline__ void pack_fields(float v0, float v1, float v2, float v3, uint32_t& w0, uint32_t& w1,
                                             uint32_t& w2) {
-  const uint32_t f0 = __float_as_uint(v0 + kMagic), f1 = __float_as_uint(v1 + kMagic);
-  const uint32_t f2 = __float_as_uint(v2 + kMagic), f3 = __float_as_uint(v3 + kMagic);
+  float g0, g1, g2, g3;
+  add2(g0, g1, v0, v1, kMagic, kMagic);
+  add2(g2, g3, v2, v3, kMagic, kMagic);
+  const uint32_t f0 = __float_as_uint(g0), f1 = __float_as_uint(g1), f2 = __float_as_uint(g2), f3 = __float_as_uint(g3);
   w0 = __byte_perm(f0, f1, 0x4210);   // f0 bytes 0-2, f1 byte 0
   w1 = __byte_perm(f1, f2, 0x5421);   // f1 bytes 1-2, f2 bytes 0-1
   w2 = __byte_perm(f2, f3, 0x6542);   // f2 byte 2, f3 bytes 0-2
@@ -386,12 +408,12 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     mbar_init(bar(B_XF), 1);          // armed with the expected bytes, filled by the peer's st.async
     mbar_init(bar(B_XE), kSmWarps);
     mbar_init(bar(B_DRAIN), 1);
-    mbar_init(bar(B_YRDY), kSmWarps);     // own partial written to Y by every softmax warp
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(B_PAIR_W + i), 2);    // both warps of a lane quarter wrote their value
       mbar_init(bar(B_PAIR_R + i), 2);    // both warps of a lane quarter read the other's value
     }
     *abort_flag = 0u;
+    *reinterpret_cast<volatile uint32_t*>(smem + OFF_YCNT) = 0u;
     mbar_expect_tx(bar(B_XF), kXBytes);   // phase 0 of the partial-score exchange
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -631,7 +653,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     constexpr int QW = DH / 2, QW_PER = QW >= 16 ? QW / 2 : QW;
     const int o_lo = hf * O_PER, o_hi = min(DH, o_lo + O_PER);
     const int q_lo = hf * QW_PER, q_hi = min(QW, q_lo + QW_PER);
-    uint32_t n_pair = 0, n_send = 0;
+    uint32_t n_pair = 0;
     // One arrival per softmax warp (the warp-collective waits and __syncwarp order
     // every lane's work before it).
     auto warp_arrive = [&](int which) {
@@ -646,40 +668,47 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           !warp_all(wait_bar(bar(B_XE), (j & 1u) ^ 1u, abort_flag, p.err, true)))
         return false;
       tc_fence_after();
+      uint32_t v[32];
+      FA3_TMEM_LD16(tmem + lane_base + TM_S + hf * 32, v);
+      FA3_TMEM_LD16(tmem + lane_base + TM_S + hf * 32 + 16, (v + 16));
+      tmem_wait_ld();
+      tc_fence_before();
+      warp_arrive(B_S_EMPTY);
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int q = 2 * hf + qq;                         // 16-token group of the tile
-        uint32_t v[16];
-        FA3_TMEM_LD16(tmem + lane_base + TM_S + q * 16, v);
-        tmem_wait_ld();
         uint32_t wv[12];
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-          pack_fields(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
-                      __uint_as_float(v[4 * g + 3]), wv[3 * g], wv[3 * g + 1], wv[3 * g + 2]);
+          pack_fields(__uint_as_float(v[16 * qq + 4 * g]), __uint_as_float(v[16 * qq + 4 * g + 1]),
+                      __uint_as_float(v[16 * qq + 4 * g + 2]), __uint_as_float(v[16 * qq + 4 * g + 3]), wv[3 * g],
+                      wv[3 * g + 1], wv[3 * g + 2]);
 #pragma unroll
         for (int c = 0; c < 3; ++c)
           *reinterpret_cast<uint4*>(smem + OFF_Y + ((3 * q + c) * kRows + h) * 16) =
               make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
       }
-      tc_fence_before();
-      warp_arrive(B_S_EMPTY);
       fence_proxy_async();                                  // Y is read by the bulk-copy engine
-      warp_arrive(B_YRDY);
-      bool sent = true;
-      if (warp == 0) {
-        sent = warp_all(wait_bar(bar(B_YRDY), n_send & 1u, abort_flag, p.err));
-        if (sent && lane == 0) bulk_s2cluster(peer_x, sbase + OFF_Y, kXBytes, peer_xf);
+      __syncwarp();
+      if (lane == 0) {
+        // The last softmax warp to finish its part of Y starts the copy.
+        uint32_t done;
+        asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                     : "=r"(done) : "r"(sbase + OFF_YCNT) : "memory");
+        if ((done & (kSmWarps - 1)) == kSmWarps - 1) bulk_s2cluster(peer_x, sbase + OFF_Y, kXBytes, peer_xf);
       }
-      ++n_send;
-      return sent;
+      return true;
     };
-    // Swaps one float per head with the other warp of this lane quarter.
-    auto pair_swap = [&](float mine, float& other) -> bool {
+    // Swaps one float per head with the other warp of this lane quarter, in two
+    // halves so that other work can run between them.
+    auto pair_put = [&](float mine) -> bool {
       if (n_pair > 0 && !warp_all(wait_bar(bar(B_PAIR_R + qd), (n_pair - 1) & 1u, abort_flag, p.err)))
         return false;                                       // the other warp still reads the previous value
       *mx_own = mine;
       warp_arrive(B_PAIR_W + qd);
+      return true;
+    };
+    auto pair_get = [&](float& other) -> bool {
       if (!warp_all(wait_bar(bar(B_PAIR_W + qd), n_pair & 1u, abort_flag, p.err))) return false;
       other = *mx_oth;
       warp_arrive(B_PAIR_R + qd);
@@ -714,51 +743,37 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       ok = send_partial(it);
       for (int tt = lo; tt < hi && ok; ++tt, ++it) {
         const int nvalid = min(kTok, len - tt * kTok) - hf * 32;   // valid tokens in this warp's half
-        ok = warp_all(wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true)) &&
-             warp_all(wait_bar(bar(B_R_FULL), it & 1u, abort_flag, p.err));
+        ok = warp_all(wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true));
         if (!ok) break;
-        tc_fence_after();
-        // ---- scores: exact latent sum (own + peer partial) and the RoPE term, which
-        //      both CTAs compute identically, so both hold bit-identical scores
-        float part[32];
+        // ---- exact latent sums of this warp's 32 tokens (own + peer partial):
+        //      (M + v_own) + (M + v_peer - 2M), every step exact
+        float lat[32];
+        {
+          uint32_t xw[24], yw[24];
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const int q = 2 * hf + qq;
-          uint32_t r[16];
-          if (p.Dr > 0) {
-            FA3_TMEM_LD16(tmem + lane_base + TM_R + q * 16, r);
-            tmem_wait_ld();
-          }
-          uint32_t xw[12], yw[12];
-#pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            const uint32_t off = ((3 * q + c) * kRows + h) * 16;
+          for (int c = 0; c < 6; ++c) {
+            const uint32_t off = ((6 * hf + c) * kRows + h) * 16;
             const uint4 xo = *reinterpret_cast<const uint4*>(smem + OFF_X + off);
             const uint4 yo = *reinterpret_cast<const uint4*>(smem + OFF_Y + off);
             xw[4 * c] = xo.x; xw[4 * c + 1] = xo.y; xw[4 * c + 2] = xo.z; xw[4 * c + 3] = xo.w;
             yw[4 * c] = yo.x; yw[4 * c + 1] = yo.y; yw[4 * c + 2] = yo.z; yw[4 * c + 3] = yo.w;
           }
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 0; g < 8; ++g) {
             float xp[4], xs[4];
             unpack_fields(xw[3 * g], xw[3 * g + 1], xw[3 * g + 2], xp);
             unpack_fields(yw[3 * g], yw[3 * g + 1], yw[3 * g + 2], xs);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              // (M + v_own) + (M + v_peer - 2M): every step exact, the result is v_own + v_peer
-              const float lat = xs[i] + (xp[i] - 2.f * kMagic);
-              const float rr = p.Dr > 0 ? __uint_as_float(r[4 * g + i]) * c_rope : 0.f;
-              part[16 * qq + 4 * g + i] = fmaf(lat, c_lat, rr);
+            for (int i = 0; i < 4; i += 2) {
+              float t0, t1;
+              add2(t0, t1, xp[i], xp[i + 1], -2.f * kMagic, -2.f * kMagic);
+              add2(lat[4 * g + i], lat[4 * g + i + 1], xs[i], xs[i + 1], t0, t1);
             }
           }
         }
-        if (nvalid < 32) {
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) part[jj] = jj < nvalid ? part[jj] : -CUDART_INF_F;
-        }
-        tc_fence_before();
-        warp_arrive(B_R_EMPTY);
-        // Re-arm for the next tile before telling the peer that its buffer is free.
+        // X and Y have been consumed (every loaded word fed the sums above): re-arm
+        // XF for the next tile, free X for the peer and send the next partial,
+        // so that the cluster copy overlaps the rest of this tile's softmax.
         if (tid == 0) mbar_expect_tx(bar(B_XF), kXBytes);
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(peer_xe);
@@ -766,16 +781,44 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           ok = send_partial(it + 1);
           if (!ok) break;
         }
-        // tile maximum as a tree (short dependency chains), then across the pair
-        float mx[4];
+        // ---- scores: the RoPE term is computed identically in both CTAs, so both
+        //      hold bit-identical scores
+        ok = warp_all(wait_bar(bar(B_R_FULL), it & 1u, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        float part[32];
+        if (p.Dr > 0) {
+          uint32_t r[32];
+          FA3_TMEM_LD16(tmem + lane_base + TM_R + hf * 32, r);
+          FA3_TMEM_LD16(tmem + lane_base + TM_R + hf * 32 + 16, (r + 16));
+          tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mx[q] = fmaxf(fmaxf(fmaxf(part[8 * q], part[8 * q + 1]), fmaxf(part[8 * q + 2], part[8 * q + 3])),
-                        fmaxf(fmaxf(part[8 * q + 4], part[8 * q + 5]), fmaxf(part[8 * q + 6], part[8 * q + 7])));
+          for (int i = 0; i < 32; i += 2) {
+            float r0, r1;
+            mul2(r0, r1, __uint_as_float(r[i]), __uint_as_float(r[i + 1]), c_rope, c_rope);
+            fma2(part[i], part[i + 1], lat[i], lat[i + 1], c_lat, c_lat, r0, r1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) mul2(part[i], part[i + 1], lat[i], lat[i + 1], c_lat, c_lat);
         }
-        const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        tc_fence_before();
+        warp_arrive(B_R_EMPTY);
+        if (nvalid < 32) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) part[jj] = jj < nvalid ? part[jj] : -CUDART_INF_F;
+        }
+        // tile maximum of this half as a tree (short dependency chains), then across the pair
+        float mx[11];
+#pragma unroll
+        for (int q = 0; q < 10; ++q) mx[q] = max3(part[3 * q], part[3 * q + 1], part[3 * q + 2]);
+        mx[10] = fmaxf(part[30], part[31]);
+        const float mh = fmaxf(max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), max3(mx[6], mx[7], mx[8])),
+                               fmaxf(mx[9], mx[10]));
+        ok = pair_put(mh);
+        if (!ok) break;
         float mo;
-        ok = pair_swap(mh, mo);
+        ok = pair_get(mo);
         if (!ok) break;
         const float mt = fmaxf(mh, mo);
 
@@ -792,9 +835,11 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float e0 = ex2_approx(part[2 * j] - m_ref), e1 = ex2_approx(part[2 * j + 1] - m_ref);
+          float d0, d1;
+          add2(d0, d1, part[2 * j], part[2 * j + 1], -m_ref, -m_ref);
+          const float e0 = ex2_approx(d0), e1 = ex2_approx(d1);
           pk[j] = pack_f16x2(e0, e1);
-          ps[j & 3] += e0 + e1;
+          add2(ps[2 * (j & 1)], ps[2 * (j & 1) + 1], ps[2 * (j & 1)], ps[2 * (j & 1) + 1], e0, e1);
         }
         l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
         // P is single-buffered and O must hold P.C of the previous tile.
@@ -830,7 +875,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       // ---- segment done: the row sum over both halves, then wait for the last
       //      P.C and write the output (or a partial)
       float lo_sum;
-      ok = pair_swap(l, lo_sum);
+      ok = pair_put(l) && pair_get(lo_sum);
       if (!ok) break;
       const float l_row = hf == 0 ? l + lo_sum : lo_sum + l;   // the same order in both warps
       ok = warp_all(wait_bar(bar(B_PV_DONE), (it - 1) & 1u, abort_flag, p.err));
