@@ -344,7 +344,7 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "i8 KV codes; f16 tensor-core MMA (exact integer scores); f32 softmax/accum",
+        "vs_baseline": None, "dtype": "i8 KV codes; f16 tensor-core MMA (exact integer latent partials); f32 softmax/accum",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": B, "heads": H, "latent": DL, "rope": DR, "context": T,
                    "step": "quantize-append of the new token + MLA decode (+ split-K combine)",

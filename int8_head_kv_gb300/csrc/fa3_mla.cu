@@ -44,14 +44,13 @@ namespace fa3 {
 namespace {
 
 constexpr int kTok = 64;          // tokens per tile
-constexpr int kThreads = 384;     // 12 warps
+constexpr int kThreads = 384;     // 12 warps: at most 3 per SM sub-partition, so up to 168 registers each
 constexpr int kSmWarps = 8;       // softmax: two warps per TMEM lane quarter, one per half of the tile's tokens
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kConvWarp0 = 10;
-constexpr int kConvThreads = 64;
+constexpr int kMmaWarp = 8;
+constexpr int kConvWarp0 = 9;     // converters (3 warps); the first thread also issues the RoPE key TMA
+constexpr int kConvThreads = 96;
 constexpr int kRows = 128;        // heads (TMEM lanes)
-constexpr int NS = 2;             // TMA staging depth (int8 latent tile + RoPE key tile)
+constexpr int NR = 2;             // RoPE key tile stages (TMA)
 constexpr int NC = 3;             // fp16 latent tile buffers (Q.C^T runs two tiles ahead of P.C)
 
 // Shared memory map (bytes from a 1024-byte aligned base).
@@ -59,17 +58,19 @@ constexpr uint32_t OFF_QR = 0;                                   // bf16 RoPE qu
 constexpr uint32_t QR_BYTES = 16384;
 constexpr uint32_t OFF_C16 = OFF_QR + QR_BYTES;                  // NC x fp16 latent tile half (<= 32 KB)
 constexpr uint32_t C16_BYTES = 32768;
-constexpr uint32_t OFF_STG = OFF_C16 + NC * C16_BYTES;           // NS x int8 TMA staging (<= 16 KB)
-constexpr uint32_t STG_BYTES = 16384;
-constexpr uint32_t OFF_ROPE = OFF_STG + NS * STG_BYTES;          // NS x bf16 RoPE key tile (<= 8 KB)
+constexpr uint32_t OFF_ROPE = OFF_C16 + NC * C16_BYTES;          // NR x bf16 RoPE key tile (<= 8 KB)
 constexpr uint32_t ROPE_BYTES = 8192;
-constexpr uint32_t OFF_P = OFF_ROPE + NS * ROPE_BYTES;           // fp16 P, 128 x 64 (16 KB)
-constexpr uint32_t OFF_X = OFF_P + 16384;                        // peer's packed latent partials
-constexpr uint32_t kXChunks = 12;                                // 64 values x 24 bits = 12 x 16 bytes per head
-constexpr uint32_t kXBytes = kXChunks * kRows * 16;
-constexpr uint32_t OFF_Y = OFF_X + kXBytes;                      // own packed latent partials (same layout)
-constexpr uint32_t OFF_BAR = OFF_Y + kXBytes;
-constexpr uint32_t OFF_MX = OFF_BAR + 512;                       // float [2][128]: per-half row maxima / sums
+constexpr uint32_t OFF_P = OFF_ROPE + NR * ROPE_BYTES;           // fp16 P, 128 x 64 (16 KB)
+// Partial-score exchange, double-buffered: slot s of X receives the peer's fp32
+// partial scores of every other tile, written by the peer's st.async.  Each
+// softmax warp owns a 4 KB region of a slot: [chunk 0..7][lane][16 bytes], 32
+// values per lane.
+constexpr int kXChunks = 8;
+constexpr uint32_t kXWarpBytes = kXChunks * 32 * 16;
+constexpr uint32_t kXSlotBytes = kSmWarps * kXWarpBytes;         // 32 KB
+constexpr uint32_t OFF_X = OFF_P + 16384;
+constexpr uint32_t OFF_BAR = OFF_X + 2 * kXSlotBytes;
+constexpr uint32_t OFF_MX = OFF_BAR + 1024;                      // float [2][128]: per-half row maxima / sums
 constexpr uint32_t SMEM_BYTES = OFF_MX + 1024 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -81,24 +82,26 @@ constexpr uint32_t TM_R = 448;    // RoPE scores, 64 columns
 
 // Barrier slots (8 bytes each) at OFF_BAR.
 enum {
-  B_TILE_FULL = 0, B_STG_EMPTY = B_TILE_FULL + NS, B_ROPE_EMPTY = B_STG_EMPTY + NS,
-  B_C16_FULL = B_ROPE_EMPTY + NS, B_C16_EMPTY = B_C16_FULL + NC,
-  B_S_FULL = B_C16_EMPTY + NC, B_S_EMPTY, B_R_FULL, B_R_EMPTY, B_P_FULL, B_PV_DONE, B_Q_READY, B_QR_FULL, B_QK_DONE,
-  B_XF, B_XE, B_DRAIN, B_PAIR_W, B_PAIR_R = B_PAIR_W + 4, NBAR = B_PAIR_R + 4
+  B_ROPE_FULL = 0, B_ROPE_EMPTY = B_ROPE_FULL + NR,
+  B_C16_FULL = B_ROPE_EMPTY + NR, B_C16_EMPTY = B_C16_FULL + NC,
+  B_S_FULL = B_C16_EMPTY + NC, B_S_EMPTY, B_P_FULL, B_PV_DONE, B_Q_READY, B_QR_FULL, B_QK_DONE,
+  B_DRAIN,
+  B_XF,                          // [slot][warp]: that warp's region of X slot landed (3 KB of tx)
+  B_XE = B_XF + 2 * kSmWarps,    // [slot][warp]: the peer's warp has read its region of that X slot
+  B_PAIR_W = B_XE + 2 * kSmWarps, B_PAIR_R = B_PAIR_W + 4, NBAR = B_PAIR_R + 4
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + 8 * NBAR;   // u32 TMEM base address
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;         // u32 abort flag
 constexpr uint32_t OFF_SCHED = OFF_TMEM_SLOT + 8;         // 4 x int64: b_first, pre_first, x0, x1
-constexpr uint32_t OFF_YCNT = OFF_SCHED + 32;             // u32: softmax warps done writing Y (mod 8)
-static_assert(OFF_YCNT + 4 <= OFF_BAR + 512, "barrier area");
+static_assert(OFF_SCHED + 32 <= OFF_BAR + 1024, "barrier area");
 
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: normal waits last microseconds
 constexpr int kMaxSeg = 256;                   // clusters a sequence can span (>= resident clusters)
 
 struct MlaParams {
-  CUtensorMap tm_ckv;    // int8 [B][T_max][Dl], box {min(Dl/2,128), 64, 1}
   CUtensorMap tm_rope;   // bf16 viewed as (8, T_max, Dr/8, B), box {8, 64, Dr/8, 1}
   const uint16_t* q;
+  const int8_t* ckv;     // [B][T_max][Dl]
   const float* q_scale;
   const float* kv_scale;
   const int32_t* lens;
@@ -207,6 +210,11 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// Arrives on the barrier at the same shared-memory offset in every CTA of cta_mask once the MMAs complete.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               ::"r"(bar), "h"(cta_mask) : "memory");
+}
 
 #define FA3_TMEM_LD32(taddr, v)                                                                                   \
   asm volatile(                                                                                                   \
@@ -311,27 +319,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// Exact integer-valued floats v with |v| < 2^22 <-> 24-bit fields.  x = v + 1.5*2^23
-// is exact, its exponent byte is 0x4B and its low 24 bits are v + 2^22, so four
-// values pack into three words and come back as x by restoring the exponent byte.
-constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
-__device__ __forceinline__ void pack_fields(float v0, float v1, float v2, float v3, uint32_t& w0, uint32_t& w1,
-                                            uint32_t& w2) {
-  float g0, g1, g2, g3;
-  add2(g0, g1, v0, v1, kMagic, kMagic);
-  add2(g2, g3, v2, v3, kMagic, kMagic);
-  const uint32_t f0 = __float_as_uint(g0), f1 = __float_as_uint(g1), f2 = __float_as_uint(g2), f3 = __float_as_uint(g3);
-  w0 = __byte_perm(f0, f1, 0x4210);   // f0 bytes 0-2, f1 byte 0
-  w1 = __byte_perm(f1, f2, 0x5421);   // f1 bytes 1-2, f2 bytes 0-1
-  w2 = __byte_perm(f2, f3, 0x6542);   // f2 byte 2, f3 bytes 0-2
-}
-__device__ __forceinline__ void unpack_fields(uint32_t w0, uint32_t w1, uint32_t w2, float (&x)[4]) {
-  constexpr uint32_t kExp = 0x4B000000u;
-  x[0] = __uint_as_float(__byte_perm(w0, kExp, 0x7210));
-  x[1] = __uint_as_float((__byte_perm(w0, w1, 0x5543) & 0x00FFFFFFu) | kExp);
-  x[2] = __uint_as_float((__byte_perm(w1, w2, 0x4432) & 0x00FFFFFFu) | kExp);
-  x[3] = __uint_as_float(__byte_perm(w2, kExp, 0x7321));
-}
 // Bulk copy from this CTA's shared memory into a cluster peer's, completing on the peer's barrier.
 __device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -363,15 +350,25 @@ struct SegWalk {
   }
 };
 
+// Walks this cluster's tiles one by one (sequence, tile index).
+struct TileWalk {
+  SegWalk w;
+  int b = 0, tt = 0, hi = 0;
+  bool valid = false;
+  __device__ bool next(const MlaParams& p) {
+    if (valid && tt + 1 < hi) { ++tt; return true; }
+    int lo, tb;
+    valid = w.next(p, b, lo, hi, tb);
+    tt = lo;
+    return valid;
+  }
+};
+
 template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ MlaParams p) {
-  // Compile-time geometry of this CTA's latent half.
-  constexpr int BOX_W = DH < 128 ? DH : 128;        // bytes per TMA box row (<= the 128-byte swizzle span)
-  constexpr int N_BOX = DH / BOX_W;
-  constexpr int CPB = BOX_W / 16;                   // 16-byte chunks per box row
-  constexpr uint32_t SWZ_MASK = BOX_W == 128 ? 7u : BOX_W == 64 ? 3u : 1u;
-  constexpr int CONV_UNITS = kTok * (DH / 16) / kConvThreads;   // 16-byte int8 chunks per converter thread
+  constexpr int CONV_TOTAL = kTok * (DH / 16);      // 16-byte int8 chunks of a tile (this CTA's latent half)
+  constexpr int CONV_UNITS = (CONV_TOTAL + kConvThreads - 1) / kConvThreads;   // per converter thread
   constexpr int QA_WORDS = DH / 2;                  // 32-bit TMEM columns of one head's fp16 query half
 
   extern __shared__ uint8_t smem_raw[];
@@ -383,38 +380,40 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   const int cluster = blockIdx.x >> 1;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * (uint32_t)i; };
-  const int rope_chunks = p.Dr / 8;                 // 8-wide RoPE chunks (all of them, in both CTAs)
+  const int rope_chunks = p.Dr / 8;                 // 8-wide RoPE chunks of the key tile (TMA box)
+  // The RoPE term is split over the pair: CTA r contracts 16-wide chunks [rk0, rk1).
+  const int rope_k = p.Dr / 16;
+  const int rk0 = rank == 0 ? 0 : (rope_k + 1) / 2, rk1 = rank == 0 ? (rope_k + 1) / 2 : rope_k;
 
   // ---- set-up: barriers, TMEM, schedule
   if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(bar(B_TILE_FULL + i), 1);
-      mbar_init(bar(B_STG_EMPTY + i), kConvThreads);
+    for (int i = 0; i < NR; ++i) {
+      mbar_init(bar(B_ROPE_FULL + i), 1);
       mbar_init(bar(B_ROPE_EMPTY + i), 1);
     }
     for (int i = 0; i < NC; ++i) {
       mbar_init(bar(B_C16_FULL + i), kConvThreads);
       mbar_init(bar(B_C16_EMPTY + i), 1);
     }
-    mbar_init(bar(B_S_FULL), 1);
-    mbar_init(bar(B_S_EMPTY), kSmWarps);     // latent scores read
-    mbar_init(bar(B_R_FULL), 1);
-    mbar_init(bar(B_R_EMPTY), kSmWarps);     // RoPE scores read
+    mbar_init(bar(B_S_FULL), 1);            // latent and RoPE partial scores of a tile
+    mbar_init(bar(B_S_EMPTY), kSmWarps);     // both read
     mbar_init(bar(B_P_FULL), kSmWarps);
     mbar_init(bar(B_PV_DONE), 1);
     mbar_init(bar(B_Q_READY), kSmWarps);
     mbar_init(bar(B_QR_FULL), 1);
     mbar_init(bar(B_QK_DONE), 1);
-    mbar_init(bar(B_XF), 1);          // armed with the expected bytes, filled by the peer's st.async
-    mbar_init(bar(B_XE), kSmWarps);
     mbar_init(bar(B_DRAIN), 1);
+    for (int i = 0; i < 2 * kSmWarps; ++i) {
+      mbar_init(bar(B_XF + i), 1);
+      mbar_init(bar(B_XE + i), 1);
+    }
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(B_PAIR_W + i), 2);    // both warps of a lane quarter wrote their value
       mbar_init(bar(B_PAIR_R + i), 2);    // both warps of a lane quarter read the other's value
     }
     *abort_flag = 0u;
-    *reinterpret_cast<volatile uint32_t*>(smem + OFF_YCNT) = 0u;
-    mbar_expect_tx(bar(B_XF), kXBytes);   // phase 0 of the partial-score exchange
+    // first use of every X region: expect the peer's 3 KB
+    for (int i = 0; i < 2 * kSmWarps; ++i) mbar_expect_tx(bar(B_XF + i), kXWarpBytes);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -466,86 +465,74 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();   // peer barriers are initialised before any remote arrive
+  cluster_sync();   // peer barriers are initialised before any remote arrive or copy
 
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
   const int64_t* sched = reinterpret_cast<const int64_t*>(smem + OFF_SCHED);
   SegWalk walk0{sched[2], sched[3], sched[1], (int)sched[0]};
-  const uint32_t tile_tx = (uint32_t)(kTok * DH) + (uint32_t)(kTok * 2 * p.Dr);
+  const uint32_t rope_tx = (uint32_t)(kTok * 2 * p.Dr);
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      SegWalk w = walk0;
-      int b, lo, hi, tb;
-      uint32_t it = 0;
-      bool ok = true;
-      while (ok && w.next(p, b, lo, hi, tb)) {
-        for (int tt = lo; tt < hi && ok; ++tt, ++it) {
-          const uint32_t st = it % NS, ph = (it / NS) & 1u;
-          ok = wait_bar(bar(B_STG_EMPTY + st), ph ^ 1u, abort_flag, p.err) &&
-               wait_bar(bar(B_ROPE_EMPTY + st), ph ^ 1u, abort_flag, p.err);
-          if (!ok) break;
-          mbar_expect_tx(bar(B_TILE_FULL + st), tile_tx);
-#pragma unroll
-          for (int j = 0; j < N_BOX; ++j)
-            tma_3d(sbase + OFF_STG + st * STG_BYTES + (uint32_t)(j * kTok * BOX_W), &p.tm_ckv,
-                   (int)rank * DH + j * BOX_W, tt * kTok, b, bar(B_TILE_FULL + st));
-          if (rope_chunks > 0)
-            tma_4d(sbase + OFF_ROPE + st * ROPE_BYTES, &p.tm_rope, 0, tt * kTok, 0, b, bar(B_TILE_FULL + st));
-        }
-      }
-      // Drain: every issued copy must land before the CTA may exit.
-      for (uint32_t k = (it >= NS ? it - NS : 0); k < it; ++k)
-        wait_bar(bar(B_TILE_FULL + k % NS), (k / NS) & 1u, abort_flag, p.err);
-    }
-  } else if (warp >= kConvWarp0) {
+  if (warp >= kConvWarp0) {
     // ------------------------------------------------------ int8 -> fp16 converters
+    // Unit u = (token u % 64, 16-byte chunk u / 64) of a tile; consecutive threads
+    // take consecutive tokens.  Each thread loads its units of the next tile into
+    // registers while the current one waits for its buffer.  Writes land as
+    // K-major core matrices (8 tokens x 16 bytes): consecutive threads write
+    // consecutive 16-byte rows, without bank conflicts.
+    // The first converter thread also streams the RoPE key tiles in with TMA.
     const int ct = tid - kConvWarp0 * 32;
-    SegWalk w = walk0;
-    int b, lo, hi, tb;
+    const bool rope_issuer = (ct == 0) && rope_chunks > 0;
+    TileWalk tw{walk0};
+    uint4 v[CONV_UNITS];
+    auto load = [&](int b, int tt) {
+#pragma unroll
+      for (int i = 0; i < CONV_UNITS; ++i) {
+        const int u = ct + kConvThreads * i, n = u % kTok, cc = u / kTok;
+        const int row = tt * kTok + n;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (u < CONV_TOTAL && row < p.T_max)
+          v[i] = __ldg(reinterpret_cast<const uint4*>(p.ckv + ((int64_t)b * p.T_max + row) * p.Dl + rank * DH) + cc);
+      }
+    };
+    bool more = tw.next(p);
+    if (more) load(tw.b, tw.tt);
     uint32_t it = 0;
     bool ok = true;
-    while (ok && w.next(p, b, lo, hi, tb)) {
-      for (int tt = lo; tt < hi && ok; ++tt, ++it) {
-        const uint32_t st = it % NS, cs = it % NC;
-        ok = wait_bar(bar(B_TILE_FULL + st), (it / NS) & 1u, abort_flag, p.err) &&
-             wait_bar(bar(B_C16_EMPTY + cs), ((it / NC) & 1u) ^ 1u, abort_flag, p.err);
-        if (!ok) break;
-        const uint8_t* stg = smem + OFF_STG + st * STG_BYTES;
-        uint8_t* c16 = smem + OFF_C16 + cs * C16_BYTES;
-        // Unit u = (token n, 16-byte latent chunk cc); consecutive threads take
-        // consecutive tokens, so both the swizzled reads and the core-matrix
-        // writes are conflict-free.  All loads are issued before any convert.
-        uint4 v[CONV_UNITS];
-#pragma unroll
-        for (int i = 0; i < CONV_UNITS; ++i) {
-          const int u = ct + kConvThreads * i;
-          const int n = u % kTok, cc = u / kTok;
-          const int j = cc / CPB, c = cc % CPB;
-          // TMA swizzle: the 16-byte chunk index is XORed with bits 7.. of the row address.
-          const uint32_t row_addr = (uint32_t)(n * BOX_W);
-          const uint32_t phys = ((uint32_t)c ^ ((row_addr >> 7) & SWZ_MASK)) * 16u;
-          v[i] = *reinterpret_cast<const uint4*>(stg + j * kTok * BOX_W + row_addr + phys);
+    for (; ok && more; ++it) {
+      if (rope_issuer) {
+        const uint32_t st = it % NR;
+        ok = wait_bar(bar(B_ROPE_EMPTY + st), ((it / NR) & 1u) ^ 1u, abort_flag, p.err);
+        if (ok) {
+          mbar_expect_tx(bar(B_ROPE_FULL + st), rope_tx);
+          tma_4d(sbase + OFF_ROPE + st * ROPE_BYTES, &p.tm_rope, 0, tw.tt * kTok, 0, tw.b, bar(B_ROPE_FULL + st));
         }
+      }
+      const uint32_t cs = it % NC;
+      ok = ok && wait_bar(bar(B_C16_EMPTY + cs), ((it / NC) & 1u) ^ 1u, abort_flag, p.err);
+      if (!ok) break;
+      uint8_t* c16 = smem + OFF_C16 + cs * C16_BYTES;
 #pragma unroll
-        for (int i = 0; i < CONV_UNITS; ++i) {
-          const int u = ct + kConvThreads * i;
-          const int n = u % kTok, cc = u / kTok;
+      for (int i = 0; i < CONV_UNITS; ++i) {
+        const int u = ct + kConvThreads * i, n = u % kTok, cc = u / kTok;
+        if (u < CONV_TOTAL) {
           uint4 o0, o1;
           i8x4_to_f16x4(v[i].x, o0.x, o0.y);
           i8x4_to_f16x4(v[i].y, o0.z, o0.w);
           i8x4_to_f16x4(v[i].z, o1.x, o1.y);
           i8x4_to_f16x4(v[i].w, o1.z, o1.w);
-          const int kc = 2 * cc;             // 8-wide latent chunk of the first 8 values
-          *reinterpret_cast<uint4*>(c16 + kc * 1024 + n * 16) = o0;
-          *reinterpret_cast<uint4*>(c16 + (kc + 1) * 1024 + n * 16) = o1;
+          *reinterpret_cast<uint4*>(c16 + (2 * cc) * 1024 + n * 16) = o0;
+          *reinterpret_cast<uint4*>(c16 + (2 * cc + 1) * 1024 + n * 16) = o1;
         }
-        fence_proxy_async();
-        mbar_arrive(bar(B_C16_FULL + cs));
-        mbar_arrive(bar(B_STG_EMPTY + st));
       }
+      fence_proxy_async();
+      mbar_arrive(bar(B_C16_FULL + cs));
+      more = tw.next(p);
+      if (more) load(tw.b, tw.tt);
     }
+    // Drain: every issued RoPE copy must land before the CTA may exit.
+    if (rope_issuer)
+      for (uint32_t k = (it >= NR ? it - NR : 0); k < it; ++k)
+        wait_bar(bar(B_ROPE_FULL + k % NR), (k / NR) & 1u, abort_flag, p.err);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -557,13 +544,15 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       int b, lo, hi, tb;
       uint32_t it = 0, seg = 0;
       bool ok = true;
+      // P.C of tile j; completion frees P and the C buffer.
       auto issue_pv = [&](uint32_t j, bool first) -> bool {
         if (!wait_bar(bar(B_P_FULL), j & 1u, abort_flag, p.err)) return false;
         tc_fence_after();
         const uint32_t cs = j % NC;
+        const uint32_t pbase = sbase + OFF_P;
 #pragma unroll
         for (int kk = 0; kk < kTok / 16; ++kk) {
-          const uint64_t a = sdesc(sbase + OFF_P + kk * 4096, 2048, 128);
+          const uint64_t a = sdesc(pbase + kk * 4096, 2048, 128);
           // MN-major, no swizzle: LBO strides the K (token) core groups, SBO the N (latent) ones.
           const uint64_t bd = sdesc(sbase + OFF_C16 + cs * C16_BYTES + kk * 256, 128, 1024);
           mma_f16(tmem + TM_O, a, bd, id_pv, (first && kk == 0) ? 0u : 1u);
@@ -572,34 +561,26 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         mma_commit(bar(B_C16_EMPTY + cs));
         return true;
       };
-      // Q.C^T of tile j into S (latent partial scores).
-      auto issue_qk = [&](uint32_t j) -> bool {
-        const uint32_t cs = j % NC;
+      // Q.C^T of tile j into S (latent partial scores) and this CTA's share of the
+      // RoPE term into R; the last tile of a segment also releases both query operands.
+      auto issue_qk = [&](uint32_t j, bool last) -> bool {
+        const uint32_t cs = j % NC, st = j % NR;
         if (!(wait_bar(bar(B_C16_FULL + cs), (j / NC) & 1u, abort_flag, p.err) &&
               wait_bar(bar(B_S_EMPTY), (j & 1u) ^ 1u, abort_flag, p.err)))
           return false;
+        if (rope_chunks > 0 && !wait_bar(bar(B_ROPE_FULL + st), (j / NR) & 1u, abort_flag, p.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint64_t bd = sdesc(sbase + OFF_C16 + cs * C16_BYTES + kk * 2048, 1024, 128);
           mma_f16_ts(tmem + TM_S, tmem + TM_QA + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(B_S_FULL));
-        return true;
-      };
-      // RoPE scores of tile j into R; the last tile of a segment also releases both query operands.
-      auto issue_rope = [&](uint32_t j, bool last) -> bool {
-        const uint32_t st = j % NS;
-        if (!(wait_bar(bar(B_TILE_FULL + st), (j / NS) & 1u, abort_flag, p.err) &&
-              wait_bar(bar(B_R_EMPTY), (j & 1u) ^ 1u, abort_flag, p.err)))
-          return false;
-        tc_fence_after();
-        for (int kk = 0; kk < p.Dr / 16; ++kk) {
+        for (int kk = rk0; kk < rk1; ++kk) {
           const uint64_t a = sdesc(sbase + OFF_QR + kk * 4096, 2048, 128);
           const uint64_t bd = sdesc(sbase + OFF_ROPE + st * ROPE_BYTES + kk * 2048, 1024, 128);
-          mma_f16(tmem + TM_R, a, bd, id_rope, kk > 0 ? 1u : 0u);
+          mma_f16(tmem + TM_R, a, bd, id_rope, kk > rk0 ? 1u : 0u);
         }
-        mma_commit(bar(B_R_FULL));
+        mma_commit(bar(B_S_FULL));
         mma_commit(bar(B_ROPE_EMPTY + st));
         if (last) mma_commit(bar(B_QK_DONE));
         return true;
@@ -616,14 +597,13 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         }
         ok = ok && wait_bar(bar(B_Q_READY), seg & 1u, abort_flag, p.err);   // latent query in TMEM
         ++seg;
-        // Order on the tensor pipe: Q.C^T runs two tiles and the RoPE term one tile
-        // ahead of P.C, so that the softmax finds the next tile's partial scores
-        // ready while it works on the current one.
+        // Order on the tensor pipe: Q.C^T runs two tiles ahead of P.C, so that the
+        // softmax finds the next tile's partial scores ready while it works on the
+        // current one.
         const uint32_t n = (uint32_t)(hi - lo), base = it;
-        ok = ok && issue_qk(base) && issue_rope(base, n == 1) && (n < 2 || issue_qk(base + 1));
+        ok = ok && issue_qk(base, n == 1) && (n < 2 || issue_qk(base + 1, n == 2));
         for (uint32_t k = 0; k < n && ok; ++k) {
-          if (k + 1 < n) ok = issue_rope(base + k + 1, k + 2 == n);
-          if (ok && k + 2 < n) ok = issue_qk(base + k + 2);
+          if (k + 2 < n) ok = issue_qk(base + k + 2, k + 3 == n);
           if (ok) ok = issue_pv(base + k, k == 0);
         }
         it = base + n;
@@ -645,9 +625,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const float kvs = p.kv_scale[0];
     const float c_rope = p.sm_log2;
     const float c_lat = (h < p.H ? p.q_scale[h] : 0.f) * kvs * p.sm_log2;
+    const uint32_t region = (uint32_t)warp * kXWarpBytes + (uint32_t)lane * 16;   // + slot, + chunk * 512
     const uint32_t peer_x = mapa(sbase + OFF_X, peer);
     const uint32_t peer_xf = mapa(bar(B_XF), peer);
-    const uint32_t peer_xe = mapa(bar(B_XE), peer);
     // Column ranges of O (fp32 words) and of the fp16 query (32-bit words) this warp handles.
     constexpr int O_PER = DH >= 64 ? DH / 2 : DH;
     constexpr int QW = DH / 2, QW_PER = QW >= 16 ? QW / 2 : QW;
@@ -660,43 +640,45 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(which));
     };
-    // Own latent partial of tile j -> Y as 24-bit fields (this warp's 32 tokens),
-    // then one bulk copy of Y into the peer's X that completes on the peer's XF.
+    const uint32_t peer_xe = mapa(bar(B_XE), peer);
+    const bool has_rope = rk1 > rk0;
+    // This CTA's partial score of tile j for this warp's 32 tokens, in log2 units:
+    //   (latent partial) * q_scale * kv_scale * c + (RoPE share) * c.
+    // It stays in registers (own) and goes, as fp32, into the peer's X slot by
+    // st.async; both CTAs then add the same two values, so their scores agree bit
+    // for bit.
+    float own[32];
     auto send_partial = [&](uint32_t j) -> bool {
-      // XE: the peer has consumed tile j-1, so the previous copy out of Y is complete.
+      const uint32_t s = j & 1u, xe = s * kSmWarps + (uint32_t)warp;
+      // XE: the peer's warp has read tile j-2 from this slot.
       if (!warp_all(wait_bar(bar(B_S_FULL), j & 1u, abort_flag, p.err)) ||
-          !warp_all(wait_bar(bar(B_XE), (j & 1u) ^ 1u, abort_flag, p.err, true)))
+          !warp_all(wait_bar(bar(B_XE + xe), ((j >> 1) & 1u) ^ 1u, abort_flag, p.err, true)))
         return false;
       tc_fence_after();
-      uint32_t v[32];
-      FA3_TMEM_LD16(tmem + lane_base + TM_S + hf * 32, v);
-      FA3_TMEM_LD16(tmem + lane_base + TM_S + hf * 32 + 16, (v + 16));
-      tmem_wait_ld();
+      const uint32_t dst = peer_x + s * kXSlotBytes + region;
+      const uint32_t rbar = peer_xf + 8u * xe;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t v[16], r[16];
+        FA3_TMEM_LD16(tmem + lane_base + TM_S + hf * 32 + hh * 16, v);
+        if (has_rope) FA3_TMEM_LD16(tmem + lane_base + TM_R + hf * 32 + hh * 16, r);
+        tmem_wait_ld();
+        float* o = own + 16 * hh;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          float r0 = 0.f, r1 = 0.f;
+          if (has_rope) mul2(r0, r1, __uint_as_float(r[i]), __uint_as_float(r[i + 1]), c_rope, c_rope);
+          fma2(o[i], o[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), c_lat, c_lat, r0, r1);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                       ::"r"(dst + (4 * hh + c) * 512), "r"(__float_as_uint(o[4 * c])),
+                         "r"(__float_as_uint(o[4 * c + 1])), "r"(__float_as_uint(o[4 * c + 2])),
+                         "r"(__float_as_uint(o[4 * c + 3])), "r"(rbar) : "memory");
+      }
       tc_fence_before();
       warp_arrive(B_S_EMPTY);
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        const int q = 2 * hf + qq;                         // 16-token group of the tile
-        uint32_t wv[12];
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-          pack_fields(__uint_as_float(v[16 * qq + 4 * g]), __uint_as_float(v[16 * qq + 4 * g + 1]),
-                      __uint_as_float(v[16 * qq + 4 * g + 2]), __uint_as_float(v[16 * qq + 4 * g + 3]), wv[3 * g],
-                      wv[3 * g + 1], wv[3 * g + 2]);
-#pragma unroll
-        for (int c = 0; c < 3; ++c)
-          *reinterpret_cast<uint4*>(smem + OFF_Y + ((3 * q + c) * kRows + h) * 16) =
-              make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
-      }
-      fence_proxy_async();                                  // Y is read by the bulk-copy engine
-      __syncwarp();
-      if (lane == 0) {
-        // The last softmax warp to finish its part of Y starts the copy.
-        uint32_t done;
-        asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
-                     : "=r"(done) : "r"(sbase + OFF_YCNT) : "memory");
-        if ((done & (kSmWarps - 1)) == kSmWarps - 1) bulk_s2cluster(peer_x, sbase + OFF_Y, kXBytes, peer_xf);
-      }
       return true;
     };
     // Swaps one float per head with the other warp of this lane quarter, in two
@@ -738,72 +720,35 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
       const int len = p.lens[b];
       float m_ref = -CUDART_INF_F, l = 0.f;
-      // The own partial of the next tile goes out right after this tile's scores,
-      // so the cluster copy overlaps this tile's softmax.
       ok = send_partial(it);
       for (int tt = lo; tt < hi && ok; ++tt, ++it) {
+        const uint32_t s = it & 1u, use = (it >> 1) & 1u, xs = s * kSmWarps + (uint32_t)warp;
         const int nvalid = min(kTok, len - tt * kTok) - hf * 32;   // valid tokens in this warp's half
-        ok = warp_all(wait_bar(bar(B_XF), it & 1u, abort_flag, p.err, true));
+        ok = warp_all(wait_bar(bar(B_XF + xs), use, abort_flag, p.err, true));
         if (!ok) break;
-        // ---- exact latent sums of this warp's 32 tokens (own + peer partial):
-        //      (M + v_own) + (M + v_peer - 2M), every step exact
-        float lat[32];
+        // ---- scores: own + peer partial (the same two values in both CTAs)
+        float part[32];
         {
-          uint32_t xw[24], yw[24];
+          const uint32_t xo_ = OFF_X + s * kXSlotBytes + region;
 #pragma unroll
-          for (int c = 0; c < 6; ++c) {
-            const uint32_t off = ((6 * hf + c) * kRows + h) * 16;
-            const uint4 xo = *reinterpret_cast<const uint4*>(smem + OFF_X + off);
-            const uint4 yo = *reinterpret_cast<const uint4*>(smem + OFF_Y + off);
-            xw[4 * c] = xo.x; xw[4 * c + 1] = xo.y; xw[4 * c + 2] = xo.z; xw[4 * c + 3] = xo.w;
-            yw[4 * c] = yo.x; yw[4 * c + 1] = yo.y; yw[4 * c + 2] = yo.z; yw[4 * c + 3] = yo.w;
-          }
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            float xp[4], xs[4];
-            unpack_fields(xw[3 * g], xw[3 * g + 1], xw[3 * g + 2], xp);
-            unpack_fields(yw[3 * g], yw[3 * g + 1], yw[3 * g + 2], xs);
-#pragma unroll
-            for (int i = 0; i < 4; i += 2) {
-              float t0, t1;
-              add2(t0, t1, xp[i], xp[i + 1], -2.f * kMagic, -2.f * kMagic);
-              add2(lat[4 * g + i], lat[4 * g + i + 1], xs[i], xs[i + 1], t0, t1);
-            }
+          for (int c = 0; c < kXChunks; ++c) {
+            const float4 xo = *reinterpret_cast<const float4*>(smem + xo_ + c * 512);
+            add2(part[4 * c], part[4 * c + 1], own[4 * c], own[4 * c + 1], xo.x, xo.y);
+            add2(part[4 * c + 2], part[4 * c + 3], own[4 * c + 2], own[4 * c + 3], xo.z, xo.w);
           }
         }
-        // X and Y have been consumed (every loaded word fed the sums above): re-arm
-        // XF for the next tile, free X for the peer and send the next partial,
-        // so that the cluster copy overlaps the rest of this tile's softmax.
-        if (tid == 0) mbar_expect_tx(bar(B_XF), kXBytes);
+        // This warp's X region is consumed: expect the peer's tile after next and
+        // tell the peer's warp that the region is free.
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(peer_xe);
+        if (lane == 0) {
+          mbar_expect_tx(bar(B_XF + xs), kXWarpBytes);
+          mbar_arrive_remote(peer_xe + 8u * xs);
+        }
+        // The next tile's partial goes out now: its copy has the rest of this tile to land.
         if (tt + 1 < hi) {
           ok = send_partial(it + 1);
           if (!ok) break;
         }
-        // ---- scores: the RoPE term is computed identically in both CTAs, so both
-        //      hold bit-identical scores
-        ok = warp_all(wait_bar(bar(B_R_FULL), it & 1u, abort_flag, p.err));
-        if (!ok) break;
-        tc_fence_after();
-        float part[32];
-        if (p.Dr > 0) {
-          uint32_t r[32];
-          FA3_TMEM_LD16(tmem + lane_base + TM_R + hf * 32, r);
-          FA3_TMEM_LD16(tmem + lane_base + TM_R + hf * 32 + 16, (r + 16));
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float r0, r1;
-            mul2(r0, r1, __uint_as_float(r[i]), __uint_as_float(r[i + 1]), c_rope, c_rope);
-            fma2(part[i], part[i + 1], lat[i], lat[i + 1], c_lat, c_lat, r0, r1);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) mul2(part[i], part[i + 1], lat[i], lat[i + 1], c_lat, c_lat);
-        }
-        tc_fence_before();
-        warp_arrive(B_R_EMPTY);
         if (nvalid < 32) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) part[jj] = jj < nvalid ? part[jj] : -CUDART_INF_F;
@@ -815,10 +760,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         mx[10] = fmaxf(part[30], part[31]);
         const float mh = fmaxf(max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), max3(mx[6], mx[7], mx[8])),
                                fmaxf(mx[9], mx[10]));
-        ok = pair_put(mh);
-        if (!ok) break;
         float mo;
-        ok = pair_get(mo);
+        ok = pair_put(mh) && pair_get(mo);
         if (!ok) break;
         const float mt = fmaxf(mh, mo);
 
@@ -854,6 +797,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
               make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
         // The rescale is decided per head (lane) but tcgen05.ld/st are warp-wide:
         // the whole warp takes part, lanes that keep their reference scale by 1.
+        // O must already hold P.C of the previous tile.
         if (__any_sync(0xffffffffu, rescale)) {
           if (!rescale) alpha = 1.f;
 #pragma unroll 1
@@ -877,7 +821,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       float lo_sum;
       ok = pair_put(l) && pair_get(lo_sum);
       if (!ok) break;
-      const float l_row = hf == 0 ? l + lo_sum : lo_sum + l;   // the same order in both warps
+      const float l_row = l + lo_sum;
       ok = warp_all(wait_bar(bar(B_PV_DONE), (it - 1) & 1u, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
@@ -1141,20 +1085,6 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   MlaParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.DH = Dl / 2;
-  {
-    const int box_w = prm.DH < 128 ? prm.DH : 128;
-    const cuuint64_t dims[3] = {(cuuint64_t)Dl, (cuuint64_t)T_max, (cuuint64_t)B};
-    const cuuint64_t strides[2] = {(cuuint64_t)Dl, (cuuint64_t)Dl * T_max};
-    const cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)kTok, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    const CUtensorMapSwizzle sw = box_w == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : box_w == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                                : CU_TENSOR_MAP_SWIZZLE_32B;
-    if (encode(&prm.tm_ckv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t*>(ckv), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return FA3_ECUDA;
-  }
   if (Dr > 0) {
     // (8 values, token, 8-wide chunk, sequence): one box lands as K-major core matrices.
     const cuuint64_t dims[4] = {8, (cuuint64_t)T_max, (cuuint64_t)(Dr / 8), (cuuint64_t)B};
@@ -1167,7 +1097,7 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
       return FA3_ECUDA;
   }
   char* ws = static_cast<char*>(workspace);
-  prm.q = q; prm.q_scale = q_scale; prm.kv_scale = kv_scale; prm.lens = lens; prm.out = out;
+  prm.q = q; prm.ckv = ckv; prm.q_scale = q_scale; prm.kv_scale = kv_scale; prm.lens = lens; prm.out = out;
   prm.part_o = reinterpret_cast<float*>(ws);
   prm.part_ml = reinterpret_cast<float2*>(ws + off_ml);
   prm.q_lat = reinterpret_cast<uint16_t*>(ws + off_qlat);
