@@ -254,15 +254,16 @@ def run_gpu(args):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = torch.empty(F.mla_workspace_size(B, H, DL, T), dtype=torch.uint8, device=dev)
 
-    def step(i, mla_events=None):
+    def step(i, ev=None):
         c = i % NC
         F.quantize_append(new_kv[c], kv_scale, caches[c], pos, new_rope[c], ropes[c], err)
-        if mla_events is not None:
-            mla_events[0].record(stream)
+        if ev is not None:
+            ev[0].record(stream)                     # the whole decode call ...
+            F.set_kernel_timing(ev[2], ev[3])        # ... and, recorded by the library, its main kernel
         F.decode_attn_mla(qs[c], caches[c][:, :, 0], ropes[c], q_scale, kv_scale, lens, SOFTMAX_SCALE, out=out,
                           workspace=ws, dev_err=err)
-        if mla_events is not None:
-            mla_events[1].record(stream)
+        if ev is not None:
+            ev[1].record(stream)
 
     for i in range(args.warmup):
         step(i)
@@ -270,7 +271,11 @@ def run_gpu(args):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
 
-    mla_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    mla_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
+    for evs in mla_ev:                                  # create the CUDA events before the timed region
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         if world > 1:
             dist.barrier()
@@ -290,8 +295,10 @@ def run_gpu(args):
         tt = torch.tensor([ms_total], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_total = float(tt.item())
+    F.set_kernel_timing(None, None)
     ms_step = ms_total / args.steps
-    mla_ms = statistics.mean(a.elapsed_time(b) for a, b in mla_ev)
+    mla_ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in mla_ev)
+    kern_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in mla_ev)
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
     hq = qs[0].cpu().pin_memory()
@@ -332,8 +339,9 @@ def run_gpu(args):
     bf16 = pk.get("bf16_tflops", 1900.0)
     tokens = B * world
     value = tokens / (ms_step / 1e3)
-    kv_gbs = kv_bytes_per_step() / (mla_ms / 1e3) / 1e9
-    tflops = flops_per_step() / (mla_ms / 1e3) / 1e12
+    kv_gbs = kv_bytes_per_step() / (mla_ms / 1e3) / 1e9           # whole decode call
+    k_tflops = flops_per_step() / (kern_ms / 1e3) / 1e12          # main kernel alone
+    k_gbs = kv_bytes_per_step() / (kern_ms / 1e3) / 1e9
     traffic = recorded_traffic()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -350,12 +358,19 @@ def run_gpu(args):
                    "step": "quantize-append of the new token + MLA decode (+ split-K combine)",
                    "l2": "inputs larger than L2: 167.8 MB of KV per step, two cache copies rotated"},
         "kv_gbs": kv_gbs, "kv_hbm_frac_of_measured": kv_gbs / hbm,
-        "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s",
-                     "frac": tflops / bf16, "traffic": traffic,
-                     "kernel": "fa3_decode_attn_mla call = query pre-pass + mla_decode_kernel + combine "
-                               "(CUDA events around the call); traffic: mla_decode_kernel alone, from ncu",
-                     "peak_source": "measured bf16 dense (burst), MEASURED_PEAKS.json; f16 runs at the bf16 rate"},
-        "hbm_roofline": {"achieved": kv_gbs, "peak": hbm, "unit": "GB/s", "frac": kv_gbs / hbm},
+        "roofline": {"bound": "tensor", "achieved": k_tflops, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": k_tflops / bf16, "traffic": traffic,
+                     "kernel": "mla_decode_kernel", "ms_per_launch": kern_ms,
+                     "algorithmic": f"{flops_per_step() / 1e9:.2f} GFLOP per launch (2*B*T*H*(2*Dl+Dr))",
+                     "timing": "CUDA events recorded by the library around the kernel (fa3_set_kernel_timing), "
+                               "every timed step, on the launching stream",
+                     "peak_source": "measured bf16 dense burst (MEASURED_PEAKS.json), of measured; f16 runs at "
+                                    "the bf16 rate",
+                     "frac_of_sustained": k_tflops / pk.get("bf16_tflops_sustained", bf16)},
+        "hbm_roofline": {"kernel": "mla_decode_kernel", "achieved": k_gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": k_gbs / hbm},
+        "decode_call": {"ms": mla_ms, "kv_gbs": kv_gbs, "tflops": flops_per_step() / (mla_ms / 1e3) / 1e12,
+                        "kernels": "query pre-pass + mla_decode_kernel + split-K combine"},
         "calibration": {"workload": "B=4 H=128 S=2048 D=192 bf16, ratio 0.9999", "ms_per_batch": cal_ms,
                         "gbs": 4 * H * 2048 * 192 * 2 / (cal_ms / 1e3) / 1e9},
         "cpu_baseline": cpu,

@@ -59,6 +59,17 @@ const char* fa3_status_string(int status);
 /* Library ABI version (major*100 + minor). */
 int fa3_version(void);
 
+/* Measurement aid (no counterpart in the pages).  When both events are
+ * non-NULL, every later call of fa3_decode_attn_mla, fa3_decode_attn_gqa and
+ * fa3_calibrate_perhead records start_event on its stream just before its
+ * main kernel (the MLA decode, the GQA decode, the calibration histogram) and
+ * stop_event just after it, so that the caller can time that kernel alone
+ * (cudaEventElapsedTime).  The events are cudaEvent_t passed as void*, owned
+ * by the caller and must outlive their use; NULL, NULL turns this off.  One
+ * setting for the whole process, not synchronized between host threads.
+ * Returns FA3_EINVAL when exactly one of the two is NULL. */
+int fa3_set_kernel_timing(void* start_event, void* stop_event);
+
 /* ------------------------------------------------------------------------
  * Calibration -- msModelSlim FA3量化, 原理 / 算法流程 steps 1-3.
  *

@@ -364,8 +364,10 @@ FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L
   }
   const unsigned grid = (unsigned)(total_chunks < sms ? total_chunks : sms);
   uint32_t* counts = static_cast<uint32_t*>(workspace);
+  timing_begin(s);
   hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, chunks_per_head, (int)total_chunks,
                                                 counts, vec);
+  timing_end(s);
   if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
   const bool fast = (uint64_t)(N - t + 1) <= (uint64_t)kCandCap;
   const int wsmem = fast ? (int)((N - t + 1) * sizeof(uint32_t)) : 0;

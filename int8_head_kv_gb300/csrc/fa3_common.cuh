@@ -13,6 +13,10 @@ namespace fa3 {
 // Host-side check for the current device; the kernels are built for sm_103a only.
 int check_device(int* num_sms);
 
+// Optional caller events recorded around the main kernel of a call (fa3_set_kernel_timing).
+void timing_begin(cudaStream_t s);
+void timing_end(cudaStream_t s);
+
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA3_OK : FA3_ECUDA; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

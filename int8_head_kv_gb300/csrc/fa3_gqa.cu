@@ -366,7 +366,9 @@ FA3_API int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* 
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = G; a.T_max = T_max; a.splits = splits; a.chunk = chunk;
   a.sm_log2 = softmax_scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  timing_begin(s);
   gqa_decode_kernel<<<dim3(splits, Hkv, B), kThreads, 0, s>>>(a);
+  timing_end(s);
   if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
   if (splits > 1) {
     gqa_combine_kernel<<<dim3(Hq, B), kD, 0, s>>>(a);

@@ -1131,12 +1131,14 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   cudaError_t le = cudaErrorInvalidValue;
+  timing_begin(s);
   switch (prm.DH) {
     case 32: le = launch_mla<32>(cfg, prm); break;
     case 64: le = launch_mla<64>(cfg, prm); break;
     case 128: le = launch_mla<128>(cfg, prm); break;
     case 256: le = launch_mla<256>(cfg, prm); break;
   }
+  timing_end(s);
   if (le != cudaSuccess) return FA3_ECUDA;
   mla_combine_kernel<<<dim3(H, B), Dl / 4, 0, s>>>(prm);
   return cuda_status(cudaGetLastError());

@@ -9,6 +9,17 @@
 
 namespace fa3 {
 
+namespace {
+cudaEvent_t g_timing_start = nullptr, g_timing_stop = nullptr;
+}  // namespace
+
+void timing_begin(cudaStream_t s) {
+  if (g_timing_start && g_timing_stop) cudaEventRecord(g_timing_start, s);
+}
+void timing_end(cudaStream_t s) {
+  if (g_timing_start && g_timing_stop) cudaEventRecord(g_timing_stop, s);
+}
+
 int check_device(int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA3_ECUDA;
@@ -139,6 +150,13 @@ FA3_API const char* fa3_status_string(int status) {
 }
 
 FA3_API int fa3_version(void) { return 100; }
+
+FA3_API int fa3_set_kernel_timing(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return FA3_EINVAL;
+  g_timing_start = static_cast<cudaEvent_t>(start_event);
+  g_timing_stop = static_cast<cudaEvent_t>(stop_event);
+  return FA3_OK;
+}
 
 FA3_API int fa3_qparams(const float* min_v, const float* max_v, float* scale, int H, void* stream) {
   if (!min_v || !max_v || !scale || H <= 0) return FA3_EINVAL;

@@ -37,6 +37,7 @@ _D = ctypes.c_double
 _SIGS = {
     "fa3_status_string": (ctypes.c_char_p, [_I]),
     "fa3_version": (_I, []),
+    "fa3_set_kernel_timing": (_I, [_P, _P]),
     "fa3_calibrate_workspace_size": (_SZ, [_I]),
     "fa3_calibrate_perhead": (_I, [_P, _I64, _I, _I64, _I64, _I64, _D, _P, _P, _P, _SZ, _P]),
     "fa3_qparams": (_I, [_P, _P, _P, _I, _P]),
@@ -108,6 +109,15 @@ def _workspace(key, nbytes: int, device, zero: bool = False) -> Optional[torch.T
 
 
 # --------------------------------------------------------------------- calls
+def set_kernel_timing(start: Optional["torch.cuda.Event"], stop: Optional["torch.cuda.Event"]):
+    """fa3_set_kernel_timing: later decode / calibration calls record these events
+    around their main kernel (None, None turns it off).  The events must have been
+    recorded once, so that their CUDA handles exist."""
+    a = None if start is None else ctypes.c_void_p(start.cuda_event)
+    b = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+    _check("fa3_set_kernel_timing", lib().fa3_set_kernel_timing(a, b))
+
+
 def calibrate_workspace_size(H: int) -> int:
     return int(lib().fa3_calibrate_workspace_size(H))
 

@@ -75,3 +75,10 @@ def test_gqa_validation(L):
     assert call(Hq=60) == EINVAL          # not a multiple of Hkv
     assert call(D=64) == ERANGE
     assert call(Hq=128, Hkv=8) == ERANGE  # 16 query heads per KV head
+
+
+def test_kernel_timing_hook_validation(L):
+    # exactly one event is an error; none turns the hook off (no CUDA call either way)
+    assert L.fa3_set_kernel_timing(None, FAKE) == EINVAL
+    assert L.fa3_set_kernel_timing(FAKE, None) == EINVAL
+    assert L.fa3_set_kernel_timing(None, None) == 0
