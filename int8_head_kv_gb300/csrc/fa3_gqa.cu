@@ -33,6 +33,12 @@ constexpr int kD = 128;
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kHeadsPerTile = 8;
+#ifndef FA3_GQA_STAGES
+#define FA3_GQA_STAGES 4
+#endif
+constexpr int kStages = FA3_GQA_STAGES;         // cp.async ring depth per warp
+constexpr int kStageBytes = 2 * 16 * kD;        // one 16-token step: K then V rows (4 KB)
+constexpr int kSmemBytes = kWarps * kStages * kStageBytes;
 
 struct GqaArgs {
   const int8_t* q;
@@ -86,8 +92,17 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t x) {
   return __half22float2(h);
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const int8_t* p) {
-  return __ldcs(reinterpret_cast<const uint4*>(p));
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
@@ -95,9 +110,15 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
 }
 
 __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
-  __shared__ float sm_o[kWarps][kHeadsPerTile][kD];
+  // Per-warp rings of 16-token K/V steps.  A 128-byte row stores its 16-byte
+  // chunk c at position c ^ f(row & 7), f(r) = (r & 6) ^ 4 (r & 1): every 8-lane
+  // phase of the K and V fragment loads below then touches 8 distinct 16-byte
+  // bank groups.  After the token loop the same memory holds the warps' partial O.
+  extern __shared__ __align__(128) uint8_t gsm[];
+  float (*sm_o)[kHeadsPerTile][kD] = reinterpret_cast<float (*)[kHeadsPerTile][kD]>(gsm);
   __shared__ float sm_m[kWarps][kHeadsPerTile];
   __shared__ float sm_l[kWarps][kHeadsPerTile];
+  static_assert(kWarps * kHeadsPerTile * kD * 4 <= kSmemBytes, "partial O fits in the rings");
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -142,27 +163,49 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
   const int8_t* kbase = p.k + ((int64_t)b * p.T_max) * tok_stride + (int64_t)g * kD;
   const int8_t* vbase = p.v + ((int64_t)b * p.T_max) * tok_stride + (int64_t)g * kD;
 
-  auto load_tile = [&](int t0, uint4 (&kr)[4], uint4 (&vr)[4]) {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    const int ta = t0 + r, tb = t0 + r + 8;
-    kr[0] = ta < t_end ? ldg_stream(kbase + ta * tok_stride + 16 * qd) : z;
-    kr[1] = ta < t_end ? ldg_stream(kbase + ta * tok_stride + 64 + 16 * qd) : z;
-    kr[2] = tb < t_end ? ldg_stream(kbase + tb * tok_stride + 16 * qd) : z;
-    kr[3] = tb < t_end ? ldg_stream(kbase + tb * tok_stride + 64 + 16 * qd) : z;
-    const int tv[4] = {t0 + 2 * qd, t0 + 2 * qd + 1, t0 + 2 * qd + 8, t0 + 2 * qd + 9};
+  const uint32_t ring = (uint32_t)__cvta_generic_to_shared(gsm) + (uint32_t)(warp * kStages * kStageBytes);
+  auto swz = [](int row) { return (row & 6) ^ ((row & 1) << 2); };
+  // Step it of the CTA's range (16 tokens) -> ring stage: 256 chunks of 16 bytes,
+  // 8 per lane; rows past the range are zero-filled (their scores are masked).
+  auto issue = [&](int it, int stage) {
+    const int t0 = t_begin + 16 * it;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) vr[i] = tv[i] < t_end ? ldg_stream(vbase + tv[i] * tok_stride + 16 * r) : z;
+    for (int k = 0; k < 8; ++k) {
+      const int i = lane + 32 * k, kv = i >> 7, row = (i >> 3) & 15, col = i & 7;
+      const int t = t0 + row;
+      const bool ok = t < t_end;
+      const int8_t* src = (kv ? vbase : kbase) + (int64_t)(ok ? t : t_begin) * tok_stride + col * 16;
+      cp_async16(ring + stage * kStageBytes + kv * 2048 + row * 128 + ((col ^ swz(row)) << 4), src, ok ? 16u : 0u);
+    }
   };
+  auto chunk_addr = [&](uint32_t base, int row, int col) { return base + row * 128 + ((col ^ swz(row)) << 4); };
 
   const int span = t_end - t_begin;
   const int n_tiles = span > 0 ? (span + 15) / 16 : 0;
-  uint4 kr[4], vr[4];
-  if (warp < n_tiles) load_tile(t_begin + 16 * warp, kr, vr);
-  for (int it = warp; it < n_tiles; it += kWarps) {
+  const int n_my = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;   // steps warp, warp+4, ...
+#pragma unroll
+  for (int m = 0; m < kStages - 1; ++m) {
+    if (m < n_my) issue(warp + kWarps * m, m);
+    cp_async_commit();
+  }
+  for (int m = 0; m < n_my; ++m) {
+    const int it = warp + kWarps * m;
     const int t0 = t_begin + 16 * it;
-    uint4 nkr[4], nvr[4];
-    if (it + kWarps < n_tiles) load_tile(t0 + 16 * kWarps, nkr, nvr);
-
+    if (m + kStages - 1 < n_my) issue(it + kWarps * (kStages - 1), (m + kStages - 1) % kStages);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const uint32_t kst = ring + (m % kStages) * kStageBytes, vst = kst + 2048;
+    uint4 kr[4], vr[4];
+    kr[0] = lds128(chunk_addr(kst, r, qd));
+    kr[1] = lds128(chunk_addr(kst, r, 4 + qd));
+    kr[2] = lds128(chunk_addr(kst, r + 8, qd));
+    kr[3] = lds128(chunk_addr(kst, r + 8, 4 + qd));
+    vr[0] = lds128(chunk_addr(vst, 2 * qd, r));
+    vr[1] = lds128(chunk_addr(vst, 2 * qd + 1, r));
+    vr[2] = lds128(chunk_addr(vst, 2 * qd + 8, r));
+    vr[3] = lds128(chunk_addr(vst, 2 * qd + 9, r));
+    __syncwarp();   // every lane has its fragments: the stage may be refilled
     // ---- scores S^T = K . Q^T (exact integer dot products in fp32)
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -213,13 +256,11 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
       i8x4_to_f16x4(p23, a2, a3);
       mma16816(o[i], a0, a1, a2, a3, b0, b1);
     }
-    if (it + kWarps < n_tiles) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) { kr[i] = nkr[i]; vr[i] = nvr[i]; }
-    }
   }
+  cp_async_wait<0>();
 
-  // ---- merge the 4 warps of the CTA
+  // ---- merge the 4 warps of the CTA (the rings become the partial-O buffer)
+  __syncthreads();
 #pragma unroll
   for (int o_ = 4; o_ < 32; o_ <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
@@ -315,7 +356,10 @@ int gqa_blocks_per_sm() {
   static int cached = 0;
   if (cached <= 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel, kThreads, 0) != cudaSuccess || n <= 0)
+    if (cudaFuncSetAttribute(gqa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel, kThreads, kSmemBytes) != cudaSuccess ||
+        n <= 0)
       n = 3;
     cached = n;
   }
@@ -366,8 +410,10 @@ FA3_API int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* 
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = G; a.T_max = T_max; a.splits = splits; a.chunk = chunk;
   a.sm_log2 = softmax_scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaFuncSetAttribute(gqa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    return FA3_ECUDA;
   timing_begin(s);
-  gqa_decode_kernel<<<dim3(splits, Hkv, B), kThreads, 0, s>>>(a);
+  gqa_decode_kernel<<<dim3(splits, Hkv, B), kThreads, kSmemBytes, s>>>(a);
   timing_end(s);
   if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
   if (splits > 1) {
