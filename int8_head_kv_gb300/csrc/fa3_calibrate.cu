@@ -22,7 +22,18 @@
 //             P(v) + target_num - 1.  Width in float64, argmin with ties to the
 //             smallest start, then the running min/max update.  The kernel
 //             zeroes the bins it read, leaving the workspace clean.
+// When few windows exist (N - target_num + 1 <= 16384, e.g. ratio 0.9999), every
+// window starts among the N - target_num + 1 smallest values and ends among the
+// as many largest, so only the two tails of a head need counting: a sampling
+// kernel picks per-head tail thresholds, kernel 1 counts only keys beyond them
+// (HBM-bound instead of atomic-bound), and kernel 2 places the uncounted middle
+// as one block of known size between the tails, checking that each tail holds
+// enough values.  A head that fails the check is counted again in full by a
+// second launch of kernel 2, which returns at once for every other head; the
+// result is the same exact window either way.
 #include "fa3_common.cuh"
+
+#include <math_constants.h>
 
 namespace fa3 {
 namespace {
@@ -35,6 +46,17 @@ constexpr int kScalarPerThread = (kChunk + kHistThreads - 1) / kHistThreads;    
 constexpr int kWinThreads = 1024;
 constexpr int kBinsPerThread = kBins / kWinThreads;  // 64
 constexpr int kCandCap = 16384;     // window starts the fast search can table (N - t + 1 <= kCandCap)
+constexpr int kSampleUnits = 512;   // strided samples per head for the tail thresholds (16-byte groups or values)
+constexpr int kSampleThreads = 256;
+constexpr int kTailThreads = 256;
+constexpr int kTailGroups = 8;      // 16-byte groups per thread of the tail-count kernel
+
+// Per-head state of the tail-only path, in the workspace after the counters.
+// key_lo / key_hi: count keys <= key_lo or >= key_hi (key_lo = 0xffff: all keys);
+// flag: the tails were too thin, count this head again in full.
+struct TailInfo {
+  uint32_t key_lo, key_hi, flag, pad;
+};
 
 // Order-preserving 16-bit key of a bf16 value: positive values get the top bit
 // set, negative values are bit-inverted, so key order == value order and -0.0
@@ -55,27 +77,53 @@ __device__ __forceinline__ uint32_t bf16x2_keys(uint32_t w) {
 __device__ __forceinline__ void count16(uint32_t* bins, uint32_t key) {
   atomicAdd(&bins[key >> 1], 1u << ((key & 1u) << 4));
 }
+// Counts `key` only if it lies in a counted tail (key <= lo or key >= hi).
+__device__ __forceinline__ void count16_tails(uint32_t* bins, uint32_t key, uint32_t lo, uint32_t hi) {
+  if (key <= lo || key >= hi) count16(bins, key);
+}
 
-// Counts the 8 values of one 16-byte group.  When the whole warp holds one and the
-// same 16 bytes made of a single repeated value (a constant head), one lane adds
-// 256 at once instead of 256 conflicting atomics.
-__device__ __forceinline__ void count_group(uint32_t* bins, const uint4 v, bool valid) {
+// Packed bf16x2 min / max (IEEE: -0 == +0).
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Counts the 8 values of one 16-byte group (only keys <= lo or >= hi).  The common
+// case, no counted key in the whole warp's groups, is ruled out by comparing the
+// group's bf16 min and max with the values of the thresholds (strictly, so a tie or
+// a signed zero at a threshold always takes the exact per-key path) and one vote.
+// When the whole warp holds one and the same 16 bytes made of a single repeated
+// value (a constant head), one lane adds 256 at once instead of 256 conflicting
+// atomics.
+__device__ __forceinline__ void count_group(uint32_t* bins, const uint4 v, bool valid, uint32_t lo, uint32_t hi,
+                                            float v_lo, float v_hi) {
+  const uint32_t mn = bmin2(bmin2(v.x, v.y), bmin2(v.z, v.w)), mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+  const float gmin = fminf(__uint_as_float(mn << 16), __uint_as_float(mn & 0xffff0000u));
+  const float gmax = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
+  const bool maybe = valid && !(gmin > v_lo && gmax < v_hi);
+  if (!__any_sync(0xffffffffu, maybe)) return;
   const uint32_t w0 = __shfl_sync(0xffffffffu, v.x, 0);
   const bool uniform = __all_sync(0xffffffffu, valid && v.x == w0 && v.y == w0 && v.z == w0 && v.w == w0 &&
                                                    (w0 >> 16) == (w0 & 0xffffu));
   if (uniform) {
     if ((threadIdx.x & 31) == 0) {
       const uint32_t key = bf16x2_keys(w0) & 0xffffu;
-      atomicAdd(&bins[key >> 1], 256u << ((key & 1u) << 4));
+      if (key <= lo || key >= hi) atomicAdd(&bins[key >> 1], 256u << ((key & 1u) << 4));
     }
     return;
   }
-  if (!valid) return;
+  if (!maybe) return;
   const uint32_t k[4] = {bf16x2_keys(v.x), bf16x2_keys(v.y), bf16x2_keys(v.z), bf16x2_keys(v.w)};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    count16(bins, k[i] & 0xffffu);
-    count16(bins, k[i] >> 16);
+    count16_tails(bins, k[i] & 0xffffu, lo, hi);
+    count16_tails(bins, k[i] >> 16, lo, hi);
   }
 }
 
@@ -84,7 +132,8 @@ __device__ __forceinline__ void count_group(uint32_t* bins, const uint4 v, bool 
 // the loads of the next chunk are already in flight.
 __global__ void __launch_bounds__(kHistThreads, 1)
 hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t N,
-            int chunks_per_head, int total_chunks, uint32_t* __restrict__ counts, int vec) {
+            int chunks_per_head, int total_chunks, uint32_t* __restrict__ counts, int vec,
+            const TailInfo* __restrict__ tails) {
   extern __shared__ uint4 smem_hist[];
   uint32_t* bins = reinterpret_cast<uint32_t*>(smem_hist);   // 32768 words = 65536 16-bit bins
   const int tid = threadIdx.x;
@@ -99,14 +148,17 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
     int h; int64_t n0, n1;
     chunk_span(ci, h, n0, n1);
     const uint16_t* xh = x + (int64_t)h * stride_h;
+    // position n = b * L + l: one division per chunk, then at most a few row steps
+    // (a thread's positions grow by 8 * kHistThreads per load)
+    const int64_t b0 = n0 / L;
+    int64_t b = b0, l = n0 - b0 * L + 8 * tid;
+    while (l >= L) { l -= L; ++b; }
 #pragma unroll
     for (int k = 0; k < kGroupsPerThread; ++k) {
       v[k] = make_uint4(0, 0, 0, 0);
-      const int64_t n = n0 + 8 * (int64_t)(tid + k * kHistThreads);
-      if (n < n1) {
-        const int64_t b = n / L, l = n - b * L;
-        v[k] = __ldcs(reinterpret_cast<const uint4*>(xh + b * stride_b + l));
-      }
+      if (b * L + l < n1) v[k] = __ldcs(reinterpret_cast<const uint4*>(xh + b * stride_b + l));
+      l += 8 * kHistThreads;
+      while (l >= L) { l -= L; ++b; }
     }
   };
 
@@ -114,14 +166,19 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
   int ci = blockIdx.x;
   if (vec && ci < total_chunks) load_chunk(ci, v);
   __syncthreads();
-  for (; ci < total_chunks; ci += gridDim.x) {
+  while (ci < total_chunks) {
     int h; int64_t n0, n1;
     chunk_span(ci, h, n0, n1);
+    uint32_t lo = 0xffffu, hi = 0x10000u;       // count every key ...
+    if (tails) { lo = tails[h].key_lo; hi = tails[h].key_hi; }   // ... or only the tails
+    // the thresholds as values (-inf / +inf when everything is counted)
+    const float v_lo = lo >= 0xffffu ? CUDART_INF_F : key_value(lo);
+    const float v_hi = hi > 0xffffu ? -CUDART_INF_F : key_value(hi);
     if (vec) {
 #pragma unroll
       for (int k = 0; k < kGroupsPerThread; ++k) {
         const int64_t n = n0 + 8 * (int64_t)(tid + k * kHistThreads);
-        count_group(bins, v[k], n < n1);
+        count_group(bins, v[k], n < n1, lo, hi, v_lo, v_hi);
       }
     } else {
       const uint16_t* xh = x + (int64_t)h * stride_h;
@@ -129,27 +186,211 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
         const int64_t n = n0 + tid + (int64_t)k * kHistThreads;
         if (n < n1) {
           const int64_t b = n / L, l = n - b * L;
-          count16(bins, bf16x2_keys(xh[b * stride_b + l]) & 0xffffu);
+          count16_tails(bins, bf16x2_keys(xh[b * stride_b + l]) & 0xffffu, lo, hi);
         }
       }
     }
     __syncthreads();
-    if (vec && ci + (int)gridDim.x < total_chunks) load_chunk(ci + gridDim.x, v);
-    // flush the non-zero counters into the head's table and clear them
+    const int cn = ci + gridDim.x;
+    if (vec && cn < total_chunks) load_chunk(cn, v);
+    // flush the non-zero counters into the head's table and clear them (only the
+    // counted key ranges can hold any: groups of 8 bins [0, lo] and [hi, 0xffff])
     uint32_t* ch = counts + (int64_t)h * kBins;
-    for (int i = tid; i < kBins / 8; i += kHistThreads) {
+    const int g_lo = lo >= 0xffffu ? kBins / 8 : (int)(lo >> 3) + 1, g_hi = hi > 0xffffu ? kBins / 8 : (int)(hi >> 3);
+    for (int i0 = tid; i0 < kBins / 8; i0 += kHistThreads) {
+      const int i = i0 < g_lo ? i0 : (g_hi > g_lo ? g_hi + (i0 - g_lo) : kBins / 8);
+      if (i >= kBins / 8) break;
       const uint4 q = smem_hist[i];
       if ((q.x | q.y | q.z | q.w) == 0u) continue;
       const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = w[j] & 0xffffu, hi = w[j] >> 16;
-        if (lo) atomicAdd(&ch[8 * i + 2 * j], lo);
-        if (hi) atomicAdd(&ch[8 * i + 2 * j + 1], hi);
+        const uint32_t c0 = w[j] & 0xffffu, c1 = w[j] >> 16;
+        if (c0) atomicAdd(&ch[8 * i + 2 * j], c0);
+        if (c1) atomicAdd(&ch[8 * i + 2 * j + 1], c1);
       }
       smem_hist[i] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
+    ci = cn;
+  }
+}
+
+// Tail-only counting for 16-byte aligned rows: grid (ranges of a row, rows b * H + h);
+// each thread loads kTailGroups groups of 8 values at once, rules most of them out
+// with the packed min / max test of count_group, and adds the keys of the rest
+// straight into the head's u32 table (they are rare: a few 1e-4 of the values).
+__global__ void __launch_bounds__(kTailThreads)
+tail_count_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int H,
+                  uint32_t* __restrict__ counts, const TailInfo* __restrict__ tails) {
+  const int row = blockIdx.y, h = row % H, b = row / H;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)b * stride_b + (int64_t)h * stride_h);
+  const int64_t groups = L / 8;
+  const int64_t g0 = (int64_t)blockIdx.x * (kTailThreads * kTailGroups) + threadIdx.x;
+  const uint32_t lo = tails[h].key_lo, hi = tails[h].key_hi;
+  const float v_lo = lo >= 0xffffu ? CUDART_INF_F : key_value(lo);
+  const float v_hi = hi > 0xffffu ? -CUDART_INF_F : key_value(hi);
+  uint32_t* ch = counts + (int64_t)h * kBins;
+  uint4 v[kTailGroups];
+#pragma unroll
+  for (int k = 0; k < kTailGroups; ++k) {
+    const int64_t g = g0 + (int64_t)k * kTailThreads;
+    v[k] = g < groups ? __ldcs(src + g) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < kTailGroups; ++k) {
+    const bool valid = g0 + (int64_t)k * kTailThreads < groups;
+    const uint32_t mn = bmin2(bmin2(v[k].x, v[k].y), bmin2(v[k].z, v[k].w));
+    const uint32_t mx = bmax2(bmax2(v[k].x, v[k].y), bmax2(v[k].z, v[k].w));
+    const float gmin = fminf(__uint_as_float(mn << 16), __uint_as_float(mn & 0xffff0000u));
+    const float gmax = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
+    if (valid && !(gmin > v_lo && gmax < v_hi)) {
+      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t k2 = bf16x2_keys(w[i]);
+        const uint32_t a = k2 & 0xffffu, c = k2 >> 16;
+        if (a <= lo || a >= hi) atomicAdd(&ch[a], 1u);
+        if (c <= lo || c >= hi) atomicAdd(&ch[c], 1u);
+      }
+    }
+  }
+}
+
+// Warp-wide: the bin of a 256-bin histogram holding its r-th smallest element
+// (from_top: r-th largest) and that element's 1-based rank inside the bin.  Lane l
+// owns 8 consecutive bins; r must not exceed the histogram's total.
+__device__ __forceinline__ void select_bin(const uint32_t* hist, uint32_t r, bool from_top, uint32_t& bin,
+                                           uint32_t& rank) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = 8 * lane + j;
+    c[j] = hist[from_top ? 255 - i : i];
+    sum += c[j];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t m = __ballot_sync(0xffffffffu, incl >= r);
+  const int owner = m ? __ffs(m) - 1 : 31;
+  uint32_t b = 0, rk = 1, acc = incl - sum;
+  if (lane == owner) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (acc + c[j] >= r) { const int i = 8 * lane + j; b = (uint32_t)(from_top ? 255 - i : i); rk = r - acc; break; }
+      acc += c[j];
+    }
+  }
+  bin = __shfl_sync(0xffffffffu, b, owner);
+  rank = __shfl_sync(0xffffffffu, rk, owner);
+}
+
+// Tail thresholds of head h from kSampleUnits strided samples (16-byte groups when
+// vec, single values otherwise).  With S sampled keys and p = (N - t + 1) / N, the
+// sample's r-th smallest key, r = 3 S p + 4, lies above the N - t + 1 smallest
+// values of the head unless the sample over-represents the low tail badly (the
+// window kernel checks and falls back); key_lo is that key, key_hi the r-th
+// largest.  The order statistics come from a two-level radix select on the key
+// bytes.  Overlapping tails count everything.
+__global__ void __launch_bounds__(kSampleThreads)
+tail_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t N,
+            unsigned long long span, int vec, TailInfo* __restrict__ tails) {
+  constexpr int kUnits = kSampleUnits / kSampleThreads;    // 16 samples per thread
+  constexpr int kWarps = kSampleThreads / 32;
+  __shared__ uint32_t whist[kWarps][256];        // per-warp high-byte histograms
+  __shared__ uint32_t hist[3][256];              // high byte; low byte in the low bin; low byte in the high bin
+  __shared__ uint32_t sel[4];                    // b_lo, b_hi, residual rank in b_lo, in b_hi
+  const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
+  for (int i = tid; i < kWarps * 256; i += kSampleThreads) (&whist[0][0])[i] = 0u;
+  for (int i = tid; i < 3 * 256; i += kSampleThreads) (&hist[0][0])[i] = 0u;
+  const uint16_t* xh = x + (int64_t)h * stride_h;
+  const int64_t units = vec ? N / 8 : N;
+  const int per = vec ? 8 : 1;
+  // all loads first (independent), keys kept in registers for both passes
+  uint4 q[kUnits];
+  bool ok[kUnits];
+#pragma unroll
+  for (int j = 0; j < kUnits; ++j) {
+    const int g = tid + j * kSampleThreads;
+    const int64_t u = (int64_t)((unsigned long long)g * (unsigned long long)units / kSampleUnits);
+    ok[j] = u < units;
+    q[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (ok[j]) {
+      const int64_t n = u * per, b = n / L, l = n - b * L;
+      if (vec) q[j] = *reinterpret_cast<const uint4*>(xh + b * stride_b + l);
+      else q[j].x = xh[b * stride_b + l];
+    }
+  }
+  __syncthreads();
+  // fn(key, valid) is called by every lane the same number of times (warp-uniform)
+  auto for_keys = [&](auto&& fn) {
+#pragma unroll
+    for (int j = 0; j < kUnits; ++j) {
+      if (vec) {
+        const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t k2 = bf16x2_keys(w[i]);
+          fn(k2 & 0xffffu, ok[j]);
+          fn(k2 >> 16, ok[j]);
+        }
+      } else {
+        fn(bf16x2_keys(q[j].x) & 0xffffu, ok[j]);
+      }
+    }
+  };
+  // high-byte histogram, one atomic per distinct bin and warp step (the sample
+  // concentrates in a few bins, so per-lane atomics would mostly collide)
+  const int lane = tid & 31;
+  for_keys([&](uint32_t key, bool valid) {
+    const uint32_t bin = valid ? (key >> 8) : 256u;
+    const uint32_t m = __match_any_sync(0xffffffffu, bin);
+    if (valid && lane == __ffs(m) - 1) atomicAdd(&whist[warp][bin], (uint32_t)__popc(m));
+  });
+  __syncthreads();
+  for (int i = tid; i < 256; i += kSampleThreads) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) c += whist[w][i];
+    hist[0][i] = c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t total = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) total += hist[0][8 * lane + j];
+    total = __reduce_add_sync(0xffffffffu, total);
+    const double want = 3.0 * (double)total * (double)span / (double)N + 4.0;
+    const uint32_t r = want >= (double)total ? total : (uint32_t)want;
+    uint32_t b_lo = 256u, b_hi = 0u, r_lo = 1u, r_hi = 1u;
+    if (r > 0 && r < total) {
+      select_bin(hist[0], r, false, b_lo, r_lo);
+      select_bin(hist[0], r, true, b_hi, r_hi);
+    }                                            // else too few samples: count everything
+    if (lane == 0) { sel[0] = b_lo; sel[1] = b_hi; sel[2] = r_lo; sel[3] = r_hi; }
+  }
+  __syncthreads();
+  const uint32_t s0 = sel[0], s1 = sel[1];
+  for_keys([&](uint32_t key, bool valid) {
+    if (valid && (key >> 8) == s0) atomicAdd(&hist[1][key & 0xffu], 1u);
+    if (valid && (key >> 8) == s1) atomicAdd(&hist[2][key & 0xffu], 1u);
+  });
+  __syncthreads();
+  if (warp == 0) {
+    TailInfo ti{0xffffu, 0x10000u, 0u, 0u};
+    if (s0 < 256u) {
+      uint32_t k_lo, k_hi, rk;
+      select_bin(hist[1], sel[2], false, k_lo, rk);
+      select_bin(hist[2], sel[3], true, k_hi, rk);
+      const uint32_t lo = (s0 << 8) | k_lo, hi = (s1 << 8) | k_hi;
+      if (lo + 1u < hi) { ti.key_lo = lo; ti.key_hi = hi; }
+    }
+    if (lane == 0) tails[h] = ti;
   }
 }
 
@@ -169,20 +410,64 @@ __device__ __forceinline__ bool tot_less(float a, float b) {
 
 __global__ void __launch_bounds__(kWinThreads, 1)
 window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long long t,
-              float* __restrict__ min_io, float* __restrict__ max_io) {
+              float* __restrict__ min_io, float* __restrict__ max_io, TailInfo* __restrict__ tails, int mode,
+              const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int vec) {
+  // mode 0: tail counts (few windows); mode 1: the heads flagged by mode 0 are
+  // counted here in full and searched again, other heads return at once;
+  // mode 2: full counts from the histogram kernel, no tail state.
   __shared__ unsigned long long base_s[kWinThreads + 1];
   __shared__ unsigned long long warp_tot[kWinThreads / 32];
   __shared__ Cand warp_best[kWinThreads / 32];
+  __shared__ unsigned long long count_lo_s;
   const int h = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* ch = counts + (int64_t)h * kBins;
+  if (mode == 1 && tails[h].flag == 0u) return;
+  if (mode == 1) {
+    // Full count of this head (rare): global atomics, one per distinct key and warp step.
+    const uint16_t* xh = x + (int64_t)h * stride_h;
+    const int64_t units = vec ? (int64_t)N / 8 : (int64_t)N;
+    const int nk = vec ? 8 : 1;
+    for (int64_t u0 = 0; u0 < units; u0 += kWinThreads) {
+      const int64_t u = u0 + tid;
+      const bool valid = u < units;
+      uint32_t keys[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) keys[i] = 0x10000u;
+      if (valid) {
+        const int64_t n = u * nk, b = n / L, l = n - b * L;
+        if (vec) {
+          const uint4 q = *reinterpret_cast<const uint4*>(xh + b * stride_b + l);
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t k2 = bf16x2_keys(w[i]);
+            keys[2 * i] = k2 & 0xffffu;
+            keys[2 * i + 1] = k2 >> 16;
+          }
+        } else {
+          keys[0] = bf16x2_keys(xh[b * stride_b + l]) & 0xffffu;
+        }
+      }
+      for (int i = 0; i < nk; ++i) {
+        const uint32_t m = __match_any_sync(0xffffffffu, keys[i]);
+        if (keys[i] < 0x10000u && lane == __ffs(m) - 1) atomicAdd(&ch[keys[i]], (uint32_t)__popc(m));
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t key_lo = mode == 0 ? tails[h].key_lo : 0xffffu;   // read before thread 0 clears it
+  const uint32_t key_hi = mode == 0 ? tails[h].key_hi : 0u;
+  // in mode 0 the bins strictly between the tails were never counted: skip reading them
+  const uint32_t my_first = (uint32_t)tid * kBinsPerThread, my_last = my_first + kBinsPerThread - 1;
+  const bool skip = mode == 0 && key_lo < 0xffffu && my_first > key_lo && my_last < key_hi;
 
   // 64 consecutive bins per thread (re-read later from L2 rather than held in registers).
   const uint4* src = reinterpret_cast<const uint4*>(ch + tid * kBinsPerThread);
   unsigned long long sum = 0;
   uint32_t any = 0;
 #pragma unroll 4
-  for (int i = 0; i < kBinsPerThread / 4; ++i) {
+  for (int i = 0; i < kBinsPerThread / 4 && !skip; ++i) {
     const uint4 q = src[i];
     sum += (unsigned long long)q.x + q.y + q.z + q.w;
     any |= q.x | q.y | q.z | q.w;
@@ -208,20 +493,60 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
     warp_tot[lane] = wi - wv;                      // exclusive prefix of warp totals
   }
   __syncthreads();
-  const unsigned long long base = warp_tot[warp] + incl - sum;
+  unsigned long long base = warp_tot[warp] + incl - sum;
   base_s[tid] = base;
   if (tid == kWinThreads - 1) base_s[kWinThreads] = base + sum;
   __syncthreads();
+  bool search = true;
+  if (mode == 0) {
+    // Only keys <= key_lo and >= key_hi were counted: the N - total uncounted values
+    // sit between them, so one virtual bin key_lo + 1 of that size gives every
+    // counted bin its true position.  The windows are exact if each tail holds at
+    // least N - t + 1 values; otherwise flag the head for the full pass.
+    const unsigned long long total = base_s[kWinThreads];
+    const unsigned long long span = N - t + 1;
+    if (key_lo < 0xffffu) {
+      const uint32_t vb = key_lo + 1u;
+      const int owner = (int)(vb / kBinsPerThread);
+      const unsigned long long M = N - total;
+      if (tid == owner) {
+        unsigned long long below = base;
+        for (uint32_t i = (uint32_t)owner * kBinsPerThread; i < vb; ++i) below += ch[i];
+        count_lo_s = below;
+        if (M != 0) {
+          ch[vb] += (uint32_t)M;            // read back by this thread only
+          sum += M;
+          any = 1u;
+        }
+      }
+      if (tid > owner) base += M;
+      __syncthreads();
+      const unsigned long long count_lo = count_lo_s, count_hi = total - count_lo;
+      search = count_lo >= span && count_hi >= span;
+    }
+    if (tid == 0) {
+      tails[h].key_lo = 0u;
+      tails[h].key_hi = 0u;
+      if (!search) tails[h].flag = 1u;
+    }
+  } else if (mode == 1 && tid == 0) {
+    tails[h].flag = 0u;
+  }
 
   Cand best{__longlong_as_double(0x7ff0000000000000LL), 0xffffffffu, 0xffffffffu};
   unsigned long long P = base;
-  if (N - t + 1 <= (unsigned long long)kCandCap) {
-    // Few window starts (ratio near 1): table the first position of every value that
-    // can start a window, cand[position] = its bin; then each bin w looks up the
-    // starts whose window ends inside w: start position = end position - (t - 1).
-    extern __shared__ uint32_t cand[];
+  if (!search) {
+    // thin tails: the full pass decides this head
+  } else if (N - t + 1 <= (unsigned long long)kCandCap) {
+    // Few window starts (ratio near 1).  Table the first position of every value
+    // that can start a window, start_tab[position] = its bin, and the bin of every
+    // position a window can end at, end_tab[position - (t - 1)]; then window i runs
+    // from start_tab[i] to end_tab[i], and all of them are checked in parallel.
+    extern __shared__ uint32_t tab[];
     const uint32_t span = (uint32_t)(N - t + 1);
-    for (uint32_t i = tid; i < span; i += kWinThreads) cand[i] = 0xffffffffu;
+    uint32_t* start_tab = tab;
+    uint32_t* end_tab = tab + span;
+    for (uint32_t i = tid; i < span; i += kWinThreads) start_tab[i] = 0xffffffffu;
     __syncthreads();
     unsigned long long pos = base;
     if (any != 0 && base < span) {
@@ -230,13 +555,12 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
         const uint32_t c[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (c[j] != 0 && pos < span) cand[pos] = (uint32_t)(tid * kBinsPerThread + 4 * q + j);
+          if (c[j] != 0 && pos < span) start_tab[pos] = (uint32_t)(tid * kBinsPerThread + 4 * q + j);
           pos += c[j];
         }
         if (pos >= span) break;
       }
     }
-    __syncthreads();
     // end positions live in [t - 1, N); this thread's bins cover [base, base + sum)
     pos = base;
     if (any != 0 && base + sum > t - 1) {
@@ -246,17 +570,20 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const unsigned long long lo_e = pos > t - 1 ? pos : t - 1, hi_e = pos + c[j];
-          for (unsigned long long e = lo_e; e < hi_e; ++e) {
-            const uint32_t v = cand[e - (t - 1)];
-            if (v != 0xffffffffu) {
-              const uint32_t end_bin = (uint32_t)(tid * kBinsPerThread + 4 * q + j);
-              const double w = (double)key_value(end_bin) - (double)key_value(v);
-              const Cand cd{w, v, end_bin};
-              if (cand_less(cd, best)) best = cd;
-            }
-          }
+          const uint32_t bin = (uint32_t)(tid * kBinsPerThread + 4 * q + j);
+          for (unsigned long long e = lo_e; e < hi_e; ++e) end_tab[e - (t - 1)] = bin;
           pos = hi_e;
         }
+      }
+    }
+    __syncthreads();
+    for (uint32_t i = tid; i < span; i += kWinThreads) {
+      const uint32_t v = start_tab[i];
+      if (v != 0xffffffffu) {
+        const uint32_t end_bin = end_tab[i];
+        const double w = (double)key_value(end_bin) - (double)key_value(v);
+        const Cand cd{w, v, end_bin};
+        if (cand_less(cd, best)) best = cd;
       }
     }
   } else if (any != 0 && base + t <= N) {
@@ -328,7 +655,7 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
 using namespace fa3;
 
 FA3_API size_t fa3_calibrate_workspace_size(int H) {
-  return H > 0 ? (size_t)H * kBins * sizeof(uint32_t) : 0;
+  return H > 0 ? (size_t)H * kBins * sizeof(uint32_t) + (size_t)H * sizeof(TailInfo) : 0;
 }
 
 FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L, int64_t stride_b,
@@ -364,16 +691,38 @@ FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L
   }
   const unsigned grid = (unsigned)(total_chunks < sms ? total_chunks : sms);
   uint32_t* counts = static_cast<uint32_t*>(workspace);
-  timing_begin(s);
-  hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, chunks_per_head, (int)total_chunks,
-                                                counts, vec);
-  timing_end(s);
-  if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
-  const bool fast = (uint64_t)(N - t + 1) <= (uint64_t)kCandCap;
-  const int wsmem = fast ? (int)((N - t + 1) * sizeof(uint32_t)) : 0;
+  TailInfo* tails = reinterpret_cast<TailInfo*>(counts + (size_t)H * kBins);
+  const unsigned long long span = (unsigned long long)(N - t + 1);
+  const bool fast = span <= (unsigned long long)kCandCap;
+  const int wsmem = fast ? (int)(2 * span * sizeof(uint32_t)) : 0;   // start and end tables
   if (wsmem > 48 * 1024 &&
       cudaFuncSetAttribute(window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem) != cudaSuccess)
     return FA3_ECUDA;
-  window_kernel<<<H, kWinThreads, wsmem, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io);
+  if (fast) {
+    // tails only, then a full pass over the heads whose tails turned out too thin
+    tail_kernel<<<H, kSampleThreads, 0, s>>>(x, L, stride_b, stride_h, N, span, vec, tails);
+    timing_begin(s);
+    const int64_t per_cta = (int64_t)kTailThreads * kTailGroups;
+    const int64_t xb = (L / 8 + per_cta - 1) / per_cta, rows = B * (int64_t)H;
+    if (vec && xb <= 0x7fffffff && rows <= 65535) {
+      tail_count_kernel<<<dim3((unsigned)xb, (unsigned)rows), kTailThreads, 0, s>>>(x, L, stride_b, stride_h, H,
+                                                                                    counts, tails);
+    } else {
+      hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, chunks_per_head,
+                                                    (int)total_chunks, counts, vec, tails);
+    }
+    timing_end(s);
+    window_kernel<<<H, kWinThreads, wsmem, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io,
+                                                 tails, 0, x, L, stride_b, stride_h, vec);
+    window_kernel<<<H, kWinThreads, wsmem, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io,
+                                                 tails, 1, x, L, stride_b, stride_h, vec);
+  } else {
+    timing_begin(s);
+    hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, chunks_per_head, (int)total_chunks,
+                                                  counts, vec, nullptr);
+    timing_end(s);
+    window_kernel<<<H, kWinThreads, wsmem, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io,
+                                                 tails, 2, x, L, stride_b, stride_h, vec);
+  }
   return cuda_status(cudaGetLastError());
 }

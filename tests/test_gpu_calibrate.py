@@ -111,3 +111,39 @@ def test_full_size_calibration_sampled_heads():
     for h in (0, 1, 17, 42, 63, 64, 100, 127):
         lo, hi = O.recall_window(W.calib_head(w, 0, h), w.ratio)
         assert (gmn[h], gmx[h]) == (np.float32(lo), np.float32(hi)), h
+
+
+def _sampled_units(units, n_samples=512):
+    # the strided sample the tail thresholds are drawn from (16-byte groups or values)
+    return sorted({g * units // n_samples for g in range(n_samples)})
+
+
+@pytest.mark.parametrize("vec", [True, False])
+def test_thin_tails_fall_back_to_full_count(vec):
+    # Plant one extreme value into sampled units of head 0 (25 groups of 8 values, or
+    # 40 single values, more than the sample's tail rank of 16 or 5): the sample's
+    # tail order statistic then falls on that value, whose count (200 or 40) is below
+    # the 1574 smallest values a window can start from, so the tail-only count must
+    # be rejected and the head counted again in full.  Head 1 is left as is.
+    F = fa3()
+    rng = np.random.default_rng(11)
+    H, N = 2, 4 * 2048 * 192
+    ratio = 0.999                                  # N - target_num + 1 = 1574 window starts
+    x = W.bf16_round(rng.standard_normal((H, N)).astype(np.float32))
+    per, n_plant = (8, 25) if vec else (1, 40)
+    for u in _sampled_units(N // per)[:n_plant]:
+        x[0, u * per:u * per + per] = -600.0
+    if vec:
+        xd = bf16_dev(x)
+    else:
+        pad = np.zeros((H, N + 1), np.float32)     # odd row stride: the scalar path
+        pad[:, :N] = x
+        xd = bf16_dev(pad)[:, :N]
+    omn, omx = O.calibrate([x.reshape(1, H, 1, N)], ratio)
+    for _ in range(2):                             # the workspace is left clean for the next call
+        mn = torch.full((H,), float("inf"), device="cuda")
+        mx = torch.full((H,), float("-inf"), device="cuda")
+        F.calibrate_perhead(xd, ratio, mn, mx)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn))
+        assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx))
