@@ -21,16 +21,21 @@
 //     K-major B operand of Q.C^T and the MN-major B operand of P.C) and keeps
 //     its O half in TMEM;
 //   * the quantized latent query lives in TMEM as the A operand of Q.C^T; the
-//     RoPE term is computed over all RoPE dims in both CTAs (it is small), so
-//     only the exact integer latent partial crosses the cluster, packed in 24
-//     bits (|partial| <= 256*127*127 < 2^23) by st.async into the peer's shared
-//     memory; both CTAs then hold bit-identical scores and run the same online
-//     softmax (lazy rescale when the max grows by more than 8 in log2 units);
-//   * warp roles: 4 softmax warps (one TMEM lane = one head each), 1 TMA
-//     producer, 1 MMA issuer, 4 int8->fp16 converter warps;
+//     RoPE term is split over the pair (each CTA contracts half of the RoPE
+//     dims from a TMA-loaded bf16 key tile); each CTA scales its exact latent
+//     partial, adds its RoPE share and sends the fp32 partial score to the peer
+//     by st.async into its shared memory; own + peer is the same fp32 sum in
+//     both CTAs, so both run the same online softmax on identical scores (lazy
+//     rescale when the max grows by more than 8 in log2 units);
+//   * warp roles: 8 softmax warps (two per TMEM lane quarter: lane = head, each
+//     warp takes half of a tile's tokens), 1 MMA issuer, 3 int8->fp16
+//     converter warps (the first converter thread also issues the RoPE TMA);
 //   * split-K: the tiles of all sequences are dealt out evenly to the clusters
-//     that fit on the GPU; a cluster's piece of a sequence is a segment; split
-//     sequences are merged by a small log-sum-exp combine kernel.
+//     that fit on the GPU; a cluster's piece of a sequence is a segment; for a
+//     split sequence each softmax warp leaves its block of O (unnormalised, with
+//     the rows' m and l) in the workspace, and the warp that completes the last
+//     copy of that block (a per-block counter) merges all segments' blocks with
+//     log-sum-exp weights and writes the output rows.
 // Every wait is bounded; on time-out the kernel sets FA3_DEVERR_TIMEOUT, drains
 // its own copies and MMAs, frees its TMEM and returns.
 #include "fa3_common.cuh"
@@ -96,7 +101,6 @@ constexpr uint32_t OFF_SCHED = OFF_TMEM_SLOT + 8;         // 4 x int64: b_first,
 static_assert(OFF_SCHED + 32 <= OFF_BAR + 1024, "barrier area");
 
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: normal waits last microseconds
-constexpr int kMaxSeg = 256;                   // clusters a sequence can span (>= resident clusters)
 
 struct MlaParams {
   CUtensorMap tm_rope;   // bf16 viewed as (8, T_max, Dr/8, B), box {8, 64, Dr/8, 1}
@@ -106,12 +110,13 @@ struct MlaParams {
   const float* kv_scale;
   const int32_t* lens;
   float* out;
-  float* part_o;         // [slot][2][128][Dl/2]
-  float2* part_ml;       // [slot][128]
+  float* part_o;         // [slot][2][warp][O columns / 4][32][4]: unnormalised O block of each softmax warp
+  float2* part_ml;       // [slot][2][warp][32]: (m, l) of each head row of that block
   uint16_t* q_lat;       // [B][2][128][Dl/2] fp16 latent query codes (prepared per call)
   uint8_t* q_rope;       // [B][QR_BYTES] bf16 RoPE query in core-matrix layout (prepared per call)
-  int* seg_n;            // [B] segments of each sequence: -1 one cluster wrote it, 0 empty, else count
-  int* seg_slot;         // [B][kMaxSeg] partial slots of each split sequence
+  int* seg_lo;           // [B]: first cluster of a split sequence, -1 if one cluster (or none) holds it
+  int* seg_hi;           // [B]: last cluster of a split sequence
+  int64_t* total_tiles;  // tiles of all sequences (written by the query pre-pass)
   int32_t* err;
   int B, H, Dl, Dr, T_max;
   int DH;                // Dl / 2
@@ -177,11 +182,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
-}
 __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, int c3,
                                        uint32_t bar) {
   asm volatile(
@@ -209,11 +209,6 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-// Arrives on the barrier at the same shared-memory offset in every CTA of cta_mask once the MMAs complete.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               ::"r"(bar), "h"(cta_mask) : "memory");
 }
 
 #define FA3_TMEM_LD32(taddr, v)                                                                                   \
@@ -250,10 +245,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t x) {
-  __half2 h = *reinterpret_cast<__half2*>(&x);
-  return __half22float2(h);
-}
 // Four signed int8 codes -> two f16x2 (exact).
 __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;
@@ -262,6 +253,11 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
 }
+
+// Programmatic dependent launch: wait for the prerequisite grid's completion and
+// memory; let the dependent grid start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -319,11 +315,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// Bulk copy from this CTA's shared memory into a cluster peer's, completing on the peer's barrier.
-__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster) : "memory");
-}
 __device__ __forceinline__ int seq_tiles(const MlaParams& p, int b) {
   const int len = p.lens[b];
   if (len < 0 || len > p.T_max) return 0;
@@ -369,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ MlaParams p) {
   constexpr int CONV_TOTAL = kTok * (DH / 16);      // 16-byte int8 chunks of a tile (this CTA's latent half)
   constexpr int CONV_UNITS = (CONV_TOTAL + kConvThreads - 1) / kConvThreads;   // per converter thread
-  constexpr int QA_WORDS = DH / 2;                  // 32-bit TMEM columns of one head's fp16 query half
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -469,6 +459,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
   const int64_t* sched = reinterpret_cast<const int64_t*>(smem + OFF_SCHED);
+  // The prepared queries come from the pre-pass kernel, launched just before as
+  // this kernel's programmatic prerequisite; the set-up above overlapped its tail.
+  pdl_wait();
+  pdl_launch_dependents();
   SegWalk walk0{sched[2], sched[3], sched[1], (int)sched[0]};
   const uint32_t rope_tx = (uint32_t)(kTok * 2 * p.Dr);
 
@@ -827,24 +821,35 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       tc_fence_after();
       const bool full = (lo == 0 && hi == tb);
       const float inv = (full && l_row > 0.f) ? kvs / l_row : 0.f;
-      const int slot = b + cluster;
+      // A split sequence leaves this warp's block of O (its 32 head rows x its O
+      // columns, unnormalised, lane-interleaved float4 columns) and the rows' (m, l)
+      // in the workspace slot of (sequence + cluster) for mla_combine_kernel.
+      const int64_t blk = ((int64_t)(b + cluster) * 2 + rank) * kSmWarps + warp;
+      float* blk_o = p.part_o + blk * (32 * O_PER);
 #pragma unroll 1
       for (int c0 = o_lo; c0 < o_hi; c0 += 32) {
         uint32_t v[32];
         FA3_TMEM_LD32(tmem + lane_base + TM_O + c0, v);
         tmem_wait_ld();
-        if (h < p.H) {
-          float* dst = full ? p.out + ((int64_t)b * p.H + h) * p.Dl + rank * DH + c0
-                            : p.part_o + (((int64_t)slot * 2 + rank) * kRows + h) * DH + c0;
-          const float f = full ? inv : 1.f;
+        if (full) {
+          if (h < p.H) {
+            float* dst = p.out + ((int64_t)b * p.H + h) * p.Dl + rank * DH + c0;
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(dst + j) =
-                make_float4(__uint_as_float(v[j]) * f, __uint_as_float(v[j + 1]) * f,
-                            __uint_as_float(v[j + 2]) * f, __uint_as_float(v[j + 3]) * f);
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(dst + j) =
+                  make_float4(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv,
+                              __uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
+          }
+        } else {
+          const int j0 = (c0 - o_lo) / 4;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(blk_o + ((j0 + q) * 32 + lane) * 4) =
+                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
         }
       }
-      if (!full && rank == 0 && hf == 0 && h < p.H) p.part_ml[(int64_t)slot * kRows + h] = make_float2(m_ref, l_row);
+      if (!full && o_lo < o_hi) p.part_ml[blk * 32 + lane] = make_float2(m_ref, l_row);
       tc_fence_before();
     }
   }
@@ -863,11 +868,14 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 // codes stored as fp16, row-major per (sequence, latent half, head) for the
 // TMEM A operand) and lays out the RoPE query of each sequence as the
 // shared-memory image of K-major core matrices (8 heads x 8 values).
-// One thread per 8 values of one (sequence, head); heads >= H are zero.
+// One thread per 8 values of one (sequence, head); heads >= H are zero.  Also
+// writes the zero output rows of sequences without tiles and lists the clusters
+// of every split sequence for mla_combine_kernel.
 __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
+  pdl_launch_dependents();   // the decode kernel may start its set-up
   if (blockIdx.x == 0 && threadIdx.x < 32) {
-    // Segments of every sequence under the decode kernel's even split of tiles over
-    // clusters (cluster c covers tile positions [total*c/C, total*(c+1)/C)).
+    // Clusters of each sequence under the decode kernel's even split of all tiles
+    // (cluster c covers tile positions [total*c/C, total*(c+1)/C)).
     const int lane = threadIdx.x;
     const int C = p.num_clusters;
     int64_t total = 0;
@@ -877,14 +885,9 @@ __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
       for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
       total += t;
     }
-    auto owner = [&](int64_t x) {   // the largest c with floor(total*c/C) <= x
-      int lo = 0, hi = C - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (total * mid / C <= x) lo = mid; else hi = mid - 1;
-      }
-      return lo;
-    };
+    if (lane == 0) *p.total_tiles = total;
+    // the cluster whose range holds tile position x: the largest c with total*c/C <= x
+    auto owner = [&](int64_t x) -> int { return (int)min((int64_t)(C - 1), ((x + 1) * C - 1) / total); };
     int64_t pre = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int bb = b0 + lane;
@@ -897,17 +900,14 @@ __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
       }
       if (bb < p.B) {
         const int64_t start = pre + incl - t;
-        int n = 0;
+        int c0 = -1, c1 = -1;
         if (t > 0) {
-          const int c0 = owner(start), c1 = owner(start + t - 1);
-          if (c0 == c1) {
-            n = -1;
-          } else {
-            for (int c = c0; c <= c1; ++c)
-              if (total * c / C < total * (c + 1) / C && n < kMaxSeg) p.seg_slot[(int64_t)bb * kMaxSeg + n++] = bb + c;
-          }
+          c0 = owner(start);
+          c1 = owner(start + t - 1);
+          if (c0 == c1) c0 = c1 = -1;
         }
-        p.seg_n[bb] = n;
+        p.seg_lo[bb] = c0;
+        p.seg_hi[bb] = c1;
       }
       pre += __shfl_sync(0xffffffffu, incl, 31);
     }
@@ -922,6 +922,11 @@ __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
     const uint16_t* qrow = p.q + ((int64_t)b * p.H + h) * (p.Dl + p.Dr);
     uint4 o = make_uint4(0, 0, 0, 0);
     if (c < chunks_lat) {
+      if (h < p.H && seq_tiles(p, b) == 0) {      // no tiles (length 0 or invalid): a zero output row
+        float4* orow = reinterpret_cast<float4*>(p.out + ((int64_t)b * p.H + h) * p.Dl + 8 * c);
+        orow[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        orow[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       if (h < p.H) {
         const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * c);
         const float qs = p.q_scale[h], rqs = rcp_approx(qs);
@@ -943,40 +948,80 @@ __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
   }
 }
 
-// Merges the split segments of each sequence (listed by the pre-pass kernel) with
-// log-sum-exp weights; writes zero rows for empty sequences.  One block per
-// (head, sequence), Dl/4 threads, four outputs per thread.
-__global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p) {
-  const int h = blockIdx.x, b = blockIdx.y;
-  if (h >= p.H) return;
-  const int n = p.seg_n[b];
-  if (n < 0) return;                                   // one cluster held the sequence
-  const int e = 4 * threadIdx.x;
-  float4* dst = reinterpret_cast<float4*>(p.out + ((int64_t)b * p.H + h) * p.Dl + e);
-  if (n == 0) {
-    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
-    return;
+// Merges the segments of every split sequence with log-sum-exp weights.  One
+// block per (sequence, latent half, softmax-warp block of 32 heads x O columns):
+// the weights of each segment per head, then every column as a weighted sum of
+// the segments' blocks (loads of all segments in flight), transposed through
+// shared memory into coalesced output rows.  Launched as the decode kernel's
+// programmatic dependent: it waits for that grid before reading its partials.
+template <int DH>
+__global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p) {
+  constexpr int O_PER = DH >= 64 ? DH / 2 : DH;
+  constexpr int NQ = O_PER / 4;                        // float4 columns of a block row
+  extern __shared__ float csm[];
+  float* tile = csm;                                   // [32][O_PER + 4]
+  float* wts = csm + 32 * (O_PER + 4);                 // [segments][32]
+  pdl_wait();
+  const int b = blockIdx.x, rank = blockIdx.y / kSmWarps, wp = blockIdx.y % kSmWarps;
+  const int c_first = p.seg_lo[b], c_last = p.seg_hi[b];
+  const int hf = wp >> 2, qd = wp & 3;
+  if (c_first < 0 || hf * O_PER >= DH) return;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int C = p.num_clusters;
+  const int64_t total = *p.total_tiles;
+  auto covers = [&](int c) -> bool { return total >= C || total * c / C < total * (c + 1) / C; };
+  auto blk = [&](int c) -> int64_t { return ((int64_t)(b + c) * 2 + rank) * kSmWarps + wp; };
+  const int n = c_last - c_first + 1;
+  if (tid < 32) {
+    float M = -CUDART_INF_F;
+    for (int k = 0; k < n; ++k)
+      if (covers(c_first + k)) M = fmaxf(M, __ldcg(p.part_ml + blk(c_first + k) * 32 + lane).x);
+    float L = 0.f;
+    for (int k = 0; k < n; ++k) {
+      float w = 0.f;
+      if (covers(c_first + k)) {
+        const float2 ml = __ldcg(p.part_ml + blk(c_first + k) * 32 + lane);
+        w = exp2f(ml.x - M);
+        L += ml.y * w;
+      }
+      wts[k * 32 + lane] = w;
+    }
+    const float f = L > 0.f ? p.kv_scale[0] / L : 0.f;
+    for (int k = 0; k < n; ++k) wts[k * 32 + lane] *= f;
   }
-  const int* slots = p.seg_slot + (int64_t)b * kMaxSeg;
-  float M = -CUDART_INF_F;
-  for (int k = 0; k < n; ++k) M = fmaxf(M, p.part_ml[(int64_t)slots[k] * kRows + h].x);
-  const int r = e / p.DH, dd = e - r * p.DH;
-  const int64_t off = ((int64_t)r * kRows + h) * p.DH + dd;
-  const int64_t slot_stride = (int64_t)2 * kRows * p.DH;
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+  __syncthreads();
+  // positions pos = q * 32 + lane of the block, q < NQ
+  constexpr int PER = (32 * NQ + 255) / 256;
+  float4 acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
   for (int k = 0; k < n; ++k) {
-    const int64_t sl = slots[k];
-    const float2 ml = p.part_ml[sl * kRows + h];
-    const float w = exp2f(ml.x - M);
-    const float4 v = *reinterpret_cast<const float4*>(p.part_o + sl * slot_stride + off);
-    L += ml.y * w;
-    acc.x = fmaf(v.x, w, acc.x); acc.y = fmaf(v.y, w, acc.y);
-    acc.z = fmaf(v.z, w, acc.z); acc.w = fmaf(v.w, w, acc.w);
+    const float w = wts[k * 32 + lane];
+    if (w == 0.f) continue;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + blk(c_first + k) * (32 * O_PER));
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int pos = tid + 256 * i;
+      if (pos < 32 * NQ) {
+        const float4 v = __ldcg(src + pos);
+        acc[i].x = fmaf(v.x, w, acc[i].x); acc[i].y = fmaf(v.y, w, acc[i].y);
+        acc[i].z = fmaf(v.z, w, acc[i].z); acc[i].w = fmaf(v.w, w, acc[i].w);
+      }
+    }
   }
-  const float sc = L > 0.f ? p.kv_scale[0] / L : 0.f;
-  *dst = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int pos = tid + 256 * i;
+    if (pos < 32 * NQ) *reinterpret_cast<float4*>(tile + lane * (O_PER + 4) + 4 * (pos >> 5)) = acc[i];
+  }
+  __syncthreads();
+  for (int i = tid; i < 32 * NQ; i += 256) {
+    const int r = i / NQ, q = i - r * NQ, hh = qd * 32 + r;
+    if (hh < p.H)
+      *reinterpret_cast<float4*>(p.out + ((int64_t)b * p.H + hh) * p.Dl + rank * DH + hf * O_PER + 4 * q) =
+          *reinterpret_cast<const float4*>(tile + r * (O_PER + 4) + 4 * q);
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -1023,11 +1068,22 @@ bool mla_shape_ok(int H, int Dl, int Dr) {
 }
 
 
+// Decode kernel (timed by the optional caller events) and its combine kernel.
 template <int DH>
-cudaError_t launch_mla(cudaLaunchConfig_t cfg, const MlaParams& prm) {
+cudaError_t launch_mla(cudaLaunchConfig_t cfg, cudaLaunchConfig_t ccfg, const MlaParams& prm) {
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<DH>, prm);
+  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel<DH>, prm);
+  timing_end(cfg.stream);
+  if (e != cudaSuccess) return e;
+  constexpr int O_PER = DH >= 64 ? DH / 2 : DH;
+  ccfg.dynamicSmemBytes = (size_t)32 * (O_PER + 4) * sizeof(float) + (size_t)prm.num_clusters * 32 * sizeof(float);
+  if (ccfg.dynamicSmemBytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(mla_combine_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ccfg.dynamicSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaLaunchKernelEx(&ccfg, mla_combine_kernel<DH>, prm);
 }
 
 }  // namespace
@@ -1036,11 +1092,15 @@ cudaError_t launch_mla(cudaLaunchConfig_t cfg, const MlaParams& prm) {
 using namespace fa3;
 
 namespace {
-size_t mla_ws_parts(int B, int Dl, int C, size_t* off_ml, size_t* off_qlat, size_t* off_qrope) {
+// Workspace: per partial slot (sequence + cluster) and latent half, one block per
+// softmax warp (32 head rows x that warp's O columns) and its (m, l) pairs; then the
+// prepared queries, the total tile count and the clusters of each split sequence.
+size_t mla_ws_parts(int B, int Dl, int C, size_t* off_ml, size_t* off_qlat, size_t* off_qrope, size_t* off_seg) {
   const size_t slots = (size_t)B + (size_t)C;
-  size_t off = slots * 2 * kRows * (size_t)(Dl / 2) * sizeof(float);
+  const int DH = Dl / 2, o_cols = DH >= 64 ? DH / 2 : DH;
+  size_t off = slots * 2 * kSmWarps * 32 * (size_t)o_cols * sizeof(float);
   *off_ml = off;
-  off += slots * kRows * sizeof(float2);
+  off += slots * 2 * kSmWarps * 32 * sizeof(float2);
   off = (off + 255) & ~size_t(255);
   *off_qlat = off;
   off += (size_t)B * kRows * (size_t)Dl * sizeof(uint16_t);
@@ -1048,7 +1108,8 @@ size_t mla_ws_parts(int B, int Dl, int C, size_t* off_ml, size_t* off_qlat, size
   *off_qrope = off;
   off += (size_t)B * QR_BYTES;
   off = (off + 255) & ~size_t(255);
-  off += (size_t)B * (kMaxSeg + 1) * sizeof(int);      // segment lists
+  *off_seg = off;
+  off += sizeof(int64_t) + (size_t)B * 2 * sizeof(int);
   return off + 256;
 }
 }  // namespace
@@ -1058,8 +1119,8 @@ FA3_API size_t fa3_mla_workspace_size(int B, int H, int Dl, int T_max) {
   int C = 0;
   if (check_device(nullptr) == FA3_OK) C = max_clusters();
   if (C <= 0) C = 128;
-  size_t a, b2, c;
-  return mla_ws_parts(B, Dl, C, &a, &b2, &c);
+  size_t a, b2, c, d;
+  return mla_ws_parts(B, Dl, C, &a, &b2, &c, &d);
 }
 
 FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint16_t* krope, const float* q_scale,
@@ -1076,8 +1137,8 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   if (st != FA3_OK) return st;
   const int C = max_clusters();
   if (C <= 0) return FA3_ECUDA;
-  size_t off_ml, off_qlat, off_qrope;
-  const size_t need = mla_ws_parts(B, Dl, C, &off_ml, &off_qlat, &off_qrope);
+  size_t off_ml, off_qlat, off_qrope, off_seg;
+  const size_t need = mla_ws_parts(B, Dl, C, &off_ml, &off_qlat, &off_qrope, &off_seg);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FA3_EWORKSPACE;
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
   if (!encode) return FA3_ECUDA;
@@ -1102,11 +1163,9 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   prm.part_ml = reinterpret_cast<float2*>(ws + off_ml);
   prm.q_lat = reinterpret_cast<uint16_t*>(ws + off_qlat);
   prm.q_rope = reinterpret_cast<uint8_t*>(ws + off_qrope);
-  {
-    size_t off_seg = (off_qrope + (size_t)B * QR_BYTES + 255) & ~size_t(255);
-    prm.seg_n = reinterpret_cast<int*>(ws + off_seg);
-    prm.seg_slot = prm.seg_n + B;
-  }
+  prm.total_tiles = reinterpret_cast<int64_t*>(ws + off_seg);
+  prm.seg_lo = reinterpret_cast<int*>(ws + off_seg + sizeof(int64_t));
+  prm.seg_hi = prm.seg_lo + B;
   prm.err = dev_err;
   prm.B = B; prm.H = H; prm.Dl = Dl; prm.Dr = Dr; prm.T_max = T_max;
   prm.num_clusters = C;
@@ -1120,26 +1179,34 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
     mla_prepare_q_kernel<<<(unsigned)blocks, 256, 0, s>>>(prm);
     if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
   }
+  // The decode kernel and the combine kernel are programmatic dependents of the
+  // kernel before them: their launch and set-up overlap its tail.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 2; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2; attr[0].val.clusterDim.y = 1; attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaLaunchConfig_t ccfg = {};
+  ccfg.gridDim = dim3(B, 2 * kSmWarps, 1);
+  ccfg.blockDim = dim3(256, 1, 1);
+  ccfg.stream = s;
+  ccfg.attrs = &attr[1];
+  ccfg.numAttrs = 1;
   cudaError_t le = cudaErrorInvalidValue;
   timing_begin(s);
   switch (prm.DH) {
-    case 32: le = launch_mla<32>(cfg, prm); break;
-    case 64: le = launch_mla<64>(cfg, prm); break;
-    case 128: le = launch_mla<128>(cfg, prm); break;
-    case 256: le = launch_mla<256>(cfg, prm); break;
+    case 32: le = launch_mla<32>(cfg, ccfg, prm); break;
+    case 64: le = launch_mla<64>(cfg, ccfg, prm); break;
+    case 128: le = launch_mla<128>(cfg, ccfg, prm); break;
+    case 256: le = launch_mla<256>(cfg, ccfg, prm); break;
   }
-  timing_end(s);
   if (le != cudaSuccess) return FA3_ECUDA;
-  mla_combine_kernel<<<dim3(H, B), Dl / 4, 0, s>>>(prm);
   return cuda_status(cudaGetLastError());
 }
