@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "fa3.h"
 
 #define FA3_API extern "C" __attribute__((visibility("default")))
@@ -57,6 +59,29 @@ __device__ __forceinline__ int quant_code_fast(float x, float s, float rs) {
     return y > 0.0f ? 127 : -127;
   }
   return quant_code(x, s);
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched as a
+// programmatic dependent of the work before it on the stream (launch_pdl): it
+// calls pdl_wait() before its first access to memory another kernel may write,
+// and pdl_launch_dependents() once the next kernel may start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ void set_dev_err(int32_t* err, int bit) {

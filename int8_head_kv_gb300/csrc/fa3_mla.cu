@@ -254,10 +254,6 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
 }
 
-// Programmatic dependent launch: wait for the prerequisite grid's completion and
-// memory; let the dependent grid start launching.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -871,9 +867,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 // One thread per 8 values of one (sequence, head); heads >= H are zero.  Also
 // writes the zero output rows of sequences without tiles and lists the clusters
 // of every split sequence for mla_combine_kernel.
-__global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
+__global__ void __launch_bounds__(256, 8) mla_prepare_q_kernel(const MlaParams p) {
+  pdl_wait();
   pdl_launch_dependents();   // the decode kernel may start its set-up
-  if (blockIdx.x == 0 && threadIdx.x < 32) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32) {
     // Clusters of each sequence under the decode kernel's even split of all tiles
     // (cluster c covers tile positions [total*c/C, total*(c+1)/C)).
     const int lane = threadIdx.x;
@@ -912,101 +909,113 @@ __global__ void __launch_bounds__(256) mla_prepare_q_kernel(const MlaParams p) {
       pre += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
-  const int chunks_lat = p.Dl / 8, chunks_rope = p.Dr / 8;
-  const int per_row = chunks_lat + chunks_rope;
-  const int64_t n = (int64_t)p.B * kRows * per_row;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % per_row);
-    const int64_t bh = i / per_row;
-    const int h = (int)(bh % kRows), b = (int)(bh / kRows);
-    const uint16_t* qrow = p.q + ((int64_t)b * p.H + h) * (p.Dl + p.Dr);
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (c < chunks_lat) {
-      if (h < p.H && seq_tiles(p, b) == 0) {      // no tiles (length 0 or invalid): a zero output row
+  // Block row y = sequence; one 16-byte item per thread: the latent items first
+  // (head = idx / chunks, chunks = Dl / 8 a power of two), then the RoPE items.
+  const int b = blockIdx.y;
+  const int lat_shift = __ffs(p.Dl / 8) - 1;
+  const int n_lat = kRows << lat_shift, chunks_rope = p.Dr / 8;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint16_t* qb = p.q + (int64_t)b * p.H * (p.Dl + p.Dr);
+  if (idx < n_lat) {
+    const int h = idx >> lat_shift, c = idx & ((1 << lat_shift) - 1);
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (h < p.H) {
+      const uint4 v = *reinterpret_cast<const uint4*>(qb + (int64_t)h * (p.Dl + p.Dr) + 8 * c);
+      const float qs = p.q_scale[h];
+      if (seq_tiles(p, b) == 0) {      // no tiles (length 0 or invalid): a zero output row
         float4* orow = reinterpret_cast<float4*>(p.out + ((int64_t)b * p.H + h) * p.Dl + 8 * c);
         orow[0] = make_float4(0.f, 0.f, 0.f, 0.f);
         orow[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (h < p.H) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-        const float qs = p.q_scale[h], rqs = rcp_approx(qs);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        uint32_t r4[4];
+      const float rqs = rcp_approx(qs);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t r4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          r4[e] = pack_f16x2((float)quant_code_fast(bf16_to_float(wv[e] & 0xffffu), qs, rqs),
-                             (float)quant_code_fast(bf16_to_float(wv[e] >> 16), qs, rqs));
-        o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
-      }
-      const int r = c / (p.DH / 8), k = c % (p.DH / 8);
-      *reinterpret_cast<uint4*>(p.q_lat + (((int64_t)b * 2 + r) * kRows + h) * p.DH + 8 * k) = o;
-    } else {
-      const int k = c - chunks_lat;
-      if (h < p.H) o = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-      *reinterpret_cast<uint4*>(p.q_rope + (int64_t)b * QR_BYTES + k * 2048 + (h >> 3) * 128 + (h & 7) * 16) = o;
+      for (int e = 0; e < 4; ++e)
+        r4[e] = pack_f16x2((float)quant_code_fast(bf16_to_float(wv[e] & 0xffffu), qs, rqs),
+                           (float)quant_code_fast(bf16_to_float(wv[e] >> 16), qs, rqs));
+      o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
     }
+    const int hc = 1 << (lat_shift - 1);              // chunks per latent half
+    const int r = c >> (lat_shift - 1), k = c & (hc - 1);
+    *reinterpret_cast<uint4*>(p.q_lat + (((int64_t)b * 2 + r) * kRows + h) * p.DH + 8 * k) = o;
+  } else if (idx < n_lat + kRows * chunks_rope) {
+    const int j = idx - n_lat, h = j / chunks_rope, k = j - h * chunks_rope;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (h < p.H) o = *reinterpret_cast<const uint4*>(qb + (int64_t)h * (p.Dl + p.Dr) + p.Dl + 8 * k);
+    *reinterpret_cast<uint4*>(p.q_rope + (int64_t)b * QR_BYTES + k * 2048 + (h >> 3) * 128 + (h & 7) * 16) = o;
   }
 }
 
 // Merges the segments of every split sequence with log-sum-exp weights.  One
 // block per (sequence, latent half, softmax-warp block of 32 heads x O columns):
-// the weights of each segment per head, then every column as a weighted sum of
-// the segments' blocks (loads of all segments in flight), transposed through
-// shared memory into coalesced output rows.  Launched as the decode kernel's
-// programmatic dependent: it waits for that grid before reading its partials.
+// the (m, l) pairs of all segments in one round of loads, the per-head weights,
+// then every column as the weighted sum of the segments' blocks (two segments'
+// loads in flight per thread, four blocks resident per SM: one wave for the
+// usual sizes), transposed through shared memory into coalesced output rows.  Launched as the decode kernel's programmatic dependent: it waits
+// for that grid before reading the partials.
 template <int DH>
-__global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p) {
+__global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p) {
   constexpr int O_PER = DH >= 64 ? DH / 2 : DH;
   constexpr int NQ = O_PER / 4;                        // float4 columns of a block row
+  constexpr int PER = (32 * NQ + 255) / 256;           // float4 positions per thread
+  constexpr int KB = 2;                                // segments per round of loads
   extern __shared__ float csm[];
   float* tile = csm;                                   // [32][O_PER + 4]
-  float* wts = csm + 32 * (O_PER + 4);                 // [segments][32]
+  float* wts = tile + 32 * (O_PER + 4);                // [segments][32]
+  float2* mls = reinterpret_cast<float2*>(wts + 32 * p.num_clusters);   // [segments][32]
   pdl_wait();
   const int b = blockIdx.x, rank = blockIdx.y / kSmWarps, wp = blockIdx.y % kSmWarps;
-  const int c_first = p.seg_lo[b], c_last = p.seg_hi[b];
   const int hf = wp >> 2, qd = wp & 3;
+  const int c_first = p.seg_lo[b], c_last = p.seg_hi[b];
+  const int64_t total = *p.total_tiles;
   if (c_first < 0 || hf * O_PER >= DH) return;
   const int tid = threadIdx.x, lane = tid & 31;
   const int C = p.num_clusters;
-  const int64_t total = *p.total_tiles;
   auto covers = [&](int c) -> bool { return total >= C || total * c / C < total * (c + 1) / C; };
   auto blk = [&](int c) -> int64_t { return ((int64_t)(b + c) * 2 + rank) * kSmWarps + wp; };
   const int n = c_last - c_first + 1;
+  for (int k = tid >> 5; k < n; k += 8)
+    mls[k * 32 + lane] = covers(c_first + k) ? __ldcg(p.part_ml + blk(c_first + k) * 32 + lane)
+                                             : make_float2(-CUDART_INF_F, 0.f);
+  __syncthreads();
   if (tid < 32) {
     float M = -CUDART_INF_F;
-    for (int k = 0; k < n; ++k)
-      if (covers(c_first + k)) M = fmaxf(M, __ldcg(p.part_ml + blk(c_first + k) * 32 + lane).x);
+    for (int k = 0; k < n; ++k) M = fmaxf(M, mls[k * 32 + lane].x);
     float L = 0.f;
     for (int k = 0; k < n; ++k) {
-      float w = 0.f;
-      if (covers(c_first + k)) {
-        const float2 ml = __ldcg(p.part_ml + blk(c_first + k) * 32 + lane);
-        w = exp2f(ml.x - M);
-        L += ml.y * w;
-      }
+      const float2 ml = mls[k * 32 + lane];
+      const float w = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
       wts[k * 32 + lane] = w;
+      L += ml.y * w;
     }
     const float f = L > 0.f ? p.kv_scale[0] / L : 0.f;
     for (int k = 0; k < n; ++k) wts[k * 32 + lane] *= f;
   }
   __syncthreads();
-  // positions pos = q * 32 + lane of the block, q < NQ
-  constexpr int PER = (32 * NQ + 255) / 256;
   float4 acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int k = 0; k < n; ++k) {
-    const float w = wts[k * 32 + lane];
-    if (w == 0.f) continue;
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + blk(c_first + k) * (32 * O_PER));
+  for (int k0 = 0; k0 < n; k0 += KB) {
+    float4 v[KB][PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int pos = tid + 256 * i;
-      if (pos < 32 * NQ) {
-        const float4 v = __ldcg(src + pos);
-        acc[i].x = fmaf(v.x, w, acc[i].x); acc[i].y = fmaf(v.y, w, acc[i].y);
-        acc[i].z = fmaf(v.z, w, acc[i].z); acc[i].w = fmaf(v.w, w, acc[i].w);
+    for (int u = 0; u < KB; ++u) {
+      const int k = k0 + u;
+      const bool use = k < n && wts[min(k, n - 1) * 32 + lane] != 0.f;
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + blk(c_first + min(k, n - 1)) * (32 * O_PER));
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int pos = tid + 256 * i;
+        v[u][i] = (use && pos < 32 * NQ) ? __ldcg(src + pos) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < KB; ++u) {
+      const float w = k0 + u < n ? wts[(k0 + u) * 32 + lane] : 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        acc[i].x = fmaf(v[u][i].x, w, acc[i].x); acc[i].y = fmaf(v[u][i].y, w, acc[i].y);
+        acc[i].z = fmaf(v[u][i].z, w, acc[i].z); acc[i].w = fmaf(v[u][i].w, w, acc[i].w);
       }
     }
   }
@@ -1077,7 +1086,7 @@ cudaError_t launch_mla(cudaLaunchConfig_t cfg, cudaLaunchConfig_t ccfg, const Ml
   timing_end(cfg.stream);
   if (e != cudaSuccess) return e;
   constexpr int O_PER = DH >= 64 ? DH / 2 : DH;
-  ccfg.dynamicSmemBytes = (size_t)32 * (O_PER + 4) * sizeof(float) + (size_t)prm.num_clusters * 32 * sizeof(float);
+  ccfg.dynamicSmemBytes = (size_t)32 * (O_PER + 4) * sizeof(float) + (size_t)prm.num_clusters * 32 * 3 * sizeof(float);
   if (ccfg.dynamicSmemBytes > 48 * 1024) {
     e = cudaFuncSetAttribute(mla_combine_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ccfg.dynamicSmemBytes);
@@ -1173,11 +1182,10 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
-    const int64_t n = (int64_t)B * kRows * ((Dl + Dr) / 8);
-    int64_t blocks = (n + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    mla_prepare_q_kernel<<<(unsigned)blocks, 256, 0, s>>>(prm);
-    if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
+    const int per_seq = kRows * ((Dl + Dr) / 8);
+    if (launch_pdl(mla_prepare_q_kernel, dim3((unsigned)((per_seq + 255) / 256), (unsigned)B), dim3(256), 0, s,
+                   prm) != cudaSuccess)
+      return FA3_ECUDA;
   }
   // The decode kernel and the combine kernel are programmatic dependents of the
   // kernel before them: their launch and set-up overlap its tail.

@@ -36,6 +36,8 @@ int check_device(int* num_sms) {
 // One thread per head.
 __global__ void qparams_kernel(const float* __restrict__ mn, const float* __restrict__ mx,
                                float* __restrict__ scale, int H) {
+  pdl_wait();
+  pdl_launch_dependents();
   int h = blockIdx.x * blockDim.x + threadIdx.x;
   if (h < H) scale[h] = __fdiv_rn(fmaxf(fabsf(mn[h]), fabsf(mx[h])), 127.0f);
 }
@@ -46,6 +48,8 @@ __global__ void __launch_bounds__(256) quantize_append_vec_kernel(
     const uint4* __restrict__ kv, const float* __restrict__ scale, int8_t* __restrict__ cache,
     const int32_t* __restrict__ pos, int B, int T_new, int H, int D, int T_max,
     const uint4* __restrict__ rope_src, uint16_t* __restrict__ rope_cache, int Dr, int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t groups_per_row = D / 8;
   const int64_t n_groups = (int64_t)B * T_new * H * groups_per_row;
   const int64_t rope_groups_per_row = Dr / 8;
@@ -102,6 +106,8 @@ __global__ void __launch_bounds__(256) quantize_append_scalar_kernel(
     const uint16_t* __restrict__ kv, const float* __restrict__ scale, int8_t* __restrict__ cache,
     const int32_t* __restrict__ pos, int B, int T_new, int H, int D, int T_max,
     const uint16_t* __restrict__ rope_src, uint16_t* __restrict__ rope_cache, int Dr, int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t n = (int64_t)B * T_new * H * D;
   const int64_t n_rope = rope_cache ? (int64_t)B * T_new * Dr : 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -163,8 +169,7 @@ FA3_API int fa3_qparams(const float* min_v, const float* max_v, float* scale, in
   int st = check_device(nullptr);
   if (st != FA3_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  qparams_kernel<<<(H + 127) / 128, 128, 0, s>>>(min_v, max_v, scale, H);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_pdl(qparams_kernel, dim3((H + 127) / 128), dim3(128), 0, s, min_v, max_v, scale, H));
 }
 
 FA3_API int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* cache, const int32_t* pos,
@@ -187,13 +192,14 @@ FA3_API int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* 
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  cudaError_t e;
   if (vec) {
-    quantize_append_vec_kernel<<<(unsigned)blocks, 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(kv), scale, cache, pos, B, T_new, H, D, T_max,
-        reinterpret_cast<const uint4*>(rope_src), rope_cache, Dr, dev_err);
+    e = launch_pdl(quantize_append_vec_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+                   reinterpret_cast<const uint4*>(kv), scale, cache, pos, B, T_new, H, D, T_max,
+                   reinterpret_cast<const uint4*>(rope_src), rope_cache, Dr, dev_err);
   } else {
-    quantize_append_scalar_kernel<<<(unsigned)blocks, 256, 0, s>>>(kv, scale, cache, pos, B, T_new, H, D, T_max,
-                                                                   rope_src, rope_cache, Dr, dev_err);
+    e = launch_pdl(quantize_append_scalar_kernel, dim3((unsigned)blocks), dim3(256), 0, s, kv, scale, cache, pos, B,
+                   T_new, H, D, T_max, rope_src, rope_cache, Dr, dev_err);
   }
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
