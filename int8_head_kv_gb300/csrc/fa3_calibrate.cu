@@ -134,6 +134,8 @@ __global__ void __launch_bounds__(kHistThreads, 1)
 hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t N,
             int chunks_per_head, int total_chunks, uint32_t* __restrict__ counts, int vec,
             const TailInfo* __restrict__ tails) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ uint4 smem_hist[];
   uint32_t* bins = reinterpret_cast<uint32_t*>(smem_hist);   // 32768 words = 65536 16-bit bins
   const int tid = threadIdx.x;
@@ -223,6 +225,8 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
 __global__ void __launch_bounds__(kTailThreads)
 tail_count_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int H,
                   uint32_t* __restrict__ counts, const TailInfo* __restrict__ tails) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int row = blockIdx.y, h = row % H, b = row / H;
   const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)b * stride_b + (int64_t)h * stride_h);
   const int64_t groups = L / 8;
@@ -300,6 +304,8 @@ __device__ __forceinline__ void select_bin(const uint32_t* hist, uint32_t r, boo
 __global__ void __launch_bounds__(kSampleThreads)
 tail_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t N,
             unsigned long long span, int vec, TailInfo* __restrict__ tails) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int kUnits = kSampleUnits / kSampleThreads;    // 16 samples per thread
   constexpr int kWarps = kSampleThreads / 32;
   __shared__ uint32_t whist[kWarps][256];        // per-warp high-byte histograms
@@ -412,6 +418,8 @@ __global__ void __launch_bounds__(kWinThreads, 1)
 window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long long t,
               float* __restrict__ min_io, float* __restrict__ max_io, TailInfo* __restrict__ tails, int mode,
               const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int vec) {
+  pdl_wait();
+  pdl_launch_dependents();
   // mode 0: tail counts (few windows); mode 1: the heads flagged by mode 0 are
   // counted here in full and searched again, other heads return at once;
   // mode 2: full counts from the histogram kernel, no tail state.
@@ -700,29 +708,35 @@ FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L
     return FA3_ECUDA;
   if (fast) {
     // tails only, then a full pass over the heads whose tails turned out too thin
-    tail_kernel<<<H, kSampleThreads, 0, s>>>(x, L, stride_b, stride_h, N, span, vec, tails);
+    if (launch_pdl(tail_kernel, dim3(H), dim3(kSampleThreads), 0, s, x, L, stride_b, stride_h, N, span, vec, tails) !=
+        cudaSuccess)
+      return FA3_ECUDA;
     timing_begin(s);
     const int64_t per_cta = (int64_t)kTailThreads * kTailGroups;
     const int64_t xb = (L / 8 + per_cta - 1) / per_cta, rows = B * (int64_t)H;
     if (vec && xb <= 0x7fffffff && rows <= 65535) {
-      tail_count_kernel<<<dim3((unsigned)xb, (unsigned)rows), kTailThreads, 0, s>>>(x, L, stride_b, stride_h, H,
-                                                                                    counts, tails);
+      if (launch_pdl(tail_count_kernel, dim3((unsigned)xb, (unsigned)rows), dim3(kTailThreads), 0, s, x, L,
+                     stride_b, stride_h, H, counts, static_cast<const TailInfo*>(tails)) != cudaSuccess)
+        return FA3_ECUDA;
     } else {
-      hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, chunks_per_head,
-                                                    (int)total_chunks, counts, vec, tails);
+      if (launch_pdl(hist_kernel, dim3(grid), dim3(kHistThreads), smem, s, x, L, stride_b, stride_h, N,
+                     chunks_per_head, (int)total_chunks, counts, vec, static_cast<const TailInfo*>(tails)) != cudaSuccess)
+        return FA3_ECUDA;
     }
     timing_end(s);
-    window_kernel<<<H, kWinThreads, wsmem, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io,
-                                                 tails, 0, x, L, stride_b, stride_h, vec);
-    window_kernel<<<H, kWinThreads, wsmem, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io,
-                                                 tails, 1, x, L, stride_b, stride_h, vec);
+    for (int mode = 0; mode < 2; ++mode)
+      if (launch_pdl(window_kernel, dim3(H), dim3(kWinThreads), wsmem, s, counts, (unsigned long long)N,
+                     (unsigned long long)t, min_io, max_io, tails, mode, x, L, stride_b, stride_h, vec) != cudaSuccess)
+        return FA3_ECUDA;
   } else {
     timing_begin(s);
-    hist_kernel<<<grid, kHistThreads, smem, s>>>(x, L, stride_b, stride_h, N, chunks_per_head, (int)total_chunks,
-                                                  counts, vec, nullptr);
+    if (launch_pdl(hist_kernel, dim3(grid), dim3(kHistThreads), smem, s, x, L, stride_b, stride_h, N,
+                   chunks_per_head, (int)total_chunks, counts, vec, static_cast<const TailInfo*>(nullptr)) != cudaSuccess)
+      return FA3_ECUDA;
     timing_end(s);
-    window_kernel<<<H, kWinThreads, wsmem, s>>>(counts, (unsigned long long)N, (unsigned long long)t, min_io, max_io,
-                                                 tails, 2, x, L, stride_b, stride_h, vec);
+    if (launch_pdl(window_kernel, dim3(H), dim3(kWinThreads), wsmem, s, counts, (unsigned long long)N,
+                   (unsigned long long)t, min_io, max_io, tails, 2, x, L, stride_b, stride_h, vec) != cudaSuccess)
+      return FA3_ECUDA;
   }
   return cuda_status(cudaGetLastError());
 }

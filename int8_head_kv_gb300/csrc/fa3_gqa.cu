@@ -110,6 +110,8 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
 }
 
 __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
+  pdl_wait();
+  pdl_launch_dependents();
   // Per-warp rings of 16-token K/V steps.  A 128-byte row stores its 16-byte
   // chunk c at position c ^ f(row & 7), f(r) = (r & 6) ^ 4 (r & 1): every 8-lane
   // phase of the K and V fragment loads below then touches 8 distinct 16-byte
@@ -304,6 +306,8 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
 }
 
 __global__ void __launch_bounds__(kD) gqa_combine_kernel(const GqaArgs p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
   const int g = h / p.G, hh = h - g * p.G;
   const int64_t slot0 = (((int64_t)b * p.Hkv + g) * p.splits) * kHeadsPerTile + hh;
@@ -413,13 +417,11 @@ FA3_API int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* 
   if (cudaFuncSetAttribute(gqa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return FA3_ECUDA;
   timing_begin(s);
-  gqa_decode_kernel<<<dim3(splits, Hkv, B), kThreads, kSmemBytes, s>>>(a);
+  const cudaError_t le = launch_pdl(gqa_decode_kernel, dim3(splits, Hkv, B), dim3(kThreads), kSmemBytes, s, a);
   timing_end(s);
-  if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
-  if (splits > 1) {
-    gqa_combine_kernel<<<dim3(Hq, B), kD, 0, s>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return FA3_ECUDA;
-  }
+  if (le != cudaSuccess) return FA3_ECUDA;
+  if (splits > 1 && launch_pdl(gqa_combine_kernel, dim3(Hq, B), dim3(kD), 0, s, a) != cudaSuccess)
+    return FA3_ECUDA;
   return FA3_OK;
 }
 
