@@ -136,3 +136,32 @@ def test_forced_rescales():
     inp.krope = krope
     got = _run(F, w, inp, q_scale, kv_scale, ckv8, lens)
     assert_attn_close(got, _oracle(w, inp, q_scale, kv_scale, ckv8, lens), what="forced rescales")
+
+
+def test_stream_order_with_other_kernels_between_calls():
+    # The library's kernels are programmatic dependents of the kernel before them:
+    # each call must still see the query and lengths that ordinary device copies wrote
+    # just before it, and the copies after it must see its finished output.
+    F = fa3()
+    w = W.mla_dsv3(B=2, T=2048)
+    inp, q_scale, kv_scale, ckv8, _ = _prepare(w)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    variants = [(W.bf16_round(inp.q * s), np.array(ls, np.int32))
+                for s, ls in ((1.0, [2048, 1500]), (-0.7, [900, 2048]), (1.3, [64, 1]))]
+    dq = torch.empty(inp.q.shape, dtype=torch.bfloat16, device="cuda")
+    dl = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    out = torch.empty(w.B, w.H, w.Dl, dtype=torch.float32, device="cuda")
+    ws = torch.empty(F.mla_workspace_size(w.B, w.H, w.Dl, w.T_max), dtype=torch.uint8, device="cuda")
+    srcs = [(bf16_dev(q), t(ls)) for q, ls in variants]
+    ck, kr, qs, kvs = t(ckv8), bf16_dev(inp.krope), t(q_scale), t(kv_scale)
+    keep = []
+    torch.cuda.synchronize()
+    for (sq, sl) in srcs:
+        dq.copy_(sq)
+        dl.copy_(sl)
+        F.decode_attn_mla(dq, ck, kr, qs, kvs, dl, w.softmax_scale, out=out, workspace=ws)
+        keep.append(out.clone())
+    torch.cuda.synchronize()
+    for (q, ls), got in zip(variants, keep):
+        inp.q = q
+        assert_attn_close(got.cpu().numpy(), _oracle(w, inp, q_scale, kv_scale, ckv8, ls), what=f"ordered {ls}")
