@@ -75,6 +75,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Exact integer m16n8k32 MMA on int8 codes (s32 accumulate).
+__device__ __forceinline__ void mma16832_s8(int (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -135,9 +145,11 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
   const int t_begin = split * p.chunk;
   const int t_end = min(t_begin + p.chunk, n);
 
-  // Q^T fragments of head r of this group, contraction order permuted so that
-  // k-step s takes bytes [16qd + 4s, +4) (s < 4) or [64 + 16qd + 4(s-4), +4).
-  uint32_t qb[8][2];
+  // Q^T fragments of head r of this group as int8 words, contraction order
+  // permuted: thread (r, qd) holds row bytes [16qd, +16) as words 0-3 and
+  // [64 + 16qd, +16) as words 4-7; k32-step s takes words 2s and 2s + 1 of Q
+  // (B operand) and of its K rows r and r + 8 (A operand) alike.
+  uint32_t qw[8];
   {
     uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
     if (r < G) {
@@ -146,9 +158,9 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
       q1 = *reinterpret_cast<const uint4*>(qrow + 64 + 16 * qd);
     }
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      i8x4_to_f16x4(word(q0, s), qb[s][0], qb[s][1]);
-      i8x4_to_f16x4(word(q1, s), qb[s + 4][0], qb[s + 4][1]);
+    for (int j = 0; j < 4; ++j) {
+      qw[j] = word(q0, j);
+      qw[4 + j] = word(q1, j);
     }
   }
   const int h0 = 2 * qd, h1 = 2 * qd + 1;
@@ -208,20 +220,20 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
     vr[2] = lds128(chunk_addr(vst, 2 * qd + 8, r));
     vr[3] = lds128(chunk_addr(vst, 2 * qd + 9, r));
     __syncwarp();   // every lane has its fragments: the stage may be refilled
-    // ---- scores S^T = K . Q^T (exact integer dot products in fp32)
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- scores S^T = K . Q^T: exact integer dot products (int8 MMA, s32)
+    int c[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint32_t a0, a1, a2, a3;
-      i8x4_to_f16x4(word(kr[s < 4 ? 0 : 1], s & 3), a0, a2);
-      i8x4_to_f16x4(word(kr[s < 4 ? 2 : 3], s & 3), a1, a3);
-      mma16816(c, a0, a1, a2, a3, qb[s][0], qb[s][1]);
+    for (int s = 0; s < 4; ++s) {
+      const uint4& ka = kr[s < 2 ? 0 : 1];
+      const uint4& kb = kr[s < 2 ? 2 : 3];
+      const int w0 = (2 * s) & 3, w1 = (2 * s + 1) & 3;
+      mma16832_s8(c, word(ka, w0), word(kb, w0), word(ka, w1), word(kb, w1), qw[2 * s], qw[2 * s + 1]);
     }
     const bool va = t0 + r < t_end, vb = t0 + r + 8 < t_end;
-    float x0 = va ? c[0] * c0s : -CUDART_INF_F;
-    float x1 = va ? c[1] * c1s : -CUDART_INF_F;
-    float x2 = vb ? c[2] * c0s : -CUDART_INF_F;
-    float x3 = vb ? c[3] * c1s : -CUDART_INF_F;
+    float x0 = va ? (float)c[0] * c0s : -CUDART_INF_F;
+    float x1 = va ? (float)c[1] * c1s : -CUDART_INF_F;
+    float x2 = vb ? (float)c[2] * c0s : -CUDART_INF_F;
+    float x3 = vb ? (float)c[3] * c1s : -CUDART_INF_F;
 
     // ---- online softmax (log2 domain); rows of a head live in the 8 lanes sharing qd
     float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
