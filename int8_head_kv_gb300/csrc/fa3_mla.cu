@@ -106,6 +106,7 @@ struct MlaParams {
   CUtensorMap tm_rope;   // bf16 viewed as (8, T_max, Dr/8, B), box {8, 64, Dr/8, 1}
   const uint16_t* q;
   const int8_t* ckv;     // [B][T_max][Dl]
+  const uint16_t* krope; // [B][T_max][Dr] bf16 (L2 prefetch; the tiles themselves come through tm_rope)
   const float* q_scale;
   const float* kv_scale;
   const int32_t* lens;
@@ -154,6 +155,11 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t a, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok) : "r"(a), "r"(parity) : "memory");
   return ok != 0;
+}
+// Bulk prefetch of a contiguous global range into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
 }
 // Bulk asynchronous copy global -> this CTA's shared memory, completing on an mbarrier.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -484,11 +490,32 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           v[i] = __ldg(reinterpret_cast<const uint4*>(p.ckv + ((int64_t)b * p.T_max + row) * p.Dl + rank * DH) + cc);
       }
     };
+    // The register loads run one tile ahead, which is shorter than the HBM latency:
+    // the first converter thread of CTA 0 also prefetches into L2 the latent rows
+    // (both halves) and RoPE key rows of the tile kPrefetch tiles ahead.
+    constexpr int kPrefetch = 4;
+    const bool pf_issuer = ct == 0 && rank == 0;
+    TileWalk pfw{walk0};
+    auto prefetch = [&]() {
+      const int rows = min(kTok, p.T_max - pfw.tt * kTok);
+      const int64_t row0 = (int64_t)pfw.b * p.T_max + (int64_t)pfw.tt * kTok;
+      prefetch_l2(p.ckv + row0 * p.Dl, (uint32_t)(rows * p.Dl));
+      if (p.Dr > 0) prefetch_l2(p.krope + row0 * p.Dr, (uint32_t)(rows * p.Dr * 2));
+    };
+    bool pf_more = pf_issuer && pfw.next(p);
+    for (int i = 0; i < kPrefetch && pf_more; ++i) {
+      prefetch();
+      pf_more = pfw.next(p);
+    }
     bool more = tw.next(p);
     if (more) load(tw.b, tw.tt);
     uint32_t it = 0;
     bool ok = true;
     for (; ok && more; ++it) {
+      if (pf_more) {
+        prefetch();
+        pf_more = pfw.next(p);
+      }
       if (rope_issuer) {
         const uint32_t st = it % NR;
         ok = wait_bar(bar(B_ROPE_EMPTY + st), ((it / NR) & 1u) ^ 1u, abort_flag, p.err);
@@ -1167,7 +1194,7 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
       return FA3_ECUDA;
   }
   char* ws = static_cast<char*>(workspace);
-  prm.q = q; prm.ckv = ckv; prm.q_scale = q_scale; prm.kv_scale = kv_scale; prm.lens = lens; prm.out = out;
+  prm.q = q; prm.ckv = ckv; prm.krope = krope; prm.q_scale = q_scale; prm.kv_scale = kv_scale; prm.lens = lens; prm.out = out;
   prm.part_o = reinterpret_cast<float*>(ws);
   prm.part_ml = reinterpret_cast<float2*>(ws + off_ml);
   prm.q_lat = reinterpret_cast<uint16_t*>(ws + off_qlat);
