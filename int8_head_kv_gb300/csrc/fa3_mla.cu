@@ -56,15 +56,16 @@ constexpr int kConvWarp0 = 9;     // converters (3 warps); the first thread also
 constexpr int kConvThreads = 96;
 constexpr int kRows = 128;        // heads (TMEM lanes)
 constexpr int NR = 2;             // RoPE key tile stages (TMA)
-constexpr int NC = 3;             // fp16 latent tile buffers (Q.C^T runs two tiles ahead of P.C)
+constexpr int NC = 4;             // fp16 latent tile buffers (Q.C^T runs two tiles ahead of P.C)
 
 // Shared memory map (bytes from a 1024-byte aligned base).
-constexpr uint32_t OFF_QR = 0;                                   // bf16 RoPE query, all Dr dims (<= 16 KB)
-constexpr uint32_t QR_BYTES = 16384;
-constexpr uint32_t OFF_C16 = OFF_QR + QR_BYTES;                  // NC x fp16 latent tile half (<= 32 KB)
+constexpr uint32_t QR_BYTES = 16384;                             // prepared RoPE query image of a sequence
+constexpr uint32_t OFF_QR = 0;                                   // this CTA's RoPE query share (<= 8 KB)
+constexpr uint32_t QR_CTA_BYTES = 8192;
+constexpr uint32_t OFF_C16 = OFF_QR + QR_CTA_BYTES;              // NC x fp16 latent tile half (<= 32 KB)
 constexpr uint32_t C16_BYTES = 32768;
-constexpr uint32_t OFF_ROPE = OFF_C16 + NC * C16_BYTES;          // NR x bf16 RoPE key tile (<= 8 KB)
-constexpr uint32_t ROPE_BYTES = 8192;
+constexpr uint32_t OFF_ROPE = OFF_C16 + NC * C16_BYTES;          // NR x this CTA's share of a bf16 RoPE key tile
+constexpr uint32_t ROPE_BYTES = 4096;
 constexpr uint32_t OFF_P = OFF_ROPE + NR * ROPE_BYTES;           // fp16 P, 128 x 64 (16 KB)
 // Partial-score exchange, double-buffered: slot s of X receives the peer's fp32
 // partial scores of every other tile, written by the peer's st.async.  Each
@@ -372,10 +373,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   const int cluster = blockIdx.x >> 1;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * (uint32_t)i; };
-  const int rope_chunks = p.Dr / 8;                 // 8-wide RoPE chunks of the key tile (TMA box)
   // The RoPE term is split over the pair: CTA r contracts 16-wide chunks [rk0, rk1).
   const int rope_k = p.Dr / 16;
   const int rk0 = rank == 0 ? 0 : (rope_k + 1) / 2, rk1 = rank == 0 ? (rope_k + 1) / 2 : rope_k;
+  const bool has_rope = rk1 > rk0;
 
   // ---- set-up: barriers, TMEM, schedule
   if (tid == 0) {
@@ -466,7 +467,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
   pdl_wait();
   pdl_launch_dependents();
   SegWalk walk0{sched[2], sched[3], sched[1], (int)sched[0]};
-  const uint32_t rope_tx = (uint32_t)(kTok * 2 * p.Dr);
+  // RoPE key TMA box: 2 * ((Dr/16 + 1) / 2) 8-wide chunks from chunk 2 * rk0 (a box
+  // reaching past Dr is zero-filled and its bytes still count).
+  const uint32_t rope_tx = (uint32_t)(kTok * 16 * 2 * ((rope_k + 1) / 2));
 
   if (warp >= kConvWarp0) {
     // ------------------------------------------------------ int8 -> fp16 converters
@@ -477,7 +480,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     // consecutive 16-byte rows, without bank conflicts.
     // The first converter thread also streams the RoPE key tiles in with TMA.
     const int ct = tid - kConvWarp0 * 32;
-    const bool rope_issuer = (ct == 0) && rope_chunks > 0;
+    const bool rope_issuer = (ct == 0) && has_rope;
     TileWalk tw{walk0};
     uint4 v[CONV_UNITS];
     auto load = [&](int b, int tt) {
@@ -521,7 +524,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         ok = wait_bar(bar(B_ROPE_EMPTY + st), ((it / NR) & 1u) ^ 1u, abort_flag, p.err);
         if (ok) {
           mbar_expect_tx(bar(B_ROPE_FULL + st), rope_tx);
-          tma_4d(sbase + OFF_ROPE + st * ROPE_BYTES, &p.tm_rope, 0, tw.tt * kTok, 0, tw.b, bar(B_ROPE_FULL + st));
+          tma_4d(sbase + OFF_ROPE + st * ROPE_BYTES, &p.tm_rope, 0, tw.tt * kTok, 2 * rk0, tw.b,
+                 bar(B_ROPE_FULL + st));
         }
       }
       const uint32_t cs = it % NC;
@@ -556,7 +560,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       const uint32_t id_qk = idesc_f16(128, kTok, false, false);
       const uint32_t id_rope = idesc_f16(128, kTok, true, false);
       const uint32_t id_pv = idesc_f16(128, DH, false, true);
-      const uint32_t qr_bytes = (uint32_t)rope_chunks * 2048u;
+      const uint32_t qr_bytes = (uint32_t)(rk1 - rk0) * 4096u;
       SegWalk w = walk0;
       int b, lo, hi, tb;
       uint32_t it = 0, seg = 0;
@@ -585,7 +589,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         if (!(wait_bar(bar(B_C16_FULL + cs), (j / NC) & 1u, abort_flag, p.err) &&
               wait_bar(bar(B_S_EMPTY), (j & 1u) ^ 1u, abort_flag, p.err)))
           return false;
-        if (rope_chunks > 0 && !wait_bar(bar(B_ROPE_FULL + st), (j / NR) & 1u, abort_flag, p.err)) return false;
+        if (has_rope && !wait_bar(bar(B_ROPE_FULL + st), (j / NR) & 1u, abort_flag, p.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
@@ -593,8 +597,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
           mma_f16_ts(tmem + TM_S, tmem + TM_QA + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
         }
         for (int kk = rk0; kk < rk1; ++kk) {
-          const uint64_t a = sdesc(sbase + OFF_QR + kk * 4096, 2048, 128);
-          const uint64_t bd = sdesc(sbase + OFF_ROPE + st * ROPE_BYTES + kk * 2048, 1024, 128);
+          const uint64_t a = sdesc(sbase + OFF_QR + (kk - rk0) * 4096, 2048, 128);
+          const uint64_t bd = sdesc(sbase + OFF_ROPE + st * ROPE_BYTES + (kk - rk0) * 2048, 1024, 128);
           mma_f16(tmem + TM_R, a, bd, id_rope, kk > rk0 ? 1u : 0u);
         }
         mma_commit(bar(B_S_FULL));
@@ -609,7 +613,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         if (!ok) break;
         if (qr_bytes) {
           mbar_expect_tx(bar(B_QR_FULL), qr_bytes);
-          bulk_g2s(sbase + OFF_QR, p.q_rope + (size_t)b * QR_BYTES, qr_bytes, bar(B_QR_FULL));
+          bulk_g2s(sbase + OFF_QR, p.q_rope + (size_t)b * QR_BYTES + rk0 * 4096, qr_bytes, bar(B_QR_FULL));
           ok = wait_bar(bar(B_QR_FULL), seg & 1u, abort_flag, p.err);
         }
         ok = ok && wait_bar(bar(B_Q_READY), seg & 1u, abort_flag, p.err);   // latent query in TMEM
@@ -658,7 +662,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
       if (lane == 0) mbar_arrive(bar(which));
     };
     const uint32_t peer_xe = mapa(bar(B_XE), peer);
-    const bool has_rope = rk1 > rk0;
     // This CTA's partial score of tile j for this warp's 32 tokens, in log2 units:
     //   (latent partial) * q_scale * kv_scale * c + (RoPE share) * c.
     // It stays in registers (own) and goes, as fp32, into the peer's X slot by
@@ -1186,7 +1189,8 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
     // (8 values, token, 8-wide chunk, sequence): one box lands as K-major core matrices.
     const cuuint64_t dims[4] = {8, (cuuint64_t)T_max, (cuuint64_t)(Dr / 8), (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)Dr * 2, 16, (cuuint64_t)Dr * 2 * T_max};
-    const cuuint32_t box[4] = {8, (cuuint32_t)kTok, (cuuint32_t)(Dr / 8), 1};
+    // one CTA's share: 2 * ((Dr/16 + 1) / 2) chunks (the decode kernel's RoPE split over the pair)
+    const cuuint32_t box[4] = {8, (cuuint32_t)kTok, (cuuint32_t)(2 * ((Dr / 16 + 1) / 2)), 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     if (encode(&prm.tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(krope), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
