@@ -897,7 +897,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 // One thread per 8 values of one (sequence, head); heads >= H are zero.  Also
 // writes the zero output rows of sequences without tiles and lists the clusters
 // of every split sequence for mla_combine_kernel.
-__global__ void __launch_bounds__(256, 8) mla_prepare_q_kernel(const MlaParams p) {
+__global__ void __launch_bounds__(256, 6) mla_prepare_q_kernel(const MlaParams p) {
   pdl_wait();
   pdl_launch_dependents();   // the decode kernel may start its set-up
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32) {
