@@ -72,6 +72,12 @@ def test_edge_lengths_errors_and_small_shapes():
                        lens=[200, 129], calib_q_shape=(2, 128, 4, 256), calib_kv_shape=(1, 1, 256, 256))
     a3 = _prepare(w3)
     assert_attn_close(_run(F, w3, *a3), _oracle(w3, *a3), what="h128 dl256 dr32")
+    # Dr = 48: three 16-wide RoPE chunks, split 2 / 1 over the pair; the second CTA's
+    # RoPE key box reaches past Dr and is zero-filled there
+    w4 = W.MLAWorkload(name="h64 dl512 dr48", B=2, H=64, Dl=512, Dr=48, T_max=260, softmax_scale=0.08,
+                       lens=[260, 77], calib_q_shape=(2, 64, 4, 512), calib_kv_shape=(1, 1, 256, 512))
+    a4 = _prepare(w4)
+    assert_attn_close(_run(F, w4, *a4), _oracle(w4, *a4), what="h64 dl512 dr48")
 
 
 @pytest.mark.slow
