@@ -16,7 +16,9 @@
 //     contiguous K bytes per k-step (Q is permuted the same way);
 //   * P^T (fp16) comes from the score fragment by movmatrix.trans;
 //   * O^T[128 x 8] += V^T . P^T, the 16 output dims of a thread contiguous so
-//     every thread loads 16 contiguous V bytes per token;
+//     every thread loads 16 contiguous V bytes per token; V enters the f16 MMA as
+//     code + 1152 (two byte permutes per four codes, no subtraction), and the bias
+//     times the row sum of P is taken off once at the end;
 //   * split-K partials (unnormalised O, running max m, sum l) are merged by a
 //     small combine kernel with log-sum-exp weights.
 #include "fa3_common.cuh"
@@ -56,16 +58,6 @@ struct GqaArgs {
   float sm_log2;    // softmax_scale * log2(e)
 };
 
-// Four signed int8 codes -> two f16x2 (exact): bias to unsigned, place each
-// byte under the f16 exponent of 1024, subtract 1024 + 128.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  lo = __byte_perm(u, 0x64646464u, 0x4140);
-  hi = __byte_perm(u, 0x64646464u, 0x4342);
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
-}
-
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -73,6 +65,17 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four signed int8 codes -> two f16x2 holding code + 1152 (exact): the bias to
+// unsigned and the f16 exponent of 1024 without the subtraction.  P.V on these
+// values is P.V + 1152 * sum(P), and sum(P) is the row sum l that the softmax keeps
+// from the same fp16 P values, so the output is v_scale * (O / l - 1152).
+constexpr float kVBias = 1152.f;
+__device__ __forceinline__ void i8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4140);
+  hi = __byte_perm(u, 0x64646464u, 0x4342);
 }
 
 // Exact integer m16n8k32 MMA on int8 codes (s32 accumulate).
@@ -266,8 +269,8 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
       const uint32_t p01 = __byte_perm(word(vr[0], i >> 1), word(vr[1], i >> 1), sel);
       const uint32_t p23 = __byte_perm(word(vr[2], i >> 1), word(vr[3], i >> 1), sel);
       uint32_t a0, a1, a2, a3;
-      i8x4_to_f16x4(p01, a0, a1);
-      i8x4_to_f16x4(p23, a2, a3);
+      i8x4_to_f16x4_biased(p01, a0, a1);
+      i8x4_to_f16x4_biased(p23, a2, a3);
       mma16816(o[i], a0, a1, a2, a3, b0, b1);
     }
   }
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
       }
     }
     if (p.splits == 1) {
-      const float val = L > 0.f ? p.v_scale[g] * (O / L) : 0.f;
+      const float val = L > 0.f ? p.v_scale[g] * (O / L - kVBias) : 0.f;
       p.out[((int64_t)b * p.Hq + g * G + hh) * kD + d] = __float2bfloat16_rn(val);
     } else {
       const int64_t slot = (((int64_t)b * p.Hkv + g) * p.splits + split) * kHeadsPerTile + hh;
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kD) gqa_combine_kernel(const GqaArgs p) {
       }
     }
   }
-  const float val = L > 0.f ? p.v_scale[g] * (O / L) : 0.f;
+  const float val = L > 0.f ? p.v_scale[g] * (O / L - kVBias) : 0.f;
   p.out[((int64_t)b * p.Hq + h) * kD + d] = __float2bfloat16_rn(val);
 }
 
