@@ -16,10 +16,11 @@
 //     integer latent score;
 //   * the fp32 accumulator of 128 heads x 512 latent is all of one SM's TMEM, so
 //     a 2-CTA cluster splits the latent in halves: CTA r owns latent columns
-//     [r*Dl/2, (r+1)*Dl/2), TMA-loads only that half of each 64-token tile,
-//     converts it to fp16 core matrices in shared memory (one buffer is the
-//     K-major B operand of Q.C^T and the MN-major B operand of P.C) and keeps
-//     its O half in TMEM;
+//     [r*Dl/2, (r+1)*Dl/2), loads only that half of each 64-token tile into
+//     registers one tile ahead (with an L2 bulk prefetch four tiles ahead),
+//     converts it to fp16 core matrices in one of four shared-memory buffers
+//     (one buffer is the K-major B operand of Q.C^T and the MN-major B operand
+//     of P.C) and keeps its O half in TMEM;
 //   * the quantized latent query lives in TMEM as the A operand of Q.C^T; the
 //     RoPE term is split over the pair (each CTA contracts half of the RoPE
 //     dims from a TMA-loaded bf16 key tile); each CTA scales its exact latent
@@ -33,9 +34,11 @@
 //   * split-K: the tiles of all sequences are dealt out evenly to the clusters
 //     that fit on the GPU; a cluster's piece of a sequence is a segment; for a
 //     split sequence each softmax warp leaves its block of O (unnormalised, with
-//     the rows' m and l) in the workspace, and the warp that completes the last
-//     copy of that block (a per-block counter) merges all segments' blocks with
-//     log-sum-exp weights and writes the output rows.
+//     the rows' m and l) in the workspace, and mla_combine_kernel merges all
+//     segments' blocks with log-sum-exp weights into the output rows;
+//   * the query pre-pass, this kernel and the combine kernel are programmatic
+//     dependent launches: each waits (griddepcontrol) for the previous grid
+//     before it reads what that grid wrote.
 // Every wait is bounded; on time-out the kernel sets FA3_DEVERR_TIMEOUT, drains
 // its own copies and MMAs, frees its TMEM and returns.
 #include "fa3_common.cuh"
