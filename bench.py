@@ -178,6 +178,22 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def slowest_rank_ms(ms_local, world, device):
+    """The largest of the ranks' times (every rank's units are counted against it)."""
+    if world <= 1:
+        return float(ms_local)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, ms_slowest, world):
+    """Units per second of the whole job: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / (ms_slowest / 1e3)
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args):
     import torch
@@ -298,11 +314,7 @@ def run_gpu(args):
         clk.mark_end()
         if world > 1:
             dist.barrier()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = slowest_rank_ms(t0.elapsed_time(t1), world, dev)
     F.set_kernel_timing(None, None)
     ms_step = ms_total / args.steps
     mla_ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in mla_ev)
@@ -365,7 +377,7 @@ def run_gpu(args):
     e2e_run(args.steps)
     a1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a0.elapsed_time(a1) / args.steps
+    e2e_ms = slowest_rank_ms(a0.elapsed_time(a1), world, dev) / args.steps
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
 
@@ -373,7 +385,7 @@ def run_gpu(args):
     hbm = pk.get("hbm_gbs", 6800.0)
     bf16 = pk.get("bf16_tflops", 1900.0)
     tokens = B * world
-    value = tokens / (ms_step / 1e3)
+    value = whole_job_rate(B, ms_step, world)
     kv_gbs = kv_bytes_per_step() / (mla_ms / 1e3) / 1e9           # whole decode call
     k_tflops = flops_per_step() / (kern_ms / 1e3) / 1e12          # main kernel alone
     k_gbs = kv_bytes_per_step() / (kern_ms / 1e3) / 1e9
