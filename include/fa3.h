@@ -26,7 +26,11 @@
  *     NULL) and skip the offending row; the caller reads the word when it
  *     likes.  Kernels never trap and every wait inside them is bounded.
  *   - Calls on the same stream are ordered; calls that share a workspace
- *     must not run concurrently on different streams.
+ *     must not run concurrently on different streams.  The library's kernels
+ *     are launched as programmatic dependents of the work before them on the
+ *     stream (their launch overlaps its tail), and each waits for that work to
+ *     complete before it reads or writes memory, so stream order holds for
+ *     every buffer a caller passes.
  */
 #ifndef FA3_H_
 #define FA3_H_
