@@ -198,8 +198,9 @@ int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v,
  * Same arguments and results as fa3_decode_attn_gqa, without the workspace:
  * the split-K partials go to a fixed 8 MiB array in the library's own device
  * memory, which every GPU that loads libfa3.so holds until the process exits.
- * Sizes whose partials need more than 8 MiB (fa3_gqa_workspace_size() >
- * 8 MiB) return FA3_EWORKSPACE; use fa3_decode_attn_gqa for them.
+ * Sizes whose partials would need more than 8 MiB (fa3_gqa_workspace_size() >
+ * 8 MiB) return FA3_EWORKSPACE; the split plan (at most one wave of resident
+ * CTAs, 4 KB of partials each) keeps every size below 2 MiB on GB300.
  * The first call on each device looks up the array's device address (this
  * may initialise the module on that device): make that first call before any
  * stream capture.  All calls share the one array and it keeps the last call's

@@ -349,23 +349,18 @@ __global__ void __launch_bounds__(kD) gqa_combine_kernel(const GqaArgs p) {
 
 int gqa_blocks_per_sm();
 
-// Split-K plan: the (split, KV head, sequence) grid is sized to a whole number of
-// waves of resident CTAs, with chunks of at least 64 tokens.
+// Split-K plan: as many splits as keep the (split, KV head, sequence) grid within
+// one wave of resident CTAs (at least one split, chunks of at least 64 tokens).
+// Measured on the Llama-70B shape (128 units, 456 resident CTAs): 3 splits
+// (384 CTAs, one wave) 31.5 us, 4 splits (512 CTAs, a second partial wave)
+// 37.6 us, 7 splits (896 CTAs, two full waves) 34.5 us: each CTA's prologue and
+// merge are worth far more than a few tokens, so a single wave of longer chunks wins.
 void gqa_plan(int B, int Hkv, int T_max, int num_sms, int* splits, int* chunk) {
   const int64_t units = (int64_t)B * Hkv;
   const int64_t wave = (int64_t)num_sms * gqa_blocks_per_sm();
-  int best_s = 1;
-  double best_cost = 1e30;
-  const int max_s = (int)std::max<int64_t>(1, (T_max + 63) / 64);
-  for (int sp = 1; sp <= max_s && sp <= 64; ++sp) {
-    const int64_t ctas = units * sp;
-    const int64_t waves = (ctas + wave - 1) / wave;
-    const int64_t per = ((int64_t)T_max + sp - 1) / sp;
-    // time ~ waves x tokens per CTA, plus a fixed per-CTA cost worth ~32 tokens
-    const double cost = (double)waves * (double)(per + 32);
-    if (cost < best_cost - 1e-9) { best_cost = cost; best_s = sp; }
-  }
-  int64_t per = ((int64_t)T_max + best_s - 1) / best_s;
+  const int64_t max_s = std::max<int64_t>(1, std::min<int64_t>(64, (T_max + 63) / 64));
+  const int64_t sp = std::max<int64_t>(1, std::min<int64_t>(max_s, wave / units));
+  int64_t per = ((int64_t)T_max + sp - 1) / sp;
   per = ((per + 15) / 16) * 16;
   *chunk = (int)per;
   *splits = (int)((T_max + per - 1) / per);

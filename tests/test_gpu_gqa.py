@@ -74,3 +74,31 @@ def test_llama70b_full_size():
     ref = O.gqa_decode(*args[:6], args[6], w.softmax_scale)
     max_abs, rrms = assert_attn_close(got, ref, bf16_out=True, what="gqa llama70b")
     print(f"gqa full: max_abs(after bf16 slack)={max_abs:.3e} rel_rms={rrms:.3e}")
+
+
+def test_stream_order_with_other_kernels_between_calls():
+    # Programmatic dependent launches: each call must see the query and lengths that
+    # ordinary device copies wrote just before it; the clone after it must see its output.
+    F = fa3()
+    w = W.gqa_llama70b(B=3, T=640)
+    inp, args = _case(w, lens=[640, 300, 17])
+    q8, k8, v8, qs, ks, vs, _ = args
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    variants = [(q8, np.array([640, 300, 17], np.int32)),
+                (np.ascontiguousarray(-q8), np.array([5, 640, 211], np.int32)),
+                (np.ascontiguousarray(q8[:, ::-1]), np.array([129, 1, 640], np.int32))]
+    dq = torch.empty(q8.shape, dtype=torch.int8, device="cuda")
+    dl = torch.empty(w.B, dtype=torch.int32, device="cuda")
+    srcs = [(t(q), t(ls)) for q, ls in variants]
+    dk, dv, dqs, dks, dvs = t(k8), t(v8), t(qs), t(ks), t(vs)
+    keep = []
+    torch.cuda.synchronize()
+    for sq, sl in srcs:
+        dq.copy_(sq)
+        dl.copy_(sl)
+        out = F.decode_attn_gqa(dq, dk, dv, dqs, dks, dvs, dl, w.softmax_scale)
+        keep.append(out.clone())
+    torch.cuda.synchronize()
+    for (q, ls), got in zip(variants, keep):
+        ref = O.gqa_decode(q, k8, v8, qs, ks, vs, ls, w.softmax_scale)
+        assert_attn_close(got.float().cpu().numpy(), ref, bf16_out=True, what=f"gqa ordered {ls.tolist()}")
