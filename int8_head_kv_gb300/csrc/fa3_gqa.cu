@@ -36,9 +36,12 @@ constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kHeadsPerTile = 8;
 #ifndef FA3_GQA_STAGES
-#define FA3_GQA_STAGES 4
+#define FA3_GQA_STAGES 2
 #endif
-constexpr int kStages = FA3_GQA_STAGES;         // cp.async ring depth per warp
+// cp.async ring depth per warp: with the one-wave split plan (long chunks), two
+// stages and more resident CTAs beat deeper rings (measured 29.8 / 30.3 / 31.2 /
+// 32.7 us for 2 / 3 / 4 / 5 stages on the Llama-70B shape).
+constexpr int kStages = FA3_GQA_STAGES;
 constexpr int kStageBytes = 2 * 16 * kD;        // one 16-token step: K then V rows (4 KB)
 constexpr int kSmemBytes = kWarps * kStages * kStageBytes;
 
