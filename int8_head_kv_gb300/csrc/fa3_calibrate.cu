@@ -400,14 +400,30 @@ tail_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
   }
 }
 
+// A window: its exact width hi - lo as the unevaluated fp32 sum ws + we (the
+// rounded difference and its rounding error, Knuth's TwoSum: exact for the finite
+// fp32 differences of two bf16 values), and its keys.  fp32 throughout: this
+// GPU's fp64 rate is a small fraction of its fp32 rate.
 struct Cand {
-  double width;
+  float ws, we;
   uint32_t lo_key;
   uint32_t hi_key;
 };
 
+__device__ __forceinline__ Cand make_cand(uint32_t lo_key, uint32_t hi_key) {
+  const float b = key_value(hi_key), y = -key_value(lo_key);
+  const float s = __fadd_rn(b, y);
+  const float bp = __fsub_rn(s, b);
+  const float ap = __fsub_rn(s, bp);
+  const float e = __fadd_rn(__fsub_rn(b, ap), __fsub_rn(y, bp));
+  return Cand{s, e, lo_key, hi_key};
+}
+
+// Orders windows by exact width, then by start key: rounding is monotonic, so a
+// smaller rounded difference means a smaller exact one, and equal rounded
+// differences are ordered by their errors.
 __device__ __forceinline__ bool cand_less(const Cand& a, const Cand& b) {
-  return a.width < b.width || (a.width == b.width && a.lo_key < b.lo_key);
+  return a.ws < b.ws || (a.ws == b.ws && (a.we < b.we || (a.we == b.we && a.lo_key < b.lo_key)));
 }
 
 __device__ __forceinline__ bool tot_less(float a, float b) {
@@ -541,7 +557,7 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
     tails[h].flag = 0u;
   }
 
-  Cand best{__longlong_as_double(0x7ff0000000000000LL), 0xffffffffu, 0xffffffffu};
+  Cand best{__int_as_float(0x7f800000), 0.f, 0xffffffffu, 0xffffffffu};
   unsigned long long P = base;
   if (!search) {
     // thin tails: the full pass decides this head
@@ -588,9 +604,7 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
     for (uint32_t i = tid; i < span; i += kWinThreads) {
       const uint32_t v = start_tab[i];
       if (v != 0xffffffffu) {
-        const uint32_t end_bin = end_tab[i];
-        const double w = (double)key_value(end_bin) - (double)key_value(v);
-        const Cand cd{w, v, end_bin};
+        const Cand cd = make_cand(v, end_tab[i]);
         if (cand_less(cd, best)) best = cd;
       }
     }
@@ -611,9 +625,7 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
           pos += ch[lo_s * kBinsPerThread + j];
           if (e < pos) { end_bin = lo_s * kBinsPerThread + j; break; }
         }
-        const uint32_t start_bin = tid * kBinsPerThread + i;
-        const double w = (double)key_value(end_bin) - (double)key_value(start_bin);
-        const Cand cand{w, start_bin, end_bin};
+        const Cand cand = make_cand(tid * kBinsPerThread + i, end_bin);
         if (cand_less(cand, best)) best = cand;
       }
       P += cnt;
@@ -624,7 +636,8 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     Cand other;
-    other.width = __shfl_xor_sync(0xffffffffu, best.width, o);
+    other.ws = __shfl_xor_sync(0xffffffffu, best.ws, o);
+    other.we = __shfl_xor_sync(0xffffffffu, best.we, o);
     other.lo_key = __shfl_xor_sync(0xffffffffu, best.lo_key, o);
     other.hi_key = __shfl_xor_sync(0xffffffffu, best.hi_key, o);
     if (cand_less(other, best)) best = other;
@@ -636,7 +649,8 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       Cand other;
-      other.width = __shfl_xor_sync(0xffffffffu, best.width, o);
+      other.ws = __shfl_xor_sync(0xffffffffu, best.ws, o);
+      other.we = __shfl_xor_sync(0xffffffffu, best.we, o);
       other.lo_key = __shfl_xor_sync(0xffffffffu, best.lo_key, o);
       other.hi_key = __shfl_xor_sync(0xffffffffu, best.hi_key, o);
       if (cand_less(other, best)) best = other;
