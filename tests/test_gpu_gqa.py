@@ -102,3 +102,15 @@ def test_stream_order_with_other_kernels_between_calls():
     for (q, ls), got in zip(variants, keep):
         ref = O.gqa_decode(q, k8, v8, qs, ks, vs, ls, w.softmax_scale)
         assert_attn_close(got.float().cpu().numpy(), ref, bf16_out=True, what=f"gqa ordered {ls.tolist()}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 1), (40, 5)])
+def test_group_sizes(Hq, Hkv):
+    # G = 1 (one query head per KV head), G = 8 with a single KV head, G = 8 over 5 KV heads
+    F = fa3()
+    w = W.gqa_llama70b(B=2, T=300)
+    w.Hq, w.Hkv = Hq, Hkv
+    inp, args = _case(w, lens=[300, 65])
+    got = _run(F, w, args)
+    ref = O.gqa_decode(*args[:6], args[6], w.softmax_scale)
+    assert_attn_close(got, ref, bf16_out=True, what=f"gqa Hq={Hq} Hkv={Hkv}")

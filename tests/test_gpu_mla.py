@@ -171,3 +171,13 @@ def test_stream_order_with_other_kernels_between_calls():
     for (q, ls), got in zip(variants, keep):
         inp.q = q
         assert_attn_close(got.cpu().numpy(), _oracle(w, inp, q_scale, kv_scale, ckv8, ls), what=f"ordered {ls}")
+
+
+@pytest.mark.parametrize("H", [1, 37, 100])
+def test_head_counts_not_a_multiple_of_the_lane_quarter(H):
+    # heads >= H are padding rows of the 128-lane tiles: zero query codes, never written out
+    F = fa3()
+    w = W.MLAWorkload(name=f"h{H} dl512 dr64", B=2, H=H, Dl=512, Dr=64, T_max=333, softmax_scale=0.07,
+                      lens=[333, 70], calib_q_shape=(2, H, 4, 512), calib_kv_shape=(1, 1, 256, 512))
+    args = _prepare(w)
+    assert_attn_close(_run(F, w, *args), _oracle(w, *args), what=f"mla H={H}")
