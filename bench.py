@@ -472,11 +472,15 @@ def run_kernel(args):
         fn = lambda: F.calibrate_perhead(x, 0.9999, mn, mx)
         unit = ("GB/s", x.numel() * 2)
     else:
-        kv = torch.randn(32, 64, 1, 512, device=dev, generator=g).to(torch.bfloat16)
-        cache = torch.zeros(32, 1024, 1, 512, dtype=torch.int8, device=dev)
+        kv = torch.randn(32, args.t_new, 1, 512, device=dev, generator=g).to(torch.bfloat16)
+        cache = torch.zeros(32, max(1024, args.t_new), 1, 512, dtype=torch.int8, device=dev)
         pos = torch.zeros(32, dtype=torch.int32, device=dev)
-        sc = torch.full((1,), 0.02, device=dev)
+        # the scale the Recall-Window calibration gives for these values
+        mn, mx = torch.full((1,), float("inf"), device=dev), torch.full((1,), float("-inf"), device=dev)
+        F.calibrate_perhead(kv.transpose(1, 2).contiguous(), 0.9999, mn, mx)
+        sc = F.qparams(mn, mx)
         fn = lambda: F.quantize_append(kv, sc, cache, pos)
+        k = f"append t_new={args.t_new}"
         unit = ("GB/s", kv.numel() * 3)
     for _ in range(args.warmup):
         fn()
@@ -501,6 +505,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--kernel", choices=["mla", "gqa", "calib", "append"],
                     help="run one kernel alone (for profiling) instead of the benchmark step")
+    ap.add_argument("--t-new", type=int, default=64, help="new tokens per sequence for --kernel append")
     args = ap.parse_args()
     if args.kernel:
         run_kernel(args)

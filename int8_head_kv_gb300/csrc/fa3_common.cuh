@@ -61,6 +61,105 @@ __device__ __forceinline__ int quant_code_fast(float x, float s, float rs) {
   return quant_code(x, s);
 }
 
+// ---------------------------------------------------------------------------
+// Codes of eight bf16 values at once (one 16-byte group), bit-identical to
+// quant_code(x, s) for every input.
+//
+// Fast path, two values per packed f32x2 instruction: t = fma(x, rs, 1.5*2^23)
+// rounds x*rs half-to-even into the low mantissa bits of t (exact for |x*rs| <
+// 2^22), so the integer clamp of t's bit pattern to [magic-127, magic+127]
+// leaves the clamped code in its low byte, and also handles |x*rs| >= 2^22 and
+// +-inf (the bit patterns fall outside the range on the correct side).  The code
+// is the quotient's whenever d = x*rs - RNE(x*rs) stays within kTieBand of 1/2:
+// rcp.approx is within 2^-23.28 relative on sm_103a (measured over every
+// mantissa), so x*rs is within 2.5e-4 of x/s for |x/s| <= 128 even at 2^-19,
+// and |x/s - RNE(x*rs)| < 1/2 by a margin the float32 rounding of the quotient
+// cannot cross.
+//
+// Rare path, per lane, for values within the band of a half-integer h (or NaN,
+// or any value when s is not a normal scale in [2^-100, 2^100]): the decision
+// is taken exactly from the sign of a - |h|*s (a = |x|), which one fma computes
+// without rounding because a and |h|*s agree to within 2^-10 * s and both are
+// multiples of ulp(s)/2.  fl(a/s) rounds to |h| exactly when a/s lies within
+// half an ulp of |h| (the ulp below |h| is half as wide at |h| = 1/2), and |h|
+// itself, having at most 8 significant bits, is an even float32.
+// ---------------------------------------------------------------------------
+constexpr float kTieBand = 2.5e-4f;
+
+__device__ __forceinline__ bool exact_scale(float s) {
+  return s >= 7.888609052210118e-31f && s <= 1.2676506002282294e30f;   // [2^-100, 2^100]
+}
+
+// clamp(RNE(fl(x / s))) for x / s within 5e-4 of a half-integer of magnitude <= 127.5,
+// s an exact_scale and x finite.
+__device__ __forceinline__ int tie_code(float x, float s, float rs) {
+  const float a = fabsf(x);
+  const float h = floorf(a * rs) + 0.5f;
+  const float t = fmaf(-h, s, a);                                                     // a - h*s, exact
+  const float ulp = __uint_as_float((__float_as_uint(h) & 0x7f800000u) - (23u << 23));
+  const float up = ulp * 0.5f * s;
+  const float dn = h == 0.5f ? 0.5f * up : up;
+  float c = t > up ? h + 0.5f : (t < -dn ? h - 0.5f : rintf(h));
+  c = fminf(c, 127.0f);
+  const int ci = (int)c;
+  return x < 0.0f ? -ci : ci;
+}
+
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f32x2_fma(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f32x2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// v: eight bf16 values (element e in bits 16*(e%2) of word e/2); returns the eight
+// codes as bytes, element e in byte e.  rs = rcp_approx(s), exact = exact_scale(s).
+__device__ __forceinline__ uint2 quant_group8(uint4 v, float s, float rs, bool exact) {
+  constexpr float kMagic = 12582912.0f;                     // 1.5 * 2^23
+  constexpr int kLo = 0x4B400000 - 127, kHi = 0x4B400000 + 127;
+  const unsigned long long m2 = f32x2_pack(kMagic, kMagic), rs2 = f32x2_pack(rs, rs);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  int q[8];
+  bool rare = !exact;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const unsigned long long x2 = f32x2_pack(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+    const unsigned long long t2 = f32x2_fma(x2, rs2, m2);              // magic + RNE(x * rs)
+    const unsigned long long d2 = f32x2_fma(x2, rs2, f32x2_sub(m2, t2));  // x * rs - RNE(x * rs)
+    float t0, t1, d0, d1;
+    f32x2_unpack(t2, t0, t1);
+    f32x2_unpack(d2, d0, d1);
+    rare = rare || !(fabsf(d0) <= 0.5f - kTieBand) || !(fabsf(d1) <= 0.5f - kTieBand);
+    q[2 * k] = min(max((int)__float_as_uint(t0), kLo), kHi);
+    q[2 * k + 1] = min(max((int)__float_as_uint(t1), kLo), kHi);
+  }
+  if (rare) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float x = (e & 1) ? __uint_as_float(w[e >> 1] & 0xffff0000u) : __uint_as_float(w[e >> 1] << 16);
+      const float t = fmaf(x, rs, kMagic), r = t - kMagic, d = fmaf(x, rs, -r);
+      if (!exact || (!(fabsf(d) <= 0.5f - kTieBand) && !(fabsf(r) >= 128.0f)))
+        q[e] = (exact && fabsf(r) <= 127.0f) ? tie_code(x, s, rs) : quant_code(x, s);
+    }
+  }
+  const uint32_t lo = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
+  return make_uint2(lo, hi);
+}
+
 // Programmatic dependent launch.  Every kernel of the library is launched as a
 // programmatic dependent of the work before it on the stream (launch_pdl): it
 // calls pdl_wait() before its first access to memory another kernel may write,

@@ -42,62 +42,89 @@ __global__ void qparams_kernel(const float* __restrict__ mn, const float* __rest
   if (h < H) scale[h] = __fdiv_rn(fmaxf(fabsf(mn[h]), fabsf(mx[h])), 127.0f);
 }
 
-// Vector path: each thread converts 8 consecutive values of one row (16 B in, 8 B out).
-// Rows are (b, t, h) triples; groups of 8 values never straddle a row because D % 8 == 0.
+// Division of 32-bit unsigned integers by a divisor fixed for the launch, as a
+// multiply-high and two shifts (Granlund and Montgomery, "Division by Invariant
+// Integers using Multiplication", 1994, the unsigned N-bit method with l =
+// ceil(log2 d)): exact for every 32-bit dividend.
+struct DivU32 {
+  uint32_t m, s1, s2;
+};
+inline DivU32 make_divu32(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  DivU32 f;
+  f.m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 0 ? l - 1 : 0;
+  return f;
+}
+__device__ __forceinline__ uint32_t divu32(uint32_t n, DivU32 f) {
+  const uint32_t t1 = __umulhi(f.m, n);
+  return (t1 + ((n - t1) >> f.s1)) >> f.s2;
+}
+
+// Vector path.  The T_new new rows of sequence b are contiguous in the source and,
+// from cache row pos[b] on, contiguous in the cache as well, so the append of one
+// sequence is a stream conversion: 16-byte source group i (8 bf16 values of head
+// (i / (D/8)) mod H) becomes 8-byte cache group i, and the RoPE rows are a 16-byte
+// copy.  blockIdx.y walks the sequences, so pos[b] is one uniform load per block.
+// With G = 2 a thread converts two neighbouring groups and stores them as one
+// 16-byte word (the host picks G = 2 when every such word is 16-byte aligned).
+template <int G>
 __global__ void __launch_bounds__(256) quantize_append_vec_kernel(
     const uint4* __restrict__ kv, const float* __restrict__ scale, int8_t* __restrict__ cache,
     const int32_t* __restrict__ pos, int B, int T_new, int H, int D, int T_max,
-    const uint4* __restrict__ rope_src, uint16_t* __restrict__ rope_cache, int Dr, int32_t* err) {
+    const uint4* __restrict__ rope_src, uint16_t* __restrict__ rope_cache, int Dr, int32_t* err,
+    DivU32 div_g, DivU32 div_h) {
   pdl_wait();
   pdl_launch_dependents();
-  const int64_t groups_per_row = D / 8;
-  const int64_t n_groups = (int64_t)B * T_new * H * groups_per_row;
-  const int64_t rope_groups_per_row = Dr / 8;
-  const int64_t n_rope = rope_cache ? (int64_t)B * T_new * rope_groups_per_row : 0;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t gi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gi < n_groups + n_rope; gi += stride) {
-    if (gi < n_groups) {
-      int64_t row = gi / groups_per_row;            // (b * T_new + t) * H + h
-      int g = (int)(gi - row * groups_per_row);
-      int h = (int)(row % H);
-      int64_t bt = row / H;
-      int t = (int)(bt % T_new);
-      int b = (int)(bt / T_new);
-      int p = pos[b];
-      if (p < 0 || p > T_max - T_new) {
-        if (t == 0 && h == 0 && g == 0) set_dev_err(err, FA3_DEVERR_POS);
-        continue;
-      }
-      uint4 v = kv[gi];
-      const float s = scale[h];
-      const float rs = rcp_approx(s);
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t packed[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t word = w[2 * i + j];
-          const int c0 = quant_code_fast(bf16_to_float(word & 0xffffu), s, rs);
-          const int c1 = quant_code_fast(bf16_to_float(word >> 16), s, rs);
-          acc |= ((uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8)) << (16 * j);
-        }
-        packed[i] = acc;
-      }
-      int64_t dst = ((((int64_t)b * T_max + p + t) * H + h) * D) + (int64_t)g * 8;
-      *reinterpret_cast<uint2*>(cache + dst) = make_uint2(packed[0], packed[1]);
-    } else {
-      int64_t ri = gi - n_groups;
-      int64_t row = ri / rope_groups_per_row;         // b * T_new + t
-      int g = (int)(ri - row * rope_groups_per_row);
-      int t = (int)(row % T_new);
-      int b = (int)(row / T_new);
-      int p = pos[b];
-      if (p < 0 || p > T_max - T_new) continue;
-      int64_t dst = (((int64_t)b * T_max + p + t) * Dr) + (int64_t)g * 8;
-      *reinterpret_cast<uint4*>(rope_cache + dst) = rope_src[ri];
+  const uint32_t gpr = (uint32_t)(D / 8);
+  const uint32_t nl = (uint32_t)T_new * (uint32_t)H * gpr;                // latent groups per sequence
+  const uint32_t nr = rope_cache ? (uint32_t)T_new * (uint32_t)(Dr / 8) : 0u;
+  const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x, nthreads = gridDim.x * blockDim.x;
+  const float s_one = scale[0];                                             // the only scale when H == 1
+  const float rs_one = rcp_approx(s_one);
+  const bool ex_one = exact_scale(s_one);
+  for (int b = blockIdx.y; b < B; b += gridDim.y) {
+    const int p = pos[b];
+    if (p < 0 || p > T_max - T_new) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) set_dev_err(err, FA3_DEVERR_POS);
+      continue;
     }
+    const int64_t row0 = (int64_t)b * T_max + p;                         // first cache row written
+    const uint4* src = kv + (uint64_t)b * nl;
+    uint2* dst = reinterpret_cast<uint2*>(cache + row0 * H * D);
+    for (uint32_t i = tid * G; i < nl; i += nthreads * G) {
+      uint4 v[G];
+#pragma unroll
+      for (int u = 0; u < G; ++u)
+        if (u == 0 || i + u < nl) v[u] = src[i + u];
+      float s = s_one, rs = rs_one, s1 = s_one, rs1 = rs_one;
+      bool ex = ex_one, ex1 = ex_one;
+      if (H > 1) {
+        const uint32_t r = divu32(i, div_g);                                // (token, head) row of group i
+        const uint32_t h = r - divu32(r, div_h) * (uint32_t)H;
+        s = scale[h];
+        rs = rcp_approx(s);
+        ex = exact_scale(s);
+        s1 = s, rs1 = rs, ex1 = ex;
+        if (G == 2 && i - r * gpr + 1 == gpr) {                             // group i + 1 starts the next head
+          s1 = scale[h + 1 == (uint32_t)H ? 0 : h + 1];
+          rs1 = rcp_approx(s1);
+          ex1 = exact_scale(s1);
+        }
+      }
+      const uint2 c0 = quant_group8(v[0], s, rs, ex);
+      if (G == 2 && i + 1 < nl) {
+        const uint2 c1 = quant_group8(v[G - 1], s1, rs1, ex1);
+        *reinterpret_cast<uint4*>(dst + i) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+      } else {
+        dst[i] = c0;
+      }
+    }
+    const uint4* rsrc = rope_src + (uint64_t)b * nr;
+    uint4* rdst = reinterpret_cast<uint4*>(rope_cache + row0 * Dr);
+    for (uint32_t i = tid; i < nr; i += nthreads) rdst[i] = rsrc[i];
   }
 }
 
@@ -185,19 +212,38 @@ FA3_API int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* 
   int st = check_device(&sms);
   if (st != FA3_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t per_seq_groups = (int64_t)T_new * ((int64_t)H * (D / 8) + Dr / 8);
   const bool vec = (D % 8 == 0) && aligned16(kv) && (((uintptr_t)cache & 7u) == 0) &&
-                   (!rope_cache || ((Dr % 8 == 0) && aligned16(rope_src) && aligned16(rope_cache)));
-  const int64_t work = (int64_t)B * T_new * (H * (int64_t)D + Dr) / (vec ? 8 : 1);
-  int64_t blocks = (work + 255) / 256;
-  const int64_t cap = (int64_t)sms * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
+                   (!rope_cache || ((Dr % 8 == 0) && aligned16(rope_src) && aligned16(rope_cache))) &&
+                   per_seq_groups < ((int64_t)1 << 31);
+  const bool pairs = vec && aligned16(cache) && ((int64_t)H * D) % 16 == 0;   // 16-byte stores of two groups
+  // Grid-stride loops; blocks for a few waves of the SMs.
+  static int resident[3] = {0, 0, 0};                  // scalar, vector, vector with pairs
+  const int kind = vec ? (pairs ? 2 : 1) : 0;
+  if (resident[kind] == 0) {
+    int r = 0;
+    const cudaError_t oe =
+        kind == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, quantize_append_vec_kernel<2>, 256, 0)
+        : kind == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, quantize_append_vec_kernel<1>, 256, 0)
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, quantize_append_scalar_kernel, 256, 0);
+    if (oe != cudaSuccess) return cuda_status(oe);
+    resident[kind] = r > 0 ? r : 1;
+  }
+  const int64_t cap = (int64_t)sms * resident[kind];
   cudaError_t e;
   if (vec) {
-    e = launch_pdl(quantize_append_vec_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+    const int G = pairs ? 2 : 1;
+    const int64_t gy = std::min<int64_t>(B, 65535);
+    const int64_t items = std::max<int64_t>((int64_t)T_new * H * (D / 8) / G, (int64_t)T_new * (Dr / 8));
+    const int64_t gx = std::max<int64_t>(1, std::min<int64_t>((items + 255) / 256, 4 * ((cap + gy - 1) / gy)));
+    const DivU32 dg = make_divu32((uint32_t)(D / 8)), dh = make_divu32((uint32_t)H);
+    auto* kernel = pairs ? quantize_append_vec_kernel<2> : quantize_append_vec_kernel<1>;
+    e = launch_pdl(kernel, dim3((unsigned)gx, (unsigned)gy), dim3(256), 0, s,
                    reinterpret_cast<const uint4*>(kv), scale, cache, pos, B, T_new, H, D, T_max,
-                   reinterpret_cast<const uint4*>(rope_src), rope_cache, Dr, dev_err);
+                   reinterpret_cast<const uint4*>(rope_src), rope_cache, Dr, dev_err, dg, dh);
   } else {
+    const int64_t work = (int64_t)B * T_new * (H * (int64_t)D + Dr);
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, cap));
     e = launch_pdl(quantize_append_scalar_kernel, dim3((unsigned)blocks), dim3(256), 0, s, kv, scale, cache, pos, B,
                    T_new, H, D, T_max, rope_src, rope_cache, Dr, dev_err);
   }

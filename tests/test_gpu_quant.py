@@ -62,15 +62,73 @@ def test_append_large_with_rope_bit_exact():
 def test_append_gqa_heads_and_scalar_path():
     F = fa3()
     rng = np.random.default_rng(4)
-    for D in (128, 20):                          # 20: rows not 16-byte multiples -> scalar kernel
-        kv = W.bf16_round((rng.standard_t(4, (3, 5, 8, D)) * rng.uniform(0.1, 4, (1, 1, 8, 1))).astype(np.float32))
+    # D = 128: two groups per thread within a head; D = 24: pairs of groups that
+    # straddle two heads (three groups per row); (H, D) = (3, 24): rows of 72 bytes,
+    # one group per thread; D = 20: rows not 16-byte multiples -> scalar kernel.
+    for H, D in ((8, 128), (8, 24), (3, 24), (8, 20)):
+        kv = W.bf16_round((rng.standard_t(4, (3, 5, H, D)) * rng.uniform(0.1, 4, (1, 1, H, 1))).astype(np.float32))
         sc = (np.abs(kv).max(axis=(0, 1, 3)) / 127 * 0.8).astype(np.float32)   # forces clamping
         sc[2] = 0.0                              # a zero scale quantizes to 0
-        cache0 = np.zeros((3, 9, 8, D), np.int8)
+        cache0 = np.zeros((3, 9, H, D), np.int8)
         pos = np.array([0, 4, 2], np.int32)
         cache = torch.from_numpy(cache0).cuda()
         F.quantize_append(bf16_dev(kv), torch.from_numpy(sc).cuda(), cache, torch.from_numpy(pos).cuda())
-        assert np.array_equal(cache.cpu().numpy(), O.quantize_append(kv, sc, cache0, pos)), D
+        assert np.array_equal(cache.cpu().numpy(), O.quantize_append(kv, sc, cache0, pos)), (H, D)
+
+
+def test_append_grid_stride_passes_and_sequence_loop():
+    # 16 sequences of 512 new rows x 2 heads x 512 plus a 64-wide RoPE row: more
+    # 16-byte groups per sequence than one wave of blocks covers, so threads take
+    # several passes and passes mix latent and RoPE groups.
+    F = fa3()
+    rng = np.random.default_rng(6)
+    B, T_new, H, D, Dr, T_max = 16, 512, 2, 512, 64, 640
+    kv = W.bf16_round((rng.standard_normal((B, T_new, H, D)) * np.array([0.5, 3.0])[None, None, :, None]).astype(np.float32))
+    sc = (np.abs(kv).max(axis=(0, 1, 3)) / 127).astype(np.float32)
+    rope = W.bf16_round(rng.standard_normal((B, T_new, Dr)).astype(np.float32))
+    pos = rng.integers(0, T_max - T_new + 1, B).astype(np.int32)
+    cache0 = rng.integers(-127, 128, (B, T_max, H, D)).astype(np.int8)
+    cache = torch.from_numpy(cache0).cuda()
+    rope_cache = torch.zeros(B, T_max, Dr, dtype=torch.bfloat16, device="cuda")
+    F.quantize_append(bf16_dev(kv), torch.from_numpy(sc).cuda(), cache, torch.from_numpy(pos).cuda(),
+                      bf16_dev(rope), rope_cache)
+    assert np.array_equal(cache.cpu().numpy(), O.quantize_append(kv, sc, cache0, pos))
+    rc = rope_cache.float().cpu().numpy()
+    for b in range(B):
+        assert np.array_equal(rc[b, pos[b]:pos[b] + T_new], rope[b])
+        assert not rc[b, :pos[b]].any() and not rc[b, pos[b] + T_new:].any()
+    # More sequences than one grid dimension holds (65535): the blocks loop over them.
+    B = 70001
+    kv = W.bf16_round(rng.standard_normal((B, 1, 1, 8)).astype(np.float32))
+    pos = rng.integers(0, 2, B).astype(np.int32)
+    cache0 = np.zeros((B, 2, 1, 8), np.int8)
+    cache = torch.from_numpy(cache0).cuda()
+    F.quantize_append(bf16_dev(kv), torch.tensor([0.02], device="cuda"), cache, torch.from_numpy(pos).cuda())
+    assert np.array_equal(cache.cpu().numpy(), O.quantize_append(kv, np.array([0.02], np.float32), cache0, pos))
+
+
+def test_append_every_bf16_value():
+    # Every finite bf16 bit pattern (and +-inf) against scales that take each branch of
+    # the group conversion: power-of-two and decimal scales (many exact and near ties),
+    # a calibrated-looking one, the smallest and largest scales decided without a
+    # division, scales outside that range, a subnormal, zero and a negative scale.
+    F = fa3()
+    bits = np.arange(65536, dtype=np.uint32)
+    finite = (bits & 0x7F80) != 0x7F80
+    inf = (bits & 0x7FFF) == 0x7F80
+    x = ((bits[finite | inf] << 16).astype(np.uint32)).view(np.float32)
+    x = np.concatenate([x, np.zeros((-len(x)) % 16, np.float32)])
+    scales = np.array([0.02, 0.1, 1.0 / 127.0, 4.5 / 127.0, 0.25, 1.0 / 3.0, 7.7, 3.7e-3, 2.0 ** -100,
+                       2.0 ** 100, 2.0 ** -101, 1.5e30, 1e-39, 0.0, -0.5], np.float32)
+    H = len(scales)
+    kv = np.broadcast_to(x, (1, 1, H, len(x))).copy()
+    cache = torch.zeros(1, 1, H, len(x), dtype=torch.int8, device="cuda")
+    F.quantize_append(bf16_dev(kv), torch.from_numpy(scales).cuda(), cache, torch.zeros(1, dtype=torch.int32, device="cuda"))
+    got = cache.cpu().numpy()[0, 0]
+    for h, s in enumerate(scales):
+        want = O.quantize(x, s)
+        bad = np.flatnonzero(got[h] != want)
+        assert bad.size == 0, (float(s), x[bad[:5]], got[h][bad[:5]], want[bad[:5]])
 
 
 def test_append_bad_position_sets_error_and_skips():
