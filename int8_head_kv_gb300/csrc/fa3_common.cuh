@@ -36,29 +36,11 @@ __device__ __forceinline__ int quant_code(float x, float s) {
 }
 
 // Approximate reciprocal (hardware rcp, flush-to-zero); only used to pick codes
-// where the decision cannot differ from the IEEE quotient's (see quant_code_fast).
+// where the decision cannot differ from the IEEE quotient's (see quant_group8_biased).
 __device__ __forceinline__ float rcp_approx(float s) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
   return r;
-}
-
-// Same code as quant_code(x, s), without a division in the common case.  With
-// rs = rcp_approx(s), y = x * rs is within 2.2e-4 of the correctly rounded
-// quotient whenever |x / s| < 200 (rcp error <= 2^-20, two roundings), so when y
-// is farther than 1e-3 from every half-integer its round-half-even is the
-// quotient's; beyond 127.01 both clamp to +-127.  Everything else (ties,
-// overflow, subnormal scales) takes the IEEE division.
-__device__ __forceinline__ int quant_code_fast(float x, float s, float rs) {
-  if (s == 0.0f) return 0;
-  const float y = x * rs;
-  const float a = fabsf(y);
-  if (a < 127.0f) {
-    if (fabsf(a - floorf(a) - 0.5f) >= 1e-3f) return __float2int_rn(y);
-  } else if (a >= 127.01f && a <= 3.0e38f) {
-    return y > 0.0f ? 127 : -127;
-  }
-  return quant_code(x, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -125,19 +107,22 @@ __device__ __forceinline__ unsigned long long f32x2_sub(unsigned long long a, un
   return r;
 }
 
-// v: eight bf16 values (element e in bits 16*(e%2) of word e/2); returns the eight
-// codes as bytes, element e in byte e.  rs = rcp_approx(s), exact = exact_scale(s).
-__device__ __forceinline__ uint2 quant_group8(uint4 v, float s, float rs, bool exact) {
-  constexpr float kMagic = 12582912.0f;                     // 1.5 * 2^23
-  constexpr int kLo = 0x4B400000 - 127, kHi = 0x4B400000 + 127;
-  const unsigned long long m2 = f32x2_pack(kMagic, kMagic), rs2 = f32x2_pack(rs, rs);
+constexpr float kCodeMagic = 12582912.0f;                  // 1.5 * 2^23
+constexpr int kCodeMagicBits = 0x4B400000;                 // its bit pattern
+
+// v: eight bf16 values (element e in bits 16*(e%2) of word e/2).  q[e] receives the
+// bit pattern of the float 1.5*2^23 + code(e): its low byte is the code's, and
+// __int_as_float(q[e]) - 1.5*2^23 is the code as an exact float.  rs =
+// rcp_approx(s), exact = exact_scale(s).
+__device__ __forceinline__ void quant_group8_biased(uint4 v, float s, float rs, bool exact, int (&q)[8]) {
+  constexpr int kLo = kCodeMagicBits - 127, kHi = kCodeMagicBits + 127;
+  const unsigned long long m2 = f32x2_pack(kCodeMagic, kCodeMagic), rs2 = f32x2_pack(rs, rs);
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  int q[8];
   bool rare = !exact;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const unsigned long long x2 = f32x2_pack(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
-    const unsigned long long t2 = f32x2_fma(x2, rs2, m2);              // magic + RNE(x * rs)
+    const unsigned long long t2 = f32x2_fma(x2, rs2, m2);                 // magic + RNE(x * rs)
     const unsigned long long d2 = f32x2_fma(x2, rs2, f32x2_sub(m2, t2));  // x * rs - RNE(x * rs)
     float t0, t1, d0, d1;
     f32x2_unpack(t2, t0, t1);
@@ -150,11 +135,17 @@ __device__ __forceinline__ uint2 quant_group8(uint4 v, float s, float rs, bool e
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float x = (e & 1) ? __uint_as_float(w[e >> 1] & 0xffff0000u) : __uint_as_float(w[e >> 1] << 16);
-      const float t = fmaf(x, rs, kMagic), r = t - kMagic, d = fmaf(x, rs, -r);
+      const float t = fmaf(x, rs, kCodeMagic), r = t - kCodeMagic, d = fmaf(x, rs, -r);
       if (!exact || (!(fabsf(d) <= 0.5f - kTieBand) && !(fabsf(r) >= 128.0f)))
-        q[e] = (exact && fabsf(r) <= 127.0f) ? tie_code(x, s, rs) : quant_code(x, s);
+        q[e] = kCodeMagicBits + ((exact && fabsf(r) <= 127.0f) ? tie_code(x, s, rs) : quant_code(x, s));
     }
   }
+}
+
+// The eight codes as bytes, element e in byte e.
+__device__ __forceinline__ uint2 quant_group8(uint4 v, float s, float rs, bool exact) {
+  int q[8];
+  quant_group8_biased(v, s, rs, exact, q);
   const uint32_t lo = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
   const uint32_t hi = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
   return make_uint2(lo, hi);

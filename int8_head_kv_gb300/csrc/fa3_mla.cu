@@ -960,13 +960,12 @@ __global__ void __launch_bounds__(256, 6) mla_prepare_q_kernel(const MlaParams p
         orow[0] = make_float4(0.f, 0.f, 0.f, 0.f);
         orow[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      const float rqs = rcp_approx(qs);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      int q8[8];
+      quant_group8_biased(v, qs, rcp_approx(qs), exact_scale(qs), q8);
       uint32_t r4[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        r4[e] = pack_f16x2((float)quant_code_fast(bf16_to_float(wv[e] & 0xffffu), qs, rqs),
-                           (float)quant_code_fast(bf16_to_float(wv[e] >> 16), qs, rqs));
+        r4[e] = pack_f16x2(__int_as_float(q8[2 * e]) - kCodeMagic, __int_as_float(q8[2 * e + 1]) - kCodeMagic);
       o = make_uint4(r4[0], r4[1], r4[2], r4[3]);
     }
     const int hc = 1 << (lat_shift - 1);              // chunks per latent half
