@@ -457,6 +457,37 @@ def run_kernel(args):
         ws = torch.empty(F.mla_workspace_size(B, H, DL, T), dtype=torch.uint8, device=dev)
         fn = lambda: F.decode_attn_mla(q, ckv, kr, qs, kvs, lens, SOFTMAX_SCALE, out=out, workspace=ws)
         unit = ("KV GB/s", kv_bytes_per_step())
+    elif k == "mla_paged":
+        # the same workload in a pool of 64-token pages stored in shuffled order
+        ckv = torch.randint(-127, 128, (B, T, DL), dtype=torch.int8, device=dev, generator=g)
+        kr = torch.randn(B, T, DR, device=dev, generator=g).to(torch.bfloat16)
+        q = torch.randn(B, H, DL + DR, device=dev, generator=g).to(torch.bfloat16)
+        qs, kvs = torch.full((H,), 0.03, device=dev), torch.full((1,), 0.02, device=dev)
+        lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+        P, mp = 64, T // 64
+        perm = torch.randperm(B * mp, device=dev, generator=g)
+        ckv_pool = torch.empty(B * mp, P, DL, dtype=torch.int8, device=dev)
+        kr_pool = torch.empty(B * mp, P, DR, dtype=torch.bfloat16, device=dev)
+        ckv_pool[perm] = ckv.reshape(B * mp, P, DL)
+        kr_pool[perm] = kr.reshape(B * mp, P, DR)
+        del ckv, kr
+        bt = perm.reshape(B, mp).to(torch.int32).contiguous()
+        out = torch.empty(B, H, DL, device=dev)
+        ws = torch.empty(F.mla_workspace_size(B, H, DL, T), dtype=torch.uint8, device=dev)
+        fn = lambda: F.decode_attn_mla_paged(q, ckv_pool, kr_pool, qs, kvs, lens, bt, SOFTMAX_SCALE, out=out,
+                                             workspace=ws)
+        unit = ("KV GB/s", kv_bytes_per_step())
+    elif k == "gqa_paged":
+        Bq, Hq, Hkv, D, Tq, P = 16, 64, 8, 128, 4096, 16
+        mp = Tq // P
+        kp = torch.randint(-127, 128, (Bq * mp, P, Hkv, D), dtype=torch.int8, device=dev, generator=g)
+        vp = torch.randint(-127, 128, (Bq * mp, P, Hkv, D), dtype=torch.int8, device=dev, generator=g)
+        q8 = torch.randint(-127, 128, (Bq, Hq, D), dtype=torch.int8, device=dev, generator=g)
+        s1, s2 = torch.full((Hq,), 0.01, device=dev), torch.full((Hkv,), 0.01, device=dev)
+        lens = torch.full((Bq,), Tq, dtype=torch.int32, device=dev)
+        bt = torch.randperm(Bq * mp, device=dev, generator=g).reshape(Bq, mp).to(torch.int32).contiguous()
+        fn = lambda: F.decode_attn_gqa_paged(q8, kp, vp, s1, s2, s2, lens, bt, 1 / math.sqrt(128))
+        unit = ("KV GB/s", Bq * Tq * Hkv * D * 2)
     elif k == "gqa":
         Bq, Hq, Hkv, D, Tq = 16, 64, 8, 128, 4096
         kc = torch.randint(-127, 128, (Bq, Tq, Hkv, D), dtype=torch.int8, device=dev, generator=g)
@@ -503,7 +534,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--kernel", choices=["mla", "gqa", "calib", "append"],
+    ap.add_argument("--kernel", choices=["mla", "mla_paged", "gqa", "gqa_paged", "calib", "append"],
                     help="run one kernel alone (for profiling) instead of the benchmark step")
     ap.add_argument("--t-new", type=int, default=64, help="new tokens per sequence for --kernel append")
     args = ap.parse_args()

@@ -56,6 +56,7 @@ enum fa3_status {
 #define FA3_DEVERR_POS 1      /* append: pos[b] < 0 or pos[b] + T_new > T_max (row skipped)    */
 #define FA3_DEVERR_LENS 2     /* decode: lens[b] < 0 or lens[b] > T_max (output row set to 0) */
 #define FA3_DEVERR_TIMEOUT 4  /* a bounded wait inside a kernel gave up (output not valid)    */
+#define FA3_DEVERR_PAGE 8     /* paged calls: a block-table entry outside [0, num_pages)       */
 
 /* Human-readable name of a status code (static string). */
 const char* fa3_status_string(int status);
@@ -211,6 +212,61 @@ int fa3_decode_attn_gqa_noalloc(const int8_t* q, const int8_t* k, const int8_t* 
                                 const float* q_scale, const float* k_scale, const float* v_scale,
                                 const int32_t* lens, uint16_t* out, int B, int Hq, int Hkv, int D, int T_max,
                                 float softmax_scale, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Paged INT8 KV cache.  The pages leave the KV cache's storage to the serving
+ * runtime (MindIE "FA3 quantization", usage steps: the runtime is told which
+ * format to keep the cache in); these calls take the block-table layout of
+ * paged serving runtimes.  The cache of every sequence is a list of pages of
+ * page_size token rows in one pool shared by all sequences:
+ *   block_table  int32 [B][max_pages], device; entry i of sequence b is the
+ *                pool page that holds that sequence's tokens
+ *                [i * page_size, (i + 1) * page_size).
+ *   num_pages    pages in the pool; the per-sequence capacity is
+ *                T_max = max_pages * page_size.
+ * Token t of sequence b lives in pool row
+ *   block_table[b][t / page_size] * page_size + t % page_size,
+ * so a pool is the contiguous [B][T_max] cache of the calls above with its
+ * rows regrouped; results are exactly those of the contiguous call on the
+ * gathered cache.  Only the entries a call needs are read (pages of tokens
+ * below lens[b], or of the appended positions); such an entry outside
+ * [0, num_pages) sets FA3_DEVERR_PAGE: the append skips that token row, the
+ * decode reads that page as zeros (that sequence's output is not valid).
+ * Pages may be shared between sequences (read-only prefixes).
+ * ------------------------------------------------------------------------ */
+
+/* Quantize-on-append into a paged cache (fa3_quantize_append's arithmetic).
+ * cache      int8 [num_pages][page_size][H][D] pool.
+ * rope_cache optional bf16 [num_pages][page_size][Dr] pool (NULL, NULL, 0 to skip).
+ * Positions as for fa3_quantize_append with T_max = max_pages * page_size.
+ * Supported: any page_size >= 1. */
+int fa3_quantize_append_paged(const uint16_t* kv, const float* scale, int8_t* cache,
+                              const int32_t* block_table, const int32_t* pos,
+                              int B, int T_new, int H, int D, int num_pages, int page_size, int max_pages,
+                              const uint16_t* rope_src, uint16_t* rope_cache, int Dr,
+                              int32_t* dev_err, void* stream);
+
+/* Absorbed-MLA decode over a paged cache (fa3_decode_attn_mla's arithmetic).
+ * ckv    int8 [num_pages][page_size][Dl] pool;  krope  bf16 [num_pages][page_size][Dr] pool.
+ * Supported: as fa3_decode_attn_mla, page_size a multiple of 64 (one 64-token
+ * tile never spans two pages), num_pages * page_size < 2^31.
+ * workspace  fa3_mla_workspace_size(B, H, Dl, max_pages * page_size) bytes. */
+int fa3_decode_attn_mla_paged(const uint16_t* q, const int8_t* ckv, const uint16_t* krope,
+                              const float* q_scale, const float* kv_scale, const int32_t* lens,
+                              const int32_t* block_table, float* out, int B, int H, int Dl, int Dr,
+                              int num_pages, int page_size, int max_pages, float softmax_scale,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/* GQA decode over a paged cache (fa3_decode_attn_gqa's arithmetic).
+ * k, v   int8 [num_pages][page_size][Hkv][D] pools.
+ * Supported: as fa3_decode_attn_gqa, page_size a multiple of 16.
+ * workspace  fa3_gqa_workspace_size(B, Hq, Hkv, D, max_pages * page_size) bytes. */
+int fa3_decode_attn_gqa_paged(const int8_t* q, const int8_t* k, const int8_t* v,
+                              const float* q_scale, const float* k_scale, const float* v_scale,
+                              const int32_t* lens, const int32_t* block_table, uint16_t* out,
+                              int B, int Hq, int Hkv, int D, int num_pages, int page_size, int max_pages,
+                              float softmax_scale, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err, void* stream);
 
 #ifdef __cplusplus
 }

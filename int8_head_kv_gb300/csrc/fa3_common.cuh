@@ -151,6 +151,27 @@ __device__ __forceinline__ uint2 quant_group8(uint4 v, float s, float rs, bool e
   return make_uint2(lo, hi);
 }
 
+// Division of 32-bit unsigned integers by a divisor fixed for the launch, as a
+// multiply-high and two shifts (Granlund and Montgomery, "Division by Invariant
+// Integers using Multiplication", 1994, the unsigned N-bit method with l =
+// ceil(log2 d)): exact for every 32-bit dividend.
+struct DivU32 {
+  uint32_t m, s1, s2;
+};
+inline DivU32 make_divu32(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  DivU32 f;
+  f.m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 0 ? l - 1 : 0;
+  return f;
+}
+__device__ __forceinline__ uint32_t divu32(uint32_t n, DivU32 f) {
+  const uint32_t t1 = __umulhi(f.m, n);
+  return (t1 + ((n - t1) >> f.s1)) >> f.s2;
+}
+
 // Programmatic dependent launch.  Every kernel of the library is launched as a
 // programmatic dependent of the work before it on the stream (launch_pdl): it
 // calls pdl_wait() before its first access to memory another kernel may write,

@@ -47,8 +47,9 @@ constexpr int kSmemBytes = kWarps * kStages * kStageBytes;
 
 struct GqaArgs {
   const int8_t* q;
-  const int8_t* k;
+  const int8_t* k;       // [B][T_max][Hkv][D], or a [pool rows][Hkv][D] page pool
   const int8_t* v;
+  const int32_t* block_table;   // [B][max_pages] pool pages, or nullptr for the contiguous layout
   const float* q_scale;
   const float* k_scale;
   const float* v_scale;
@@ -58,6 +59,8 @@ struct GqaArgs {
   float2* part_ml;  // [B][Hkv][splits][8]
   int32_t* err;
   int B, Hq, Hkv, G, T_max, splits, chunk;
+  int page_size, max_pages, num_pages;
+  DivU32 div_ps;    // / page_size
   float sm_log2;    // softmax_scale * log2(e)
 };
 
@@ -125,6 +128,7 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+template <bool PAGED>
 __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -180,38 +184,57 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
   const int64_t tok_stride = (int64_t)p.Hkv * kD;
-  const int8_t* kbase = p.k + ((int64_t)b * p.T_max) * tok_stride + (int64_t)g * kD;
-  const int8_t* vbase = p.v + ((int64_t)b * p.T_max) * tok_stride + (int64_t)g * kD;
+  const int64_t seq_row0 = PAGED ? 0 : (int64_t)b * p.T_max;             // cache row of the sequence's token 0
+  const int8_t* kbase = p.k + seq_row0 * tok_stride + (int64_t)g * kD;
+  const int8_t* vbase = p.v + seq_row0 * tok_stride + (int64_t)g * kD;
 
   const uint32_t ring = (uint32_t)__cvta_generic_to_shared(gsm) + (uint32_t)(warp * kStages * kStageBytes);
   auto swz = [](int row) { return (row & 6) ^ ((row & 1) << 2); };
   // Step it of the CTA's range (16 tokens) -> ring stage: 256 chunks of 16 bytes,
   // 8 per lane; rows past the range are zero-filled (their scores are masked).
-  auto issue = [&](int it, int stage) {
-    const int t0 = t_begin + 16 * it;
+  // Paged: chunks start at multiples of 16 tokens and pages hold multiples of 16, so
+  // a step's 16 rows lie in one page; a block-table entry outside the pool reads zeros.
+  // The entry of a step is loaded one issue ahead (entry_of) and used at the next
+  // issue (row_of), so that the load's latency is not spent waiting.
+  auto entry_of = [&](int t0) -> int {
+    return p.block_table[(int64_t)b * p.max_pages + divu32((uint32_t)t0, p.div_ps)];
+  };
+  auto row_of = [&](int pg, int t0) -> int64_t {     // pool row of token t0 (-1: entry outside the pool)
+    const int off = t0 - (int)divu32((uint32_t)t0, p.div_ps) * p.page_size;
+    return (pg >= 0 && pg < p.num_pages) ? (int64_t)pg * p.page_size + off : -1;
+  };
+  const int span = t_end - t_begin;
+  const int n_tiles = span > 0 ? (span + 15) / 16 : 0;
+  const int n_my = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;   // steps warp, warp+4, ...
+  // Steps are issued in order m = 0, 1, ...
+  int pg_next = (PAGED && n_my > 0) ? entry_of(t_begin + 16 * warp) : 0;
+  auto issue = [&](int m, int stage) {
+    const int t0 = t_begin + 16 * (warp + kWarps * m);
+    int64_t r0 = t0;                                  // row of token t0 from the bases
+    if (PAGED) {
+      r0 = row_of(pg_next, t0);
+      if (m + 1 < n_my) pg_next = entry_of(t0 + 16 * kWarps);
+      if (r0 < 0 && lane == 0) set_dev_err(p.err, FA3_DEVERR_PAGE);
+    }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int i = lane + 32 * k, kv = i >> 7, row = (i >> 3) & 15, col = i & 7;
-      const int t = t0 + row;
-      const bool ok = t < t_end;
-      const int8_t* src = (kv ? vbase : kbase) + (int64_t)(ok ? t : t_begin) * tok_stride + col * 16;
+      const bool ok = t0 + row < t_end && r0 >= 0;
+      const int8_t* src = (kv ? vbase : kbase) + (ok ? r0 + row : 0) * tok_stride + col * 16;
       cp_async16(ring + stage * kStageBytes + kv * 2048 + row * 128 + ((col ^ swz(row)) << 4), src, ok ? 16u : 0u);
     }
   };
   auto chunk_addr = [&](uint32_t base, int row, int col) { return base + row * 128 + ((col ^ swz(row)) << 4); };
 
-  const int span = t_end - t_begin;
-  const int n_tiles = span > 0 ? (span + 15) / 16 : 0;
-  const int n_my = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;   // steps warp, warp+4, ...
 #pragma unroll
   for (int m = 0; m < kStages - 1; ++m) {
-    if (m < n_my) issue(warp + kWarps * m, m);
+    if (m < n_my) issue(m, m);
     cp_async_commit();
   }
   for (int m = 0; m < n_my; ++m) {
     const int it = warp + kWarps * m;
     const int t0 = t_begin + 16 * it;
-    if (m + kStages - 1 < n_my) issue(it + kWarps * (kStages - 1), (m + kStages - 1) % kStages);
+    if (m + kStages - 1 < n_my) issue(m + kStages - 1, (m + kStages - 1) % kStages);
     cp_async_commit();
     cp_async_wait<kStages - 1>();
     __syncwarp();
@@ -373,9 +396,10 @@ int gqa_blocks_per_sm() {
   static int cached = 0;
   if (cached <= 0) {
     int n = 0;
-    if (cudaFuncSetAttribute(gqa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+    if (cudaFuncSetAttribute(gqa_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel, kThreads, kSmemBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<false>, kThreads, kSmemBytes) !=
+            cudaSuccess ||
         n <= 0)
       n = 3;
     cached = n;
@@ -399,10 +423,13 @@ FA3_API size_t fa3_gqa_workspace_size(int B, int Hq, int Hkv, int D, int T_max) 
   return slots * kD * sizeof(float) + slots * sizeof(float2) + 256;
 }
 
-FA3_API int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale,
-                                const float* k_scale, const float* v_scale, const int32_t* lens, uint16_t* out,
-                                int B, int Hq, int Hkv, int D, int T_max, float softmax_scale, void* workspace,
-                                size_t workspace_bytes, int32_t* dev_err, void* stream) {
+namespace {
+// Both layouts: block_table == nullptr is the contiguous [B][T_max] cache; otherwise
+// k / v are pools of num_pages pages of page_size rows and T_max = max_pages * page_size.
+int gqa_decode(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale, const float* k_scale,
+               const float* v_scale, const int32_t* lens, const int32_t* block_table, uint16_t* out, int B, int Hq,
+               int Hkv, int D, int T_max, int num_pages, int page_size, int max_pages, float softmax_scale,
+               void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
   if (!q || !k || !v || !q_scale || !k_scale || !v_scale || !lens || !out) return FA3_EINVAL;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || T_max <= 0) return FA3_EINVAL;
   if (Hq % Hkv != 0) return FA3_EINVAL;
@@ -425,17 +452,42 @@ FA3_API int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* 
   a.part_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + slots * kD * sizeof(float)) : nullptr;
   a.err = dev_err;
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = G; a.T_max = T_max; a.splits = splits; a.chunk = chunk;
+  a.block_table = block_table; a.page_size = page_size; a.max_pages = max_pages; a.num_pages = num_pages;
+  a.div_ps = make_divu32((uint32_t)(page_size > 0 ? page_size : 1));
   a.sm_log2 = softmax_scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaFuncSetAttribute(gqa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+  auto* kernel = block_table ? gqa_decode_kernel<true> : gqa_decode_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return FA3_ECUDA;
   timing_begin(s);
-  const cudaError_t le = launch_pdl(gqa_decode_kernel, dim3(splits, Hkv, B), dim3(kThreads), kSmemBytes, s, a);
+  const cudaError_t le = launch_pdl(kernel, dim3(splits, Hkv, B), dim3(kThreads), kSmemBytes, s, a);
   timing_end(s);
   if (le != cudaSuccess) return FA3_ECUDA;
   if (splits > 1 && launch_pdl(gqa_combine_kernel, dim3(Hq, B), dim3(kD), 0, s, a) != cudaSuccess)
     return FA3_ECUDA;
   return FA3_OK;
+}
+}  // namespace
+
+FA3_API int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale,
+                                const float* k_scale, const float* v_scale, const int32_t* lens, uint16_t* out,
+                                int B, int Hq, int Hkv, int D, int T_max, float softmax_scale, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  return gqa_decode(q, k, v, q_scale, k_scale, v_scale, lens, nullptr, out, B, Hq, Hkv, D, T_max, 0, 0, 0,
+                    softmax_scale, workspace, workspace_bytes, dev_err, stream);
+}
+
+FA3_API int fa3_decode_attn_gqa_paged(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale,
+                                      const float* k_scale, const float* v_scale, const int32_t* lens,
+                                      const int32_t* block_table, uint16_t* out, int B, int Hq, int Hkv, int D,
+                                      int num_pages, int page_size, int max_pages, float softmax_scale,
+                                      void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (!block_table) return FA3_EINVAL;
+  if (num_pages <= 0 || page_size <= 0 || max_pages <= 0) return FA3_EINVAL;
+  if (page_size % 16 != 0 || (int64_t)max_pages * page_size >= ((int64_t)1 << 31)) return FA3_ERANGE;
+  return gqa_decode(q, k, v, q_scale, k_scale, v_scale, lens, block_table, out, B, Hq, Hkv, D,
+                    max_pages * page_size, num_pages, page_size, max_pages, softmax_scale, workspace,
+                    workspace_bytes, dev_err, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -107,10 +107,12 @@ static_assert(OFF_SCHED + 32 <= OFF_BAR + 1024, "barrier area");
 constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: normal waits last microseconds
 
 struct MlaParams {
-  CUtensorMap tm_rope;   // bf16 viewed as (8, T_max, Dr/8, B), box {8, 64, Dr/8, 1}
+  CUtensorMap tm_rope;   // bf16 viewed as (8, T_max, Dr/8, B), or (8, pool rows, Dr/8, 1) when paged
   const uint16_t* q;
-  const int8_t* ckv;     // [B][T_max][Dl]
-  const uint16_t* krope; // [B][T_max][Dr] bf16 (L2 prefetch; the tiles themselves come through tm_rope)
+  const int8_t* ckv;     // [B][T_max][Dl], or the [pool rows][Dl] page pool
+  const uint16_t* krope; // the same rows of Dr bf16 (L2 prefetch; the tiles themselves come through tm_rope)
+  const int32_t* block_table;   // [B][max_pages] pool pages, or nullptr for the contiguous layout
+  int page_size, max_pages, num_pages;
   const float* q_scale;
   const float* kv_scale;
   const int32_t* lens;
@@ -321,6 +323,23 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// Paged pool: tile tt of sequence b lies in the page that the block table names
+// (page_size is a multiple of 64, so a tile never spans two pages).  The entry is
+// loaded by page_ref and used only by page_row, one tile later, so that the load's
+// latency is not spent waiting.
+struct PageRef {
+  int pg;    // block-table entry as loaded
+  int off;   // row of the tile's first token inside that page
+};
+__device__ __forceinline__ PageRef page_ref(const MlaParams& p, int b, int tt) {
+  const int t0 = tt * kTok;
+  return PageRef{p.block_table[(int64_t)b * p.max_pages + t0 / p.page_size], t0 % p.page_size};
+}
+// Pool row of the tile's first token, or -1 when the entry is outside the pool.
+__device__ __forceinline__ int64_t page_row(const MlaParams& p, PageRef r) {
+  return (r.pg < 0 || r.pg >= p.num_pages) ? -1 : (int64_t)r.pg * p.page_size + r.off;
+}
+
 __device__ __forceinline__ int seq_tiles(const MlaParams& p, int b) {
   const int len = p.lens[b];
   if (len < 0 || len > p.T_max) return 0;
@@ -361,7 +380,7 @@ struct TileWalk {
   }
 };
 
-template <int DH>
+template <int DH, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ MlaParams p) {
   constexpr int CONV_TOTAL = kTok * (DH / 16);      // 16-byte int8 chunks of a tile (this CTA's latent half)
@@ -484,74 +503,158 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     // The first converter thread also streams the RoPE key tiles in with TMA.
     const int ct = tid - kConvWarp0 * 32;
     const bool rope_issuer = (ct == 0) && has_rope;
-    TileWalk tw{walk0};
-    uint4 v[CONV_UNITS];
-    auto load = [&](int b, int tt) {
-#pragma unroll
-      for (int i = 0; i < CONV_UNITS; ++i) {
-        const int u = ct + kConvThreads * i, n = u % kTok, cc = u / kTok;
-        const int row = tt * kTok + n;
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (u < CONV_TOTAL && row < p.T_max)
-          v[i] = __ldg(reinterpret_cast<const uint4*>(p.ckv + ((int64_t)b * p.T_max + row) * p.Dl + rank * DH) + cc);
-      }
-    };
-    // The register loads run one tile ahead, which is shorter than the HBM latency:
-    // the first converter thread of CTA 0 also prefetches into L2 the latent rows
-    // (both halves) and RoPE key rows of the tile kPrefetch tiles ahead.
-    constexpr int kPrefetch = 4;
-    const bool pf_issuer = ct == 0 && rank == 0;
-    TileWalk pfw{walk0};
-    auto prefetch = [&]() {
-      const int rows = min(kTok, p.T_max - pfw.tt * kTok);
-      const int64_t row0 = (int64_t)pfw.b * p.T_max + (int64_t)pfw.tt * kTok;
-      prefetch_l2(p.ckv + row0 * p.Dl, (uint32_t)(rows * p.Dl));
-      if (p.Dr > 0) prefetch_l2(p.krope + row0 * p.Dr, (uint32_t)(rows * p.Dr * 2));
-    };
-    bool pf_more = pf_issuer && pfw.next(p);
-    for (int i = 0; i < kPrefetch && pf_more; ++i) {
-      prefetch();
-      pf_more = pfw.next(p);
-    }
-    bool more = tw.next(p);
-    if (more) load(tw.b, tw.tt);
     uint32_t it = 0;
-    bool ok = true;
-    for (; ok && more; ++it) {
-      if (pf_more) {
+    if constexpr (PAGED) {
+      TileWalk tw{walk0};
+      uint4 v[CONV_UNITS];
+      // row0: the tile's first pool row (page_row of the entry loaded one tile earlier).
+      auto load = [&](int tt, int64_t row0) {
+        const int rows = row0 < 0 ? 0 : kTok;
+        if (row0 < 0 && ct == 0) set_dev_err(p.err, FA3_DEVERR_PAGE);
+#pragma unroll
+        for (int i = 0; i < CONV_UNITS; ++i) {
+          const int u = ct + kConvThreads * i, n = u % kTok, cc = u / kTok;
+          v[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (u < CONV_TOTAL && n < rows)
+            v[i] = __ldg(reinterpret_cast<const uint4*>(p.ckv + (row0 + n) * p.Dl + rank * DH) + cc);
+        }
+      };
+      // The register loads run one tile ahead, which is shorter than the HBM latency:
+      // the first converter thread of CTA 0 also prefetches into L2 the latent rows
+      // (both halves) and RoPE key rows of the tile kPrefetch tiles ahead.
+      constexpr int kPrefetch = 4;
+      const bool pf_issuer = ct == 0 && rank == 0;
+      TileWalk pfw{walk0};
+      bool pf_more = pf_issuer && pfw.next(p);
+      PageRef pf_ref = pf_more ? page_ref(p, pfw.b, pfw.tt) : PageRef{0, 0};
+      // Prefetches pfw's tile, steps pfw, and loads the next tile's entry (used on the next call).
+      auto prefetch = [&]() {
+        const int64_t pf_row = page_row(p, pf_ref);
+        if (pf_row >= 0) {
+          prefetch_l2(p.ckv + pf_row * p.Dl, (uint32_t)(kTok * p.Dl));
+          if (p.Dr > 0) prefetch_l2(p.krope + pf_row * p.Dr, (uint32_t)(kTok * p.Dr * 2));
+        }
+        pf_more = pfw.next(p);
+        if (pf_more) pf_ref = page_ref(p, pfw.b, pfw.tt);
+      };
+      for (int i = 0; i < kPrefetch && pf_more; ++i) prefetch();
+      // aw walks one tile ahead of tw, and its row is looked up while tw's tile
+      // converts, so that the block-table load is off the path of the tile loads.
+      TileWalk aw{walk0};
+      bool more = tw.next(p);
+      bool a_more = aw.next(p) && aw.next(p);
+      int64_t cur_row = more ? page_row(p, page_ref(p, tw.b, tw.tt)) : 0;
+      PageRef ahead = a_more ? page_ref(p, aw.b, aw.tt) : PageRef{0, 0};
+      if (more) load(tw.tt, cur_row);
+      bool ok = true;
+      for (; ok && more; ++it) {
+        if (pf_more) prefetch();
+        if (rope_issuer) {
+          const uint32_t st = it % NR;
+          ok = wait_bar(bar(B_ROPE_EMPTY + st), ((it / NR) & 1u) ^ 1u, abort_flag, p.err);
+          if (ok) {
+            mbar_expect_tx(bar(B_ROPE_FULL + st), rope_tx);
+            // Pool row of the tile (a bad page reads rows past the pool: zeros).
+            const int y = cur_row < 0 ? p.num_pages * p.page_size : (int)cur_row;
+            tma_4d(sbase + OFF_ROPE + st * ROPE_BYTES, &p.tm_rope, 0, y, 2 * rk0, 0, bar(B_ROPE_FULL + st));
+          }
+        }
+        const uint32_t cs = it % NC;
+        ok = ok && wait_bar(bar(B_C16_EMPTY + cs), ((it / NC) & 1u) ^ 1u, abort_flag, p.err);
+        if (!ok) break;
+        uint8_t* c16 = smem + OFF_C16 + cs * C16_BYTES;
+#pragma unroll
+        for (int i = 0; i < CONV_UNITS; ++i) {
+          const int u = ct + kConvThreads * i, n = u % kTok, cc = u / kTok;
+          if (u < CONV_TOTAL) {
+            uint4 o0, o1;
+            i8x4_to_f16x4(v[i].x, o0.x, o0.y);
+            i8x4_to_f16x4(v[i].y, o0.z, o0.w);
+            i8x4_to_f16x4(v[i].z, o1.x, o1.y);
+            i8x4_to_f16x4(v[i].w, o1.z, o1.w);
+            *reinterpret_cast<uint4*>(c16 + (2 * cc) * 1024 + n * 16) = o0;
+            *reinterpret_cast<uint4*>(c16 + (2 * cc + 1) * 1024 + n * 16) = o1;
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive(bar(B_C16_FULL + cs));
+        more = tw.next(p);
+        if (more) {
+          cur_row = page_row(p, ahead);
+          load(tw.tt, cur_row);
+        }
+        a_more = a_more && aw.next(p);
+        if (a_more) ahead = page_ref(p, aw.b, aw.tt);
+      }
+    } else {
+      TileWalk tw{walk0};
+      uint4 v[CONV_UNITS];
+      auto load = [&](int b, int tt) {
+#pragma unroll
+        for (int i = 0; i < CONV_UNITS; ++i) {
+          const int u = ct + kConvThreads * i, n = u % kTok, cc = u / kTok;
+          const int row = tt * kTok + n;
+          v[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (u < CONV_TOTAL && row < p.T_max)
+            v[i] = __ldg(reinterpret_cast<const uint4*>(p.ckv + ((int64_t)b * p.T_max + row) * p.Dl + rank * DH) + cc);
+        }
+      };
+      // The register loads run one tile ahead, which is shorter than the HBM latency:
+      // the first converter thread of CTA 0 also prefetches into L2 the latent rows
+      // (both halves) and RoPE key rows of the tile kPrefetch tiles ahead.
+      constexpr int kPrefetch = 4;
+      const bool pf_issuer = ct == 0 && rank == 0;
+      TileWalk pfw{walk0};
+      auto prefetch = [&]() {
+        const int rows = min(kTok, p.T_max - pfw.tt * kTok);
+        const int64_t row0 = (int64_t)pfw.b * p.T_max + (int64_t)pfw.tt * kTok;
+        prefetch_l2(p.ckv + row0 * p.Dl, (uint32_t)(rows * p.Dl));
+        if (p.Dr > 0) prefetch_l2(p.krope + row0 * p.Dr, (uint32_t)(rows * p.Dr * 2));
+      };
+      bool pf_more = pf_issuer && pfw.next(p);
+      for (int i = 0; i < kPrefetch && pf_more; ++i) {
         prefetch();
         pf_more = pfw.next(p);
       }
-      if (rope_issuer) {
-        const uint32_t st = it % NR;
-        ok = wait_bar(bar(B_ROPE_EMPTY + st), ((it / NR) & 1u) ^ 1u, abort_flag, p.err);
-        if (ok) {
-          mbar_expect_tx(bar(B_ROPE_FULL + st), rope_tx);
-          tma_4d(sbase + OFF_ROPE + st * ROPE_BYTES, &p.tm_rope, 0, tw.tt * kTok, 2 * rk0, tw.b,
-                 bar(B_ROPE_FULL + st));
-        }
-      }
-      const uint32_t cs = it % NC;
-      ok = ok && wait_bar(bar(B_C16_EMPTY + cs), ((it / NC) & 1u) ^ 1u, abort_flag, p.err);
-      if (!ok) break;
-      uint8_t* c16 = smem + OFF_C16 + cs * C16_BYTES;
-#pragma unroll
-      for (int i = 0; i < CONV_UNITS; ++i) {
-        const int u = ct + kConvThreads * i, n = u % kTok, cc = u / kTok;
-        if (u < CONV_TOTAL) {
-          uint4 o0, o1;
-          i8x4_to_f16x4(v[i].x, o0.x, o0.y);
-          i8x4_to_f16x4(v[i].y, o0.z, o0.w);
-          i8x4_to_f16x4(v[i].z, o1.x, o1.y);
-          i8x4_to_f16x4(v[i].w, o1.z, o1.w);
-          *reinterpret_cast<uint4*>(c16 + (2 * cc) * 1024 + n * 16) = o0;
-          *reinterpret_cast<uint4*>(c16 + (2 * cc + 1) * 1024 + n * 16) = o1;
-        }
-      }
-      fence_proxy_async();
-      mbar_arrive(bar(B_C16_FULL + cs));
-      more = tw.next(p);
+      bool more = tw.next(p);
       if (more) load(tw.b, tw.tt);
+      bool ok = true;
+      for (; ok && more; ++it) {
+        if (pf_more) {
+          prefetch();
+          pf_more = pfw.next(p);
+        }
+        if (rope_issuer) {
+          const uint32_t st = it % NR;
+          ok = wait_bar(bar(B_ROPE_EMPTY + st), ((it / NR) & 1u) ^ 1u, abort_flag, p.err);
+          if (ok) {
+            mbar_expect_tx(bar(B_ROPE_FULL + st), rope_tx);
+            tma_4d(sbase + OFF_ROPE + st * ROPE_BYTES, &p.tm_rope, 0, tw.tt * kTok, 2 * rk0, tw.b,
+                   bar(B_ROPE_FULL + st));
+          }
+        }
+        const uint32_t cs = it % NC;
+        ok = ok && wait_bar(bar(B_C16_EMPTY + cs), ((it / NC) & 1u) ^ 1u, abort_flag, p.err);
+        if (!ok) break;
+        uint8_t* c16 = smem + OFF_C16 + cs * C16_BYTES;
+#pragma unroll
+        for (int i = 0; i < CONV_UNITS; ++i) {
+          const int u = ct + kConvThreads * i, n = u % kTok, cc = u / kTok;
+          if (u < CONV_TOTAL) {
+            uint4 o0, o1;
+            i8x4_to_f16x4(v[i].x, o0.x, o0.y);
+            i8x4_to_f16x4(v[i].y, o0.z, o0.w);
+            i8x4_to_f16x4(v[i].z, o1.x, o1.y);
+            i8x4_to_f16x4(v[i].w, o1.z, o1.w);
+            *reinterpret_cast<uint4*>(c16 + (2 * cc) * 1024 + n * 16) = o0;
+            *reinterpret_cast<uint4*>(c16 + (2 * cc + 1) * 1024 + n * 16) = o1;
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive(bar(B_C16_FULL + cs));
+        more = tw.next(p);
+        if (more) load(tw.b, tw.tt);
+      }
     }
     // Drain: every issued RoPE copy must land before the CTA may exit.
     if (rope_issuer)
@@ -1084,7 +1187,7 @@ int max_clusters() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(mla_decode_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+  if (cudaFuncSetAttribute(mla_decode_kernel<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -1098,7 +1201,7 @@ int max_clusters() {
   cfg.numAttrs = 1;
   int n = 0;
   // Every width instantiation has the same block size and shared memory, hence the same residency.
-  if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<256>, &cfg) != cudaSuccess || n <= 0) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<256, false>, &cfg) != cudaSuccess || n <= 0) return 0;
   if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
 }
@@ -1112,9 +1215,10 @@ bool mla_shape_ok(int H, int Dl, int Dr) {
 // Decode kernel (timed by the optional caller events) and its combine kernel.
 template <int DH>
 cudaError_t launch_mla(cudaLaunchConfig_t cfg, cudaLaunchConfig_t ccfg, const MlaParams& prm) {
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  auto* kernel = prm.block_table ? mla_decode_kernel<DH, true> : mla_decode_kernel<DH, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  e = cudaLaunchKernelEx(&cfg, mla_decode_kernel<DH>, prm);
+  e = cudaLaunchKernelEx(&cfg, kernel, prm);
   timing_end(cfg.stream);
   if (e != cudaSuccess) return e;
   constexpr int O_PER = DH >= 64 ? DH / 2 : DH;
@@ -1164,10 +1268,13 @@ FA3_API size_t fa3_mla_workspace_size(int B, int H, int Dl, int T_max) {
   return mla_ws_parts(B, Dl, C, &a, &b2, &c, &d);
 }
 
-FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint16_t* krope, const float* q_scale,
-                                const float* kv_scale, const int32_t* lens, float* out, int B, int H, int Dl,
-                                int Dr, int T_max, float softmax_scale, void* workspace, size_t workspace_bytes,
-                                int32_t* dev_err, void* stream) {
+namespace {
+// Both layouts: block_table == nullptr is the contiguous [B][T_max] cache; otherwise
+// ckv / krope are pools of num_pages pages of page_size rows and T_max = max_pages * page_size.
+int mla_decode(const uint16_t* q, const int8_t* ckv, const uint16_t* krope, const float* q_scale,
+               const float* kv_scale, const int32_t* lens, const int32_t* block_table, float* out, int B, int H,
+               int Dl, int Dr, int T_max, int num_pages, int page_size, int max_pages, float softmax_scale,
+               void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
   if (!q || !ckv || !q_scale || !kv_scale || !lens || !out) return FA3_EINVAL;
   if (Dr > 0 && !krope) return FA3_EINVAL;
   if (B <= 0 || H <= 0 || Dl <= 0 || Dr < 0 || T_max <= 0) return FA3_EINVAL;
@@ -1189,8 +1296,10 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   prm.DH = Dl / 2;
   if (Dr > 0) {
     // (8 values, token, 8-wide chunk, sequence): one box lands as K-major core matrices.
-    const cuuint64_t dims[4] = {8, (cuuint64_t)T_max, (cuuint64_t)(Dr / 8), (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)Dr * 2, 16, (cuuint64_t)Dr * 2 * T_max};
+    // A paged pool is one "sequence" of num_pages * page_size rows.
+    const cuuint64_t rows = block_table ? (cuuint64_t)num_pages * page_size : (cuuint64_t)T_max;
+    const cuuint64_t dims[4] = {8, rows, (cuuint64_t)(Dr / 8), block_table ? 1u : (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)Dr * 2, 16, (cuuint64_t)Dr * 2 * rows};
     // one CTA's share: 2 * ((Dr/16 + 1) / 2) chunks (the decode kernel's RoPE split over the pair)
     const cuuint32_t box[4] = {8, (cuuint32_t)kTok, (cuuint32_t)(2 * ((Dr / 16 + 1) / 2)), 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
@@ -1210,6 +1319,7 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   prm.seg_hi = prm.seg_lo + B;
   prm.err = dev_err;
   prm.B = B; prm.H = H; prm.Dl = Dl; prm.Dr = Dr; prm.T_max = T_max;
+  prm.block_table = block_table; prm.num_pages = num_pages; prm.page_size = page_size; prm.max_pages = max_pages;
   prm.num_clusters = C;
   prm.sm_log2 = softmax_scale * 1.4426950408889634f;
 
@@ -1250,4 +1360,27 @@ FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint
   }
   if (le != cudaSuccess) return FA3_ECUDA;
   return cuda_status(cudaGetLastError());
+}
+}  // namespace
+
+FA3_API int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint16_t* krope, const float* q_scale,
+                                const float* kv_scale, const int32_t* lens, float* out, int B, int H, int Dl,
+                                int Dr, int T_max, float softmax_scale, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_err, void* stream) {
+  return mla_decode(q, ckv, krope, q_scale, kv_scale, lens, nullptr, out, B, H, Dl, Dr, T_max, 0, 0, 0,
+                    softmax_scale, workspace, workspace_bytes, dev_err, stream);
+}
+
+FA3_API int fa3_decode_attn_mla_paged(const uint16_t* q, const int8_t* ckv, const uint16_t* krope,
+                                      const float* q_scale, const float* kv_scale, const int32_t* lens,
+                                      const int32_t* block_table, float* out, int B, int H, int Dl, int Dr,
+                                      int num_pages, int page_size, int max_pages, float softmax_scale,
+                                      void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (!block_table) return FA3_EINVAL;
+  if (num_pages <= 0 || page_size <= 0 || max_pages <= 0) return FA3_EINVAL;
+  if (page_size % kTok != 0 || (int64_t)num_pages * page_size >= ((int64_t)1 << 31) ||
+      (int64_t)max_pages * page_size > (1 << 30) / 2)
+    return FA3_ERANGE;
+  return mla_decode(q, ckv, krope, q_scale, kv_scale, lens, block_table, out, B, H, Dl, Dr, max_pages * page_size,
+                    num_pages, page_size, max_pages, softmax_scale, workspace, workspace_bytes, dev_err, stream);
 }

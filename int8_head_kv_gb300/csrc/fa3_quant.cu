@@ -42,26 +42,15 @@ __global__ void qparams_kernel(const float* __restrict__ mn, const float* __rest
   if (h < H) scale[h] = __fdiv_rn(fmaxf(fabsf(mn[h]), fabsf(mx[h])), 127.0f);
 }
 
-// Division of 32-bit unsigned integers by a divisor fixed for the launch, as a
-// multiply-high and two shifts (Granlund and Montgomery, "Division by Invariant
-// Integers using Multiplication", 1994, the unsigned N-bit method with l =
-// ceil(log2 d)): exact for every 32-bit dividend.
-struct DivU32 {
-  uint32_t m, s1, s2;
+// Paged cache: position x of sequence b is row block_table[b][x / page_size] *
+// page_size + x % page_size of the pool.
+struct PageMap {
+  const int32_t* block_table;   // [B][max_pages]
+  int max_pages, num_pages, page_size;
+  DivU32 div_ps;                // / page_size
+  DivU32 div_row;               // / (H * D / 8): 16-byte groups per token row
+  DivU32 div_rope;              // / (Dr / 8)
 };
-inline DivU32 make_divu32(uint32_t d) {
-  uint32_t l = 0;
-  while ((1ull << l) < d) ++l;
-  DivU32 f;
-  f.m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
-  f.s1 = l < 1 ? l : 1;
-  f.s2 = l > 0 ? l - 1 : 0;
-  return f;
-}
-__device__ __forceinline__ uint32_t divu32(uint32_t n, DivU32 f) {
-  const uint32_t t1 = __umulhi(f.m, n);
-  return (t1 + ((n - t1) >> f.s1)) >> f.s2;
-}
 
 // Vector path.  The T_new new rows of sequence b are contiguous in the source and,
 // from cache row pos[b] on, contiguous in the cache as well, so the append of one
@@ -69,13 +58,16 @@ __device__ __forceinline__ uint32_t divu32(uint32_t n, DivU32 f) {
 // (i / (D/8)) mod H) becomes 8-byte cache group i, and the RoPE rows are a 16-byte
 // copy.  blockIdx.y walks the sequences, so pos[b] is one uniform load per block.
 // With G = 2 a thread converts two neighbouring groups and stores them as one
-// 16-byte word (the host picks G = 2 when every such word is 16-byte aligned).
-template <int G>
+// 16-byte word (the host picks G = 2 when every such word is 16-byte aligned; then
+// the groups of a token row are even in number and a pair never spans two rows).
+// PAGED: the cache is a page pool; each group's token row is looked up in the
+// block table (a pair shares one lookup).
+template <int G, bool PAGED>
 __global__ void __launch_bounds__(256) quantize_append_vec_kernel(
     const uint4* __restrict__ kv, const float* __restrict__ scale, int8_t* __restrict__ cache,
     const int32_t* __restrict__ pos, int B, int T_new, int H, int D, int T_max,
     const uint4* __restrict__ rope_src, uint16_t* __restrict__ rope_cache, int Dr, int32_t* err,
-    DivU32 div_g, DivU32 div_h) {
+    DivU32 div_g, DivU32 div_h, PageMap pm) {
   pdl_wait();
   pdl_launch_dependents();
   const uint32_t gpr = (uint32_t)(D / 8);
@@ -93,8 +85,26 @@ __global__ void __launch_bounds__(256) quantize_append_vec_kernel(
     }
     const int64_t row0 = (int64_t)b * T_max + p;                         // first cache row written
     const uint4* src = kv + (uint64_t)b * nl;
-    uint2* dst = reinterpret_cast<uint2*>(cache + row0 * H * D);
+    uint2* dst = reinterpret_cast<uint2*>(cache + (PAGED ? 0 : row0 * H * D));
+    // Pool row of position x of this sequence, or -1 for an entry outside the pool.
+    auto page_row = [&](uint32_t x) -> int64_t {
+      const uint32_t pi = divu32(x, pm.div_ps);
+      const int pg = pm.block_table[(int64_t)b * pm.max_pages + pi];
+      if (pg < 0 || pg >= pm.num_pages) {
+        set_dev_err(err, FA3_DEVERR_PAGE);
+        return -1;
+      }
+      return (int64_t)pg * pm.page_size + (x - pi * (uint32_t)pm.page_size);
+    };
     for (uint32_t i = tid * G; i < nl; i += nthreads * G) {
+      int64_t di = i;                                                       // uint2 index of group i in dst
+      if (PAGED) {
+        const uint32_t R = (uint32_t)H * gpr;
+        const uint32_t t = divu32(i, pm.div_row);
+        const int64_t row = page_row((uint32_t)p + t);
+        if (row < 0) continue;
+        di = row * R + (i - t * R);
+      }
       uint4 v[G];
 #pragma unroll
       for (int u = 0; u < G; ++u)
@@ -117,14 +127,24 @@ __global__ void __launch_bounds__(256) quantize_append_vec_kernel(
       const uint2 c0 = quant_group8(v[0], s, rs, ex);
       if (G == 2 && i + 1 < nl) {
         const uint2 c1 = quant_group8(v[G - 1], s1, rs1, ex1);
-        *reinterpret_cast<uint4*>(dst + i) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+        *reinterpret_cast<uint4*>(dst + di) = make_uint4(c0.x, c0.y, c1.x, c1.y);
       } else {
-        dst[i] = c0;
+        dst[di] = c0;
       }
     }
     const uint4* rsrc = rope_src + (uint64_t)b * nr;
-    uint4* rdst = reinterpret_cast<uint4*>(rope_cache + row0 * Dr);
-    for (uint32_t i = tid; i < nr; i += nthreads) rdst[i] = rsrc[i];
+    uint4* rdst = reinterpret_cast<uint4*>(rope_cache + (PAGED ? 0 : row0 * Dr));
+    for (uint32_t i = tid; i < nr; i += nthreads) {
+      int64_t di = i;
+      if (PAGED) {
+        const uint32_t gr = (uint32_t)(Dr / 8);
+        const uint32_t t = divu32(i, pm.div_rope);
+        const int64_t row = page_row((uint32_t)p + t);
+        if (row < 0) continue;
+        di = row * gr + (i - t * gr);
+      }
+      rdst[di] = rsrc[i];
+    }
   }
 }
 
@@ -199,9 +219,12 @@ FA3_API int fa3_qparams(const float* min_v, const float* max_v, float* scale, in
   return cuda_status(launch_pdl(qparams_kernel, dim3((H + 127) / 128), dim3(128), 0, s, min_v, max_v, scale, H));
 }
 
-FA3_API int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* cache, const int32_t* pos,
-                                int B, int T_new, int H, int D, int T_max, const uint16_t* rope_src,
-                                uint16_t* rope_cache, int Dr, int32_t* dev_err, void* stream) {
+namespace {
+// Both layouts: pm == nullptr is the contiguous [B][T_max] cache; otherwise the
+// cache (and the RoPE cache) are page pools addressed through *pm.
+int quantize_append(const uint16_t* kv, const float* scale, int8_t* cache, const int32_t* pos, int B, int T_new,
+                    int H, int D, int T_max, const uint16_t* rope_src, uint16_t* rope_cache, int Dr,
+                    int32_t* dev_err, void* stream, const PageMap* pm) {
   if (!kv || !scale || !cache || !pos) return FA3_EINVAL;
   if (B <= 0 || T_new <= 0 || H <= 0 || D <= 0 || T_max <= 0) return FA3_EINVAL;
   if (T_new > T_max) return FA3_EINVAL;
@@ -216,16 +239,18 @@ FA3_API int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* 
   const bool vec = (D % 8 == 0) && aligned16(kv) && (((uintptr_t)cache & 7u) == 0) &&
                    (!rope_cache || ((Dr % 8 == 0) && aligned16(rope_src) && aligned16(rope_cache))) &&
                    per_seq_groups < ((int64_t)1 << 31);
+  if (pm && !vec) return FA3_ERANGE;                   // the paged path has the vector kernel only
   const bool pairs = vec && aligned16(cache) && ((int64_t)H * D) % 16 == 0;   // 16-byte stores of two groups
+  using VecKernel = decltype(&quantize_append_vec_kernel<1, false>);
+  const VecKernel vk = pm ? (pairs ? quantize_append_vec_kernel<2, true> : quantize_append_vec_kernel<1, true>)
+                          : (pairs ? quantize_append_vec_kernel<2, false> : quantize_append_vec_kernel<1, false>);
   // Grid-stride loops; blocks for a few waves of the SMs.
-  static int resident[3] = {0, 0, 0};                  // scalar, vector, vector with pairs
-  const int kind = vec ? (pairs ? 2 : 1) : 0;
+  static int resident[5] = {0, 0, 0, 0, 0};            // scalar, then the four vector kernels
+  const int kind = vec ? 1 + (pairs ? 1 : 0) + (pm ? 2 : 0) : 0;
   if (resident[kind] == 0) {
     int r = 0;
-    const cudaError_t oe =
-        kind == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, quantize_append_vec_kernel<2>, 256, 0)
-        : kind == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, quantize_append_vec_kernel<1>, 256, 0)
-                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, quantize_append_scalar_kernel, 256, 0);
+    const cudaError_t oe = vec ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, vk, 256, 0)
+                               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, quantize_append_scalar_kernel, 256, 0);
     if (oe != cudaSuccess) return cuda_status(oe);
     resident[kind] = r > 0 ? r : 1;
   }
@@ -237,10 +262,11 @@ FA3_API int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* 
     const int64_t items = std::max<int64_t>((int64_t)T_new * H * (D / 8) / G, (int64_t)T_new * (Dr / 8));
     const int64_t gx = std::max<int64_t>(1, std::min<int64_t>((items + 255) / 256, 4 * ((cap + gy - 1) / gy)));
     const DivU32 dg = make_divu32((uint32_t)(D / 8)), dh = make_divu32((uint32_t)H);
-    auto* kernel = pairs ? quantize_append_vec_kernel<2> : quantize_append_vec_kernel<1>;
-    e = launch_pdl(kernel, dim3((unsigned)gx, (unsigned)gy), dim3(256), 0, s,
-                   reinterpret_cast<const uint4*>(kv), scale, cache, pos, B, T_new, H, D, T_max,
-                   reinterpret_cast<const uint4*>(rope_src), rope_cache, Dr, dev_err, dg, dh);
+    PageMap map = {};
+    if (pm) map = *pm;
+    e = launch_pdl(vk, dim3((unsigned)gx, (unsigned)gy), dim3(256), 0, s, reinterpret_cast<const uint4*>(kv), scale,
+                   cache, pos, B, T_new, H, D, T_max, reinterpret_cast<const uint4*>(rope_src), rope_cache, Dr,
+                   dev_err, dg, dh, map);
   } else {
     const int64_t work = (int64_t)B * T_new * (H * (int64_t)D + Dr);
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, cap));
@@ -248,4 +274,31 @@ FA3_API int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* 
                    T_new, H, D, T_max, rope_src, rope_cache, Dr, dev_err);
   }
   return cuda_status(e);
+}
+}  // namespace
+
+FA3_API int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* cache, const int32_t* pos,
+                                int B, int T_new, int H, int D, int T_max, const uint16_t* rope_src,
+                                uint16_t* rope_cache, int Dr, int32_t* dev_err, void* stream) {
+  return quantize_append(kv, scale, cache, pos, B, T_new, H, D, T_max, rope_src, rope_cache, Dr, dev_err, stream,
+                         nullptr);
+}
+
+FA3_API int fa3_quantize_append_paged(const uint16_t* kv, const float* scale, int8_t* cache,
+                                      const int32_t* block_table, const int32_t* pos, int B, int T_new, int H, int D,
+                                      int num_pages, int page_size, int max_pages, const uint16_t* rope_src,
+                                      uint16_t* rope_cache, int Dr, int32_t* dev_err, void* stream) {
+  if (!block_table) return FA3_EINVAL;
+  if (num_pages <= 0 || page_size <= 0 || max_pages <= 0) return FA3_EINVAL;
+  if ((int64_t)max_pages * page_size >= ((int64_t)1 << 31)) return FA3_ERANGE;
+  PageMap pm = {};
+  pm.block_table = block_table;
+  pm.max_pages = max_pages;
+  pm.num_pages = num_pages;
+  pm.page_size = page_size;
+  pm.div_ps = make_divu32((uint32_t)page_size);
+  pm.div_row = make_divu32((uint32_t)std::max(1, H * (D / 8)));
+  pm.div_rope = make_divu32((uint32_t)std::max(1, Dr / 8));
+  return quantize_append(kv, scale, cache, pos, B, T_new, H, D, max_pages * page_size, rope_src, rope_cache, Dr,
+                         dev_err, stream, &pm);
 }

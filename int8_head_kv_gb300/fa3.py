@@ -19,6 +19,7 @@ _lib = None
 FA3_DEVERR_POS = 1
 FA3_DEVERR_LENS = 2
 FA3_DEVERR_TIMEOUT = 4
+FA3_DEVERR_PAGE = 8
 
 
 class FA3Error(RuntimeError):
@@ -46,6 +47,11 @@ _SIGS = {
     "fa3_decode_attn_mla": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
     "fa3_gqa_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "fa3_decode_attn_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
+    "fa3_quantize_append_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
+    "fa3_decode_attn_mla_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ,
+                                       _P, _P]),
+    "fa3_decode_attn_gqa_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P,
+                                       _SZ, _P, _P]),
 }
 
 
@@ -243,4 +249,96 @@ def decode_attn_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: 
                                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
                                    _ptr(dev_err), _stream(stream))
     _check("fa3_decode_attn_gqa", st)
+    return out
+
+
+# ------------------------------------------------------------- paged cache
+def _block_table(block_table: torch.Tensor, B: int) -> int:
+    _need_contig(block_table, torch.int32, "block_table")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B][max_pages]")
+    return block_table.shape[1]
+
+
+def quantize_append_paged(kv: torch.Tensor, scale: torch.Tensor, cache: torch.Tensor, block_table: torch.Tensor,
+                          pos: torch.Tensor, rope_src: Optional[torch.Tensor] = None,
+                          rope_cache: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """kv bf16 [B][T_new][H][D] -> page pool int8 [num_pages][page_size][H][D] at pos[b]."""
+    _need_contig(kv, torch.bfloat16, "kv")
+    _need_contig(scale, torch.float32, "scale")
+    _need_contig(cache, torch.int8, "cache")
+    _need_contig(pos, torch.int32, "pos")
+    B, T_new, H, D = kv.shape
+    if cache.dim() != 4 or cache.shape[2] != H or cache.shape[3] != D:
+        raise ValueError("cache must be [num_pages][page_size][H][D]")
+    num_pages, page_size = cache.shape[0], cache.shape[1]
+    max_pages = _block_table(block_table, B)
+    Dr = 0
+    if rope_src is not None:
+        _need_contig(rope_src, torch.bfloat16, "rope_src")
+        _need_contig(rope_cache, torch.bfloat16, "rope_cache")
+        Dr = rope_src.shape[-1]
+    st = lib().fa3_quantize_append_paged(_ptr(kv), _ptr(scale), _ptr(cache), _ptr(block_table), _ptr(pos), B, T_new,
+                                         H, D, num_pages, page_size, max_pages, _ptr(rope_src), _ptr(rope_cache), Dr,
+                                         _ptr(dev_err), _stream(stream))
+    _check("fa3_quantize_append_paged", st)
+
+
+def decode_attn_mla_paged(q: torch.Tensor, ckv: torch.Tensor, krope: torch.Tensor, q_scale: torch.Tensor,
+                          kv_scale: torch.Tensor, lens: torch.Tensor, block_table: torch.Tensor, softmax_scale: float,
+                          out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Absorbed-MLA decode over page pools: ckv int8 [num_pages][page_size][Dl], krope bf16 [...][Dr]."""
+    _need_contig(q, torch.bfloat16, "q")
+    _need_contig(ckv, torch.int8, "ckv")
+    _need_contig(krope, torch.bfloat16, "krope")
+    _need_contig(q_scale, torch.float32, "q_scale")
+    _need_contig(kv_scale, torch.float32, "kv_scale")
+    _need_contig(lens, torch.int32, "lens")
+    B, H, Dqk = q.shape
+    num_pages, page_size, Dl = ckv.shape
+    Dr = krope.shape[2]
+    if Dqk != Dl + Dr:
+        raise ValueError("q last dim must be Dl + Dr")
+    max_pages = _block_table(block_table, B)
+    if out is None:
+        out = torch.empty(B, H, Dl, dtype=torch.float32, device=q.device)
+    nbytes = mla_workspace_size(B, H, Dl, max_pages * page_size)
+    if workspace is None:
+        workspace = _workspace("mla", nbytes, q.device)
+    st = lib().fa3_decode_attn_mla_paged(_ptr(q), _ptr(ckv), _ptr(krope), _ptr(q_scale), _ptr(kv_scale), _ptr(lens),
+                                         _ptr(block_table), _ptr(out), B, H, Dl, Dr, num_pages, page_size, max_pages,
+                                         float(softmax_scale), _ptr(workspace),
+                                         0 if workspace is None else workspace.numel(), _ptr(dev_err),
+                                         _stream(stream))
+    _check("fa3_decode_attn_mla_paged", st)
+    return out
+
+
+def decode_attn_gqa_paged(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: torch.Tensor,
+                          k_scale: torch.Tensor, v_scale: torch.Tensor, lens: torch.Tensor, block_table: torch.Tensor,
+                          softmax_scale: float, out: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """GQA decode over page pools: k/v int8 [num_pages][page_size][Hkv][D] -> bf16 [B][Hq][D]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need_contig(t, torch.int8, n)
+    for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need_contig(t, torch.float32, n)
+    _need_contig(lens, torch.int32, "lens")
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv = k.shape[0], k.shape[1], k.shape[2]
+    max_pages = _block_table(block_table, B)
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=q.device)
+    nbytes = gqa_workspace_size(B, Hq, Hkv, D, max_pages * page_size)
+    if workspace is None:
+        workspace = _workspace("gqa", nbytes, q.device)
+    st = lib().fa3_decode_attn_gqa_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                         _ptr(lens), _ptr(block_table), _ptr(out), B, Hq, Hkv, D, num_pages,
+                                         page_size, max_pages, float(softmax_scale), _ptr(workspace),
+                                         0 if workspace is None else workspace.numel(), _ptr(dev_err),
+                                         _stream(stream))
+    _check("fa3_decode_attn_gqa_paged", st)
     return out

@@ -207,6 +207,53 @@ def quantize_append(kv: np.ndarray, scale: np.ndarray, cache: np.ndarray, pos: n
     return out
 
 
+# ---------------------------------------------------------------------------
+# Paged cache.  The pages leave the KV cache's storage to the serving runtime
+# (MindIE, "FA3 quantization", usage steps: the runtime is told the cache's
+# format); the library's paged calls take the block-table layout, defined here
+# by the row map alone: token t of sequence b lives in pool page
+# block_table[b][t // page_size], row t % page_size.
+# ---------------------------------------------------------------------------
+def gather_paged(pool: np.ndarray, block_table: np.ndarray, page_size: int, rows: np.ndarray) -> np.ndarray:
+    """The contiguous cache [B][max_pages * page_size][...] that a page pool
+    [num_pages][page_size][...] and block table [B][max_pages] describe, for the
+    first rows[b] tokens of each sequence (later rows are left zero and no entry
+    of the table past them is read).  A needed entry outside the pool is an error.
+    """
+    B, max_pages = block_table.shape
+    out = np.zeros((B, max_pages * page_size) + pool.shape[2:], pool.dtype)
+    for b in range(B):
+        for t in range(int(rows[b])):
+            page = int(block_table[b, t // page_size])
+            if not 0 <= page < pool.shape[0]:
+                raise ValueError("block table entry outside the pool")
+            out[b, t] = pool[page, t % page_size]
+    return out
+
+
+def quantize_append_paged(kv: np.ndarray, scale: np.ndarray, pool: np.ndarray, block_table: np.ndarray,
+                          pos: np.ndarray) -> np.ndarray:
+    """quantize_append into a page pool: quantize(kv[b, t, h, :], scale[h]) goes
+    to the pool row of token pos[b] + t of sequence b (pool copied, then
+    returned).  Positions past max_pages * page_size, or a page outside the
+    pool, are errors.
+    """
+    out = np.array(pool, copy=True)
+    B, T_new, H, D = kv.shape
+    page_size = pool.shape[1]
+    for b in range(B):
+        p = int(pos[b])
+        if p < 0 or p + T_new > block_table.shape[1] * page_size:
+            raise ValueError("append position out of range")
+        for t in range(T_new):
+            x = p + t
+            page = int(block_table[b, x // page_size])
+            if not 0 <= page < pool.shape[0]:
+                raise ValueError("block table entry outside the pool")
+            out[page, x % page_size] = quantize(kv[b, t], np.asarray(scale, np.float32)[:, None])
+    return out
+
+
 def dequantize(q: np.ndarray, scale) -> np.ndarray:
     """deq_scale: code * scale, in float64."""
     return np.asarray(q, np.float64) * np.asarray(scale, np.float64)

@@ -54,3 +54,18 @@ def assert_attn_close(gpu, ref, bf16_out=False, what=""):
     assert max_abs <= ATOL, f"{what}: max abs error {max_abs:.3e} > {ATOL}"
     assert rrms <= RRMS, f"{what}: relative RMS {rrms:.3e} > {RRMS}"
     return max_abs, rrms
+
+
+def paged_layout(cache: np.ndarray, page_size: int, spare: int, rng) -> tuple:
+    """A page pool and block table holding `cache` [B][T][...]: each sequence's
+    rows are cut into pages of page_size (the last one zero-padded) and the pages
+    are stored in a random order among `spare` extra pages of noise."""
+    B, T = cache.shape[:2]
+    mp = -(-T // page_size)
+    padded = np.zeros((B, mp * page_size) + cache.shape[2:], cache.dtype)
+    padded[:, :T] = cache
+    n = B * mp + spare
+    perm = rng.permutation(n)
+    pool = (rng.standard_normal((n, page_size) + cache.shape[2:]) * 3).astype(cache.dtype)
+    pool[perm[:B * mp]] = padded.reshape((B * mp, page_size) + cache.shape[2:])
+    return pool, perm[:B * mp].reshape(B, mp).astype(np.int32)

@@ -77,6 +77,26 @@ def test_gqa_validation(L):
     assert call(Hq=128, Hkv=8) == ERANGE  # 16 query heads per KV head
 
 
+def test_paged_validation(L):
+    mla = lambda bt=FAKE, npg=8, ps=64, mp=4: L.fa3_decode_attn_mla_paged(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, bt, FAKE, 2, 128, 512, 64, npg, ps, mp, 0.07, FAKE, 1 << 30, None, None)
+    assert mla(bt=None) == EINVAL
+    assert mla(npg=0) == EINVAL
+    assert mla(ps=48) == ERANGE            # a 64-token tile would span two pages
+    assert mla(npg=1 << 26, ps=64) == ERANGE   # pool rows >= 2^31
+    gqa = lambda bt=FAKE, npg=8, ps=16, mp=4: L.fa3_decode_attn_gqa_paged(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, bt, FAKE, 2, 64, 8, 128, npg, ps, mp, 0.09, FAKE, 1 << 30,
+        None, None)
+    assert gqa(bt=None) == EINVAL
+    assert gqa(mp=0) == EINVAL
+    assert gqa(ps=24) == ERANGE            # a 16-token step would span two pages
+    app = lambda bt=FAKE, ps=16, mp=4, T_new=4: L.fa3_quantize_append_paged(
+        FAKE, FAKE, FAKE, bt, FAKE, 2, T_new, 1, 512, 8, ps, mp, None, None, 0, None, None)
+    assert app(bt=None) == EINVAL
+    assert app(ps=0) == EINVAL
+    assert app(T_new=65) == EINVAL         # more new rows than max_pages * page_size
+
+
 def test_kernel_timing_hook_validation(L):
     # exactly one event is an error; none turns the hook off (no CUDA call either way)
     assert L.fa3_set_kernel_timing(None, FAKE) == EINVAL

@@ -199,6 +199,65 @@ def test_quantize_append_writes_only_target_rows():
         O.quantize_append(kv, scale, cache, np.array([0, 7, 3], np.int32))
 
 
+# ----------------------------------------------------------------- paged cache
+def _pages_of(cache, page_size, perm):
+    """Pool and block table holding `cache` [B][T][...] (T a multiple of
+    page_size): page k of the natural order is stored at pool page perm[k]."""
+    B, T = cache.shape[:2]
+    mp = T // page_size
+    natural = cache.reshape((B * mp, page_size) + cache.shape[2:])
+    pool = np.zeros((len(perm),) + natural.shape[1:], cache.dtype)
+    pool[perm[:B * mp]] = natural
+    bt = perm[:B * mp].reshape(B, mp).astype(np.int32)
+    return pool, bt
+
+
+def test_gather_paged_identity_permutation_and_hand_rows():
+    rng = np.random.default_rng(21)
+    cache = rng.integers(-127, 128, (3, 12, 2, 4)).astype(np.int8)
+    full = np.full(3, 12)
+    ident = np.arange(9)
+    pool, bt = _pages_of(cache, 4, ident)
+    assert np.array_equal(O.gather_paged(pool, bt, 4, full), cache)
+    perm = rng.permutation(11)                          # two spare pages
+    pool, bt = _pages_of(cache, 4, perm)
+    assert np.array_equal(O.gather_paged(pool, bt, 4, full), cache)
+    # By hand: token 5 of sequence 1 is row 1 of natural page 1 * 3 + 1 = 4.
+    assert np.array_equal(pool[perm[4], 1], cache[1, 5])
+    assert np.array_equal(O.gather_paged(pool, bt, 4, full)[1, 5], pool[perm[4], 1])
+    # Rows past rows[b] are zero and their table entries are not read.
+    bt2 = bt.copy()
+    bt2[2, 1:] = -1
+    g = O.gather_paged(pool, bt2, 4, np.array([12, 12, 3]))
+    assert np.array_equal(g[2, :3], cache[2, :3]) and not g[2, 3:].any()
+    with pytest.raises(ValueError):
+        O.gather_paged(pool, bt2, 4, np.array([12, 12, 5]))
+
+
+def test_quantize_append_paged_matches_contiguous_append():
+    rng = np.random.default_rng(22)
+    B, T_new, H, D, P, mp = 3, 5, 2, 8, 4, 4
+    kv = _bf16(rng.standard_normal((B, T_new, H, D)))
+    scale = np.array([0.02, 0.05], np.float32)
+    cache = rng.integers(-127, 128, (B, mp * P, H, D)).astype(np.int8)
+    perm = rng.permutation(B * mp + 2)
+    pool, bt = _pages_of(cache, P, perm)
+    pos = np.array([0, 3, 11], np.int32)              # sequence 1 spans pages 0-2, sequence 2 ends the last
+    out = O.quantize_append_paged(kv, scale, pool, bt, pos)
+    full = np.full(B, mp * P)
+    assert np.array_equal(O.gather_paged(out, bt, P, full), O.quantize_append(kv, scale, cache, pos))
+    spare = perm[B * mp:]
+    assert np.array_equal(out[spare], pool[spare])     # pages no sequence owns stay untouched
+    # By hand: token 3 + 2 = 5 of sequence 1 is row 1 of its page 1.
+    assert np.array_equal(out[bt[1, 1], 1], O.quantize(kv[1, 2], scale[:, None]))
+    with pytest.raises(ValueError):
+        O.quantize_append_paged(kv, scale, pool, bt, np.array([0, 3, 12], np.int32))
+    bad = bt.copy()
+    bad[0, 1] = len(pool)
+    with pytest.raises(ValueError):
+        O.quantize_append_paged(kv, scale, pool, bad, pos)
+
+
 # ---------------------------------------------------------- decode attention
 def _sdpa64(q, k, v, scale):
     return torch.nn.functional.scaled_dot_product_attention(
