@@ -102,3 +102,28 @@ def test_kernel_timing_hook_validation(L):
     assert L.fa3_set_kernel_timing(None, FAKE) == EINVAL
     assert L.fa3_set_kernel_timing(FAKE, None) == EINVAL
     assert L.fa3_set_kernel_timing(None, None) == 0
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    # No fallback: with the shared library absent every call raises.
+    from int8_head_kv_gb300 import fa3 as F
+    monkeypatch.setattr(F, "_lib", None)
+    monkeypatch.setattr(F, "library_path", lambda: str(tmp_path / "missing" / "libfa3.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        F.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        F.mla_workspace_size(1, 1, 64, 64)
+
+
+def test_product_sources_never_reach_the_oracle():
+    # The package (binding, build script, kernels) neither imports nor names the
+    # oracle; the oracle is test infrastructure only.
+    import glob
+    import os
+    from helpers import ROOT
+    files = glob.glob(os.path.join(ROOT, "int8_head_kv_gb300", "**", "*.*"), recursive=True)
+    files = [f for f in files if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp"))]
+    assert len(files) >= 6
+    for f in files:
+        src = open(f, encoding="utf-8").read()
+        assert "oracle" not in src, f
