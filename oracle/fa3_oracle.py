@@ -356,6 +356,40 @@ def gqa_decode(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, q_scale: np.ndarr
     return out
 
 
+def gqa_prefill(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, q_scale: np.ndarray, k_scale: np.ndarray,
+                v_scale: np.ndarray, q_lens: np.ndarray, kv_lens: np.ndarray, softmax_scale: float) -> np.ndarray:
+    """Prefill-phase attention with INT8 q, k, v (MindIE "Attention Quantization",
+    Overview: q, k and v quantized to 8 bits), the same per-head scales as
+    gqa_decode.  Reading where the pages are silent: the q_lens[b] new rows of
+    sequence b are the last tokens of its kv_lens[b]-token context (a cached
+    prefix of kv_lens - q_lens tokens, then the new rows), and new row i, at
+    position kv_lens - q_lens + i, attends causally to positions 0 .. that
+    position.
+
+    q8: [B][S][Hq][D] (rows i >= q_lens[b] ignored), k8, v8: [B][T][Hkv][D].
+    Returns float64 [B][S][Hq][D]; ignored rows are zero.
+    """
+    B, S, Hq, D = q8.shape
+    Hkv = k8.shape[2]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    out = np.zeros((B, S, Hq, D), np.float64)
+    for b in range(B):
+        nq, nkv = int(q_lens[b]), int(kv_lens[b])
+        if nq < 0 or nq > S or nkv < nq or nkv > k8.shape[1]:
+            raise ValueError("bad q_lens / kv_lens")
+        for i in range(nq):
+            n = nkv - nq + i + 1                                   # keys 0 .. position of row i
+            for h in range(Hq):
+                g = h // G
+                acc = k8[b, :n, g].astype(np.int64) @ q8[b, i, h].astype(np.int64)    # [n] exact
+                s_ = acc.astype(np.float64) * (float(q_scale[h]) * float(k_scale[g])) * float(softmax_scale)
+                p_ = _softmax_weights(s_)
+                out[b, i, h] = float(v_scale[g]) * (p_ @ v8[b, :n, g].astype(np.float64))
+    return out
+
+
 def gqa_decode_float(q: np.ndarray, k: np.ndarray, v: np.ndarray, lens: np.ndarray,
                      softmax_scale: float) -> np.ndarray:
     """Same attention on unquantized float q, k, v (the quantization-error reference)."""

@@ -398,3 +398,54 @@ def test_gqa_float_reference_matches_sdpa():
     ref = torch.nn.functional.scaled_dot_product_attention(
         torch.from_numpy(qd)[:, None], torch.from_numpy(kd), torch.from_numpy(vd), scale=w.softmax_scale)[:, 0]
     assert np.max(np.abs(out[0] - ref.numpy())) < 1e-12
+
+
+# ------------------------------------------------------ prefill (GQA, INT8 q/k/v)
+def _prefill_case(seed=0, B=2, S=9, Hq=4, Hkv=2, D=16, T=14):
+    rng = np.random.default_rng(seed)
+    q8 = rng.integers(-127, 128, (B, S, Hq, D)).astype(np.int8)
+    k8 = rng.integers(-127, 128, (B, T, Hkv, D)).astype(np.int8)
+    v8 = rng.integers(-127, 128, (B, T, Hkv, D)).astype(np.int8)
+    qs = rng.uniform(0.002, 0.01, Hq).astype(np.float32)
+    ks = rng.uniform(0.002, 0.01, Hkv).astype(np.float32)
+    vs = rng.uniform(0.01, 0.05, Hkv).astype(np.float32)
+    return q8, k8, v8, qs, ks, vs
+
+
+def test_prefill_rows_are_decodes_at_their_positions():
+    q8, k8, v8, qs, ks, vs = _prefill_case()
+    q_lens, kv_lens = np.array([9, 4]), np.array([14, 6])        # prefixes of 5 and 2 cached tokens
+    out = O.gqa_prefill(q8, k8, v8, qs, ks, vs, q_lens, kv_lens, 0.25)
+    for b in range(2):
+        for i in range(9):
+            if i >= q_lens[b]:
+                assert not out[b, i].any()
+                continue
+            pos = kv_lens[b] - q_lens[b] + i
+            one = O.gqa_decode(q8[b:b + 1, i], k8[b:b + 1], v8[b:b + 1], qs, ks, vs, np.array([pos + 1]), 0.25)
+            assert np.allclose(out[b, i], one[0], rtol=0, atol=1e-12)
+
+
+def test_prefill_matches_causal_sdpa_on_dequantized():
+    q8, k8, v8, qs, ks, vs = _prefill_case(seed=1, B=1, S=12, T=12)
+    out = O.gqa_prefill(q8, k8, v8, qs, ks, vs, np.array([12]), np.array([12]), 0.2)
+    G = 2
+    q = q8[0].astype(np.float64) * qs[None, :, None]              # [S][Hq][D]
+    k = np.repeat(k8[0].astype(np.float64) * ks[None, :, None], G, axis=1)
+    v = np.repeat(v8[0].astype(np.float64) * vs[None, :, None], G, axis=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q.transpose(1, 0, 2)), torch.from_numpy(k.transpose(1, 0, 2)),
+        torch.from_numpy(v.transpose(1, 0, 2)), is_causal=True, scale=0.2).numpy().transpose(1, 0, 2)
+    assert np.allclose(out[0], ref, rtol=1e-9, atol=1e-12)
+
+
+def test_prefill_first_row_and_validation():
+    q8, k8, v8, qs, ks, vs = _prefill_case(seed=2)
+    out = O.gqa_prefill(q8, k8, v8, qs, ks, vs, np.array([9, 0]), np.array([9, 3]), 0.3)
+    # a plain prefill's first row sees only token 0: its output is that token's value row
+    for h in range(4):
+        assert np.allclose(out[0, 0, h], v8[0, 0, h // 2] * float(vs[h // 2]), rtol=0, atol=1e-12)
+    assert not out[1].any()                                       # no new rows
+    with pytest.raises(ValueError):
+        O.gqa_prefill(q8, k8, v8, qs, ks, vs, np.array([9, 4]), np.array([8, 6]), 0.3)   # kv_lens < q_lens
+
