@@ -103,13 +103,19 @@ def _need_contig(t: torch.Tensor, dtype, name: str):
 _ws_cache = {}
 
 
-def _workspace(key, nbytes: int, device, zero: bool = False) -> Optional[torch.Tensor]:
+def _workspace(key, nbytes: int, device, zero: bool = False, stream=None) -> Optional[torch.Tensor]:
+    """A cached scratch buffer per (call kind, device, stream): calls that share a
+    workspace must not overlap, and calls on one stream never do.  It is allocated
+    (and zeroed) on that stream, so its first use is ordered after the fill."""
     if nbytes == 0:
         return None
-    k = (key, device.index if device.index is not None else torch.cuda.current_device())
+    dev = device.index if device.index is not None else torch.cuda.current_device()
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    k = (key, dev, s.cuda_stream)
     ws = _ws_cache.get(k)
     if ws is None or ws.numel() < nbytes:
-        ws = (torch.zeros if zero else torch.empty)(nbytes, dtype=torch.uint8, device=device)
+        with torch.cuda.stream(s):
+            ws = (torch.zeros if zero else torch.empty)(nbytes, dtype=torch.uint8, device=device)
         _ws_cache[k] = ws
     return ws
 
@@ -153,7 +159,7 @@ def calibrate_perhead(x: torch.Tensor, ratio: float, min_io: torch.Tensor, max_i
         raise ValueError("min_io/max_io must hold H values")
     nbytes = calibrate_workspace_size(H)
     if workspace is None:
-        workspace = _workspace("calib", nbytes, x.device, zero=True)
+        workspace = _workspace("calib", nbytes, x.device, zero=True, stream=stream)
     st = lib().fa3_calibrate_perhead(_ptr(x), B, H, L, sb, sh, float(ratio), _ptr(min_io), _ptr(max_io),
                                      _ptr(workspace), workspace.numel(), _stream(stream))
     _check("fa3_calibrate_perhead", st)
@@ -215,7 +221,7 @@ def decode_attn_mla(q: torch.Tensor, ckv: torch.Tensor, krope: torch.Tensor, q_s
         out = torch.empty(B, H, Dl, dtype=torch.float32, device=q.device)
     nbytes = mla_workspace_size(B, H, Dl, T_max)
     if workspace is None:
-        workspace = _workspace("mla", nbytes, q.device)
+        workspace = _workspace("mla", nbytes, q.device, stream=stream)
     st = lib().fa3_decode_attn_mla(_ptr(q), _ptr(ckv), _ptr(krope), _ptr(q_scale), _ptr(kv_scale), _ptr(lens),
                                    _ptr(out), B, H, Dl, Dr, T_max, float(softmax_scale), _ptr(workspace),
                                    0 if workspace is None else workspace.numel(), _ptr(dev_err), _stream(stream))
@@ -243,7 +249,7 @@ def decode_attn_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: 
         out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=q.device)
     nbytes = gqa_workspace_size(B, Hq, Hkv, D, T_max)
     if workspace is None:
-        workspace = _workspace("gqa", nbytes, q.device)
+        workspace = _workspace("gqa", nbytes, q.device, stream=stream)
     st = lib().fa3_decode_attn_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
                                    _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_max, float(softmax_scale),
                                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
@@ -306,7 +312,7 @@ def decode_attn_mla_paged(q: torch.Tensor, ckv: torch.Tensor, krope: torch.Tenso
         out = torch.empty(B, H, Dl, dtype=torch.float32, device=q.device)
     nbytes = mla_workspace_size(B, H, Dl, max_pages * page_size)
     if workspace is None:
-        workspace = _workspace("mla", nbytes, q.device)
+        workspace = _workspace("mla", nbytes, q.device, stream=stream)
     st = lib().fa3_decode_attn_mla_paged(_ptr(q), _ptr(ckv), _ptr(krope), _ptr(q_scale), _ptr(kv_scale), _ptr(lens),
                                          _ptr(block_table), _ptr(out), B, H, Dl, Dr, num_pages, page_size, max_pages,
                                          float(softmax_scale), _ptr(workspace),
@@ -334,7 +340,7 @@ def decode_attn_gqa_paged(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_s
         out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=q.device)
     nbytes = gqa_workspace_size(B, Hq, Hkv, D, max_pages * page_size)
     if workspace is None:
-        workspace = _workspace("gqa", nbytes, q.device)
+        workspace = _workspace("gqa", nbytes, q.device, stream=stream)
     st = lib().fa3_decode_attn_gqa_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
                                          _ptr(lens), _ptr(block_table), _ptr(out), B, Hq, Hkv, D, num_pages,
                                          page_size, max_pages, float(softmax_scale), _ptr(workspace),

@@ -127,3 +127,32 @@ def test_product_sources_never_reach_the_oracle():
     for f in files:
         src = open(f, encoding="utf-8").read()
         assert "oracle" not in src, f
+
+
+def test_workspace_cache_is_per_stream(monkeypatch):
+    # One scratch buffer per (call kind, device, stream); a larger request replaces it.
+    import contextlib
+    import torch
+    from int8_head_kv_gb300 import fa3 as F
+
+    class FakeStream:
+        def __init__(self, h):
+            self.cuda_stream = h
+
+    cur = FakeStream(11)
+    monkeypatch.setattr(F, "_ws_cache", {})
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda dev=None: cur)
+    monkeypatch.setattr(torch.cuda, "stream", lambda s: contextlib.nullcontext())
+    cpu = torch.device("cpu")
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    assert F._workspace("mla", 0, cpu) is None
+    a = F._workspace("mla", 64, cpu)
+    assert a is F._workspace("mla", 32, cpu)                      # same stream: reused
+    b = F._workspace("mla", 64, cpu, stream=FakeStream(12))
+    assert b is not a                                             # another stream: its own buffer
+    c = F._workspace("gqa", 64, cpu)
+    assert c is not a                                             # another call kind
+    d = F._workspace("mla", 128, cpu)
+    assert d is not a and d.numel() == 128 and F._workspace("mla", 100, cpu) is d
+    z = F._workspace("calib", 16, cpu, zero=True)
+    assert not z.any()
