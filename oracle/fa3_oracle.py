@@ -22,8 +22,10 @@ integer (the INT8 code); there the decision is taken in IEEE float32, the
 precision of the kernels (x / scale is one correctly rounded float32 division,
 then round-half-to-even).  Readings of points the pages leave open:
 
-* window width = sorted[i+t-1] - sorted[i] in float64 (exact for bf16 inputs
-  whose exponents differ by less than 45), ties -> first (smallest) i;
+* window width = sorted[i+t-1] - sorted[i] as an exact rational number (the
+  pages do not fix the subtraction's precision; exact is the plain reading, and
+  float64 alone is not exact once the two ends lie more than 45 binades apart),
+  ties -> first (smallest) i;
 * target_num = int(ratio * N) with the product in float64 and truncation, as
   in Python; clamped to at least 1; ratio must lie in (0, 1];
 * -0.0 sorts before +0.0 (IEEE totalOrder), and min/max accumulation uses the
@@ -37,6 +39,7 @@ Every function here is pinned by ``tests/test_oracle_pins.py``.
 from __future__ import annotations
 
 import math
+from fractions import Fraction
 from typing import Iterable, Optional, Tuple
 
 import numpy as np
@@ -71,18 +74,34 @@ def sort_total_order(values: np.ndarray) -> np.ndarray:
     return s
 
 
+def _first_exact_min(lo_vals: np.ndarray, hi_vals: np.ndarray) -> int:
+    """Index of the first pair whose exact width hi - lo is smallest.
+
+    Rounding to float64 is monotone, so the exact minimum lies among the pairs
+    whose float64 width equals the smallest float64 width; those few are
+    compared again as exact rationals (every float is a dyadic rational).
+    """
+    widths = hi_vals - lo_vals
+    cand = np.flatnonzero(widths == widths.min())
+    if cand.size == 1 or widths[cand[0]] == 0.0:   # a float64 zero width is exact
+        return int(cand[0])
+    exact = [Fraction(float(hi_vals[k])) - Fraction(float(lo_vals[k])) for k in cand]
+    best = min(range(len(cand)), key=lambda j: (exact[j], j))
+    return int(cand[best])
+
+
 def recall_window(head_values: np.ndarray, ratio: float) -> Tuple[float, float]:
     """Narrowest window of the sorted head holding target_num values.
 
     FA3量化 算法流程 step 2: sort the N points, target_num = int(ratio*N), slide
     i = 0 .. N - target_num over [sorted[i], sorted[i+target_num-1]], keep the
-    window of smallest length; output (min_val, max_val).
+    window of smallest length (exact length; the first i among equals); output
+    (min_val, max_val).
     """
     s = sort_total_order(head_values)
     n = s.size
     t = target_num(ratio, n)
-    widths = s[t - 1:] - s[: n - t + 1]          # window_length for i = 0 .. N - t
-    i = int(np.argmin(widths))                    # first minimum
+    i = _first_exact_min(s[: n - t + 1], s[t - 1:])   # window_length for i = 0 .. N - t
     return float(s[i]), float(s[i + t - 1])
 
 
@@ -90,8 +109,9 @@ def recall_window_bruteforce(head_values: np.ndarray, ratio: float) -> Tuple[flo
     """Same answer by exhaustive search over value pairs, without any sort.
 
     Among all pairs (a, b) of data values with a <= b whose closed interval
-    holds at least target_num values, the narrowest one (float64 width), ties
-    broken by the smallest a and then the smallest b.  O(N^2) memory.
+    holds at least target_num values, the narrowest one (exact width, every
+    candidate width compared as a rational), ties broken by the smallest a and
+    then the smallest b.  O(N^2) memory.
     """
     v = np.asarray(head_values, dtype=np.float64).ravel()
     n = v.size
@@ -102,11 +122,9 @@ def recall_window_bruteforce(head_values: np.ndarray, ratio: float) -> Tuple[flo
     b = v[None, :]
     count = le[None, :] - lt[:, None]                          # #{a <= x <= b}
     ok = (a <= b) & (count >= t)
-    width = np.where(ok, b - a, np.inf)
-    wmin = width.min()
-    cand = np.argwhere(width == wmin)
-    best = min(((v[i], v[j]) for i, j in cand), key=lambda p: (p[0], p[1]))
-    return float(best[0]), float(best[1])
+    pairs = np.argwhere(ok)
+    best = min(((Fraction(float(v[j])) - Fraction(float(v[i])), v[i], v[j]) for i, j in pairs))
+    return float(best[1]), float(best[2])
 
 
 # ---------------------------------------------------------------------------

@@ -139,8 +139,9 @@ def test_workspace_cache_is_per_stream(monkeypatch):
         def __init__(self, h):
             self.cuda_stream = h
 
+    from collections import OrderedDict
     cur = FakeStream(11)
-    monkeypatch.setattr(F, "_ws_cache", {})
+    monkeypatch.setattr(F, "_ws_cache", OrderedDict())
     monkeypatch.setattr(torch.cuda, "current_stream", lambda dev=None: cur)
     monkeypatch.setattr(torch.cuda, "stream", lambda s: contextlib.nullcontext())
     cpu = torch.device("cpu")
@@ -156,3 +157,45 @@ def test_workspace_cache_is_per_stream(monkeypatch):
     assert d is not a and d.numel() == 128 and F._workspace("mla", 100, cpu) is d
     z = F._workspace("calib", 16, cpu, zero=True)
     assert not z.any()
+    # at most _WS_PER_KIND streams per (call kind, device): the least recently used goes
+    for h in range(20, 20 + F._WS_PER_KIND):
+        F._workspace("mla", 64, cpu, stream=FakeStream(h))
+    mla_streams = [k[2] for k in F._ws_cache if k[0] == "mla"]
+    assert len(mla_streams) == F._WS_PER_KIND and 11 not in mla_streams and 12 not in mla_streams
+    assert ("gqa", 0, 11) in F._ws_cache and ("calib", 0, 11) in F._ws_cache
+
+
+def test_failed_calibration_drops_its_cached_workspace(monkeypatch):
+    # After an error the key-count table may not be clear again: the binding must not
+    # hand the cached buffer to the next calibration on that stream.
+    import contextlib
+    from collections import OrderedDict
+    import torch
+    from int8_head_kv_gb300 import fa3 as F
+
+    class FakeStream:
+        cuda_stream = 11
+
+    class FakeLib:
+        def fa3_calibrate_workspace_size(self, H):
+            return 64
+
+        def fa3_calibrate_perhead(self, *a):
+            return 3                                    # FA3_ECUDA
+
+        def fa3_status_string(self, s):
+            return b"FA3_ECUDA"
+
+    monkeypatch.setattr(F, "_ws_cache", OrderedDict())
+    monkeypatch.setattr(F, "lib", lambda: FakeLib())
+    monkeypatch.setattr(F, "_need", lambda *a: None)
+    monkeypatch.setattr(F, "_need_contig", lambda *a: None)
+    monkeypatch.setattr(F, "_stream", lambda s=None: None)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda dev=None: FakeStream())
+    monkeypatch.setattr(torch.cuda, "stream", lambda s: contextlib.nullcontext())
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    x = torch.zeros(2, 8, dtype=torch.bfloat16)
+    mn, mx = torch.zeros(2), torch.zeros(2)
+    with pytest.raises(F.FA3Error):
+        F.calibrate_perhead(x, 0.9, mn, mx)
+    assert ("calib", 0, 11) not in F._ws_cache

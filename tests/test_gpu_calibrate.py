@@ -1,4 +1,6 @@
 """GPU parity of the per-head Recall-Window calibration: bit-exact min/max against the oracle."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -96,21 +98,66 @@ def test_resume_from_saved_range():
     assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn)) and np.array_equal(_bits(mx.cpu().numpy()), _bits(omx))
 
 
+def _exact_width_heads(N, t):
+    """Two heads whose first two windows have lengths 1 + 2^-120 and 1 (equal in
+    float64): the exact reading must pick the second, (0, 1).  Head 0 holds
+    t - 3 copies of 0.5 between the ends and 2^100 after them; head 1
+    repeats the hand-worked golden example's values to fill N."""
+    a = np.empty(N, np.float32)
+    a[0], a[1], a[2:t - 1], a[t - 1:t + 1], a[t + 1:] = -2.0 ** -120, 0.0, 0.5, 1.0, 2.0 ** 100
+    b = np.tile(np.array([1.0, -2.0 ** -120, 1.0, 0.0], np.float32), N // 4)
+    return np.stack([a, b])
+
+
+@pytest.mark.parametrize("ratio", ["tail", "full"])
+def test_exact_window_widths_mixed_magnitudes(ratio):
+    # Window lengths that tie after rounding to float64 but not exactly, on the
+    # tail path (few windows) and on the full-histogram path (many windows), plus
+    # random heads spanning ~130 binades.
+    F = fa3()
+    N = 98304
+    r = (N - 0.5) / N if ratio == "tail" else 0.5
+    t = O.target_num(r, N)
+    rng = np.random.default_rng(21)
+    x = np.concatenate([_exact_width_heads(N, t)[:1] if ratio == "tail" else _exact_width_heads(N, t),
+                        np.stack([W.mixed_magnitude_head(rng, N) for _ in range(3)])])
+    H = x.shape[0]
+    gmn, gmx = _gpu_calibrate(F, [x.reshape(1, H, 1, N)], r, H)
+    omn, omx = O.calibrate([x.reshape(1, H, 1, N)], r)
+    assert (float(omn[0]), float(omx[0])) == (0.0, 1.0)
+    assert np.array_equal(_bits(gmn), _bits(omn)), (gmn, omn)
+    assert np.array_equal(_bits(gmx), _bits(omx)), (gmx, omx)
+
+
 @pytest.mark.slow
-def test_full_size_calibration_sampled_heads():
-    # One (4, 128, 2048, 192) batch on the GPU; eight heads recomputed by the oracle.
+def test_full_size_calibration_all_heads_four_batches():
+    # The (4, 128, 2048, 192) workload: four batches with the running min/max, every
+    # head compared bit for bit after every batch (the oracle runs one thread per head).
+    from concurrent.futures import ThreadPoolExecutor
     F = fa3()
     w = W.calib_scale()
     x = torch.empty(w.B, w.H, w.S, w.D, dtype=torch.bfloat16, device="cuda")
-    for h in range(w.H):
-        x[:, h] = bf16_dev(W.calib_head(w, 0, h))
     mn = torch.full((w.H,), float("inf"), device="cuda")
     mx = torch.full((w.H,), float("-inf"), device="cuda")
-    F.calibrate_perhead(x, w.ratio, mn, mx)
-    gmn, gmx = mn.cpu().numpy(), mx.cpu().numpy()
-    for h in (0, 1, 17, 42, 63, 64, 100, 127):
-        lo, hi = O.recall_window(W.calib_head(w, 0, h), w.ratio)
-        assert (gmn[h], gmx[h]) == (np.float32(lo), np.float32(hi)), h
+    omn, omx = O.init_range(w.H)
+
+    def head(kh):
+        v = W.calib_head(w, *kh)
+        return v, O.recall_window(v, w.ratio)
+
+    with ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1))) as ex:
+        for k in range(w.batches):
+            lo, hi = np.empty(w.H, np.float32), np.empty(w.H, np.float32)
+            for h, (v, (a, b)) in enumerate(ex.map(head, [(k, h) for h in range(w.H)])):
+                x[:, h] = bf16_dev(v)
+                lo[h], hi[h] = a, b
+            F.calibrate_perhead(x, w.ratio, mn, mx)
+            O.accumulate(omn, omx, lo, hi)
+            torch.cuda.synchronize()
+            assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn)), k
+            assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx)), k
+    sc = F.qparams(mn, mx).cpu().numpy()
+    assert np.array_equal(_bits(sc), _bits(O.qparams(omn, omx)))
 
 
 def _sampled_units(units, n_samples=512):

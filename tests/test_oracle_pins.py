@@ -32,6 +32,35 @@ def test_recall_window_hand_example():
     assert sc[0] == np.float32(g["abs_max"]) / np.float32(127)
 
 
+def test_recall_window_exact_width_hand_example():
+    # Two windows whose lengths differ by 2^-120 but round to the same float64.
+    g = json.load(open(os.path.join(GOLDEN, "recall_window_exact_width.json")))
+    v = np.array([float.fromhex(x) for x in g["values_hex"]], np.float32)
+    assert O.target_num(g["ratio"], v.size) == g["target_num"]
+    want = (float.fromhex(g["min_val_hex"]), float.fromhex(g["max_val_hex"]))
+    assert O.recall_window(v, g["ratio"]) == want
+    assert O.recall_window_bruteforce(v, g["ratio"]) == want
+    # the float64 lengths do tie, so the example separates the two readings
+    s = np.sort(v.astype(np.float64))
+    w = s[2:] - s[:2]
+    assert w[0] == w[1] and (s[0], s[2]) == tuple(float.fromhex(x) for x in g["float64_first_min_hex"])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_recall_window_exact_widths_match_bruteforce_mixed_magnitudes(seed):
+    rng = np.random.default_rng(100 + seed)
+    v = W.mixed_magnitude_head(rng, int(rng.integers(20, 250)))
+    ties = 0
+    for ratio in (1.0, 0.9999, 0.95, 0.9, 0.75, 0.5, 0.2):
+        got = O.recall_window(v, ratio)
+        assert got == O.recall_window_bruteforce(v, ratio), (seed, ratio)
+        t = O.target_num(ratio, v.size)
+        s = O.sort_total_order(v)
+        w = s[t - 1:] - s[: v.size - t + 1]
+        ties += int(np.count_nonzero(w == w.min()) > 1)
+    assert ties > 0          # float64 lengths tied somewhere: the exact comparison decided
+
+
 def test_target_num_values():
     # The two calibration sizes of the workloads: 0.9999 * 16384 and 0.9999 * 1572864.
     assert O.target_num(0.9999, 2 * 128 * 64) == 16382

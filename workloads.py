@@ -71,6 +71,17 @@ def student_t(rng, shape, nu, sigma) -> np.ndarray:
     return (rng.standard_t(nu, size=shape).astype(np.float32) * np.asarray(sigma, np.float32)).astype(np.float32)
 
 
+def mixed_magnitude_head(rng: np.random.Generator, n: int) -> np.ndarray:
+    """A calibration head whose values span about 130 binades: integers in [-3, 3]
+    (many windows of equal integer length), 15 % of them replaced by values of
+    magnitude 2^-133 .. 2^-100, so that window lengths differ only far below
+    float64's precision.  bf16-exact float32 [n]."""
+    v = rng.integers(-3, 4, n).astype(np.float64)
+    tiny = np.ldexp(rng.integers(1, 256, n).astype(np.float64), rng.integers(-133, -107, n))
+    v = np.where(rng.random(n) < 0.15, np.where(rng.random(n) < 0.5, -tiny, tiny), v)
+    return bf16_round(v.astype(np.float32))
+
+
 # ----------------------------------------------------------------------------
 # Absorbed-MLA decode workloads
 # ----------------------------------------------------------------------------
