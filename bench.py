@@ -131,48 +131,126 @@ def recorded_traffic():
         return None
 
 
+def bench_config():
+    """The workload both arms report (same keys)."""
+    return {"workload": WORKLOAD, "batch": B, "heads": H, "latent": DL, "rope": DR, "context": T,
+            "step": "quantize-append of the new token + MLA decode (+ split-K combine)",
+            "l2": "inputs larger than L2: 167.8 MB of KV per step, two cache copies rotated"}
+
+
+def calib_batch_law(gen, dev, shape=(4, H, 2048, 192), nu=3):
+    """A calibration batch of the calibration-at-scale workload's law, drawn on the
+    GPU: Student-t with nu = 3 (a normal over the root of a chi-square of three
+    squared normals / 3), each head scaled by its own log-uniform sigma in [0.1, 10]."""
+    import torch
+    z = torch.randn(shape, generator=gen, device=dev)
+    chi2 = sum(torch.randn(shape, generator=gen, device=dev) ** 2 for _ in range(nu))
+    sig = torch.exp(torch.empty(shape[1], device=dev).uniform_(math.log(0.1), math.log(10.0), generator=gen))
+    return (z * torch.rsqrt(chi2 / nu) * sig[None, :, None, None]).to(torch.bfloat16)
+
+
 # ------------------------------------------------------------------ CPU oracle arm
-def oracle_sample(seconds_hint=20.0):
-    """Time the CPU oracle on a bounded sample: whole sequences of the same shape."""
-    import workloads as W
-    from oracle import fa3_oracle as O
-    w = W.mla_dsv3(B=2, T=T)
-    inp = W.mla_inputs(w, with_calib=False)
-    rng = np.random.default_rng(1)
-    q_scale = rng.uniform(0.02, 0.04, H).astype(np.float32)
-    kv_scale = np.float32(np.abs(inp.ckv).max() / 127)
-    ckv8 = O.quantize(inp.ckv, kv_scale)
-    done, t0 = 0, time.perf_counter()
-    while True:
-        b = done % w.B
-        O.mla_decode(inp.q[b:b + 1], ckv8[b:b + 1], inp.krope[b:b + 1], q_scale, float(kv_scale),
-                     inp.lens[b:b + 1], w.softmax_scale)
-        done += 1
-        el = time.perf_counter() - t0
-        if el > seconds_hint or done >= 8:
-            break
-    return done / el, done, el
+class OracleSample:
+    """The CPU oracle on whole decode sequences of the workload's shape (1 query
+    token x 128 heads over 8192 cached tokens).  Four seeded sequences are drawn
+    once and reused (the oracle's cost does not depend on the values)."""
+
+    N_DISTINCT = 4
+
+    def __init__(self):
+        import workloads as W
+        from oracle import fa3_oracle as O
+        self.O = O
+        w = W.mla_dsv3(B=self.N_DISTINCT, T=T)
+        self.w = w
+        self.inp = W.mla_inputs(w, with_calib=False)
+        rng = np.random.default_rng(1)
+        self.q_scale = rng.uniform(0.02, 0.04, H).astype(np.float32)
+        self.kv_scale = np.float32(np.abs(self.inp.ckv).max() / 127)
+        self.ckv8 = O.quantize(self.inp.ckv, self.kv_scale)
+
+    def one(self, i):
+        b = i % self.N_DISTINCT
+        return self.O.mla_decode(self.inp.q[b:b + 1], self.ckv8[b:b + 1], self.inp.krope[b:b + 1], self.q_scale,
+                                 float(self.kv_scale), self.inp.lens[b:b + 1], self.w.softmax_scale)
+
+    def run(self, n_seq, threads):
+        """Decodes n_seq sequences, `threads` at a time (numpy releases the GIL in its
+        matmuls); returns the elapsed seconds."""
+        from concurrent.futures import ThreadPoolExecutor
+        t0 = time.perf_counter()
+        if threads <= 1:
+            for i in range(n_seq):
+                self.one(i)
+        else:
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                list(ex.map(self.one, range(n_seq)))
+        return time.perf_counter() - t0
+
+
+def _blas_limit(n):
+    """Limits numpy's BLAS threads to n where threadpoolctl is installed."""
+    try:
+        from threadpoolctl import threadpool_limits
+        return threadpool_limits(n), True
+    except Exception:
+        import contextlib
+        return contextlib.nullcontext(), False
+
+
+def cpu_baseline(seconds=8.0):
+    """The oracle timed on the host cores, single-threaded and on every core."""
+    cores = len(os.sched_getaffinity(0))
+    smp = OracleSample()
+    smp.run(1, 1)                                                     # warm
+    lim, limited = _blas_limit(1)
+    with lim:
+        n1, el1 = 0, 0.0
+        while el1 < seconds / 2 and n1 < 16:
+            el1 += smp.run(1, 1)
+            n1 += 1
+    nall, elall = 0, 0.0
+    while elall < seconds / 2 and nall < 8 * B:
+        elall += smp.run(B, cores)
+        nall += B
+    single = {"value": n1 / el1, "unit": "tokens/s", "cores": 1,
+              "sample": f"{n1} sequences one after another in {el1:.1f} s"
+                        + ("" if limited else " (numpy's BLAS threads not limited: threadpoolctl absent; the "
+                                              "int64 latent matmul, most of the work, is single-threaded)")}
+    return {"value": nall / elall, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nall} whole decode sequences of the workload's shape (1 token x 128 heads x 8192 ctx) in "
+                      f"{elall:.1f} s, {cores} sequences at a time on {cores} threads, numpy",
+            "single_thread": single}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    per_step = []
-    for _ in range(args.warmup + args.steps):
-        rate, n, el = oracle_sample(seconds_hint=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
-        per_step.append((rate, n, el))
-    timed = per_step[args.warmup:]
-    rate = sum(n for _, n, _ in timed) / sum(el for _, _, el in timed)
     cores = len(os.sched_getaffinity(0))
+    smp = OracleSample()
+    # a step is the workload's 32 sequences, fewer if W + K whole steps would take
+    # more than about two minutes; the line states how many were timed per step
+    par = min(B, cores)
+    t1 = smp.run(par, cores) / par                                   # seconds per sequence, all cores busy
+    n_seq = B
+    while n_seq > 1 and (args.warmup + args.steps) * max(n_seq, par) * t1 * 1.2 > 120.0:
+        n_seq //= 2
+    for _ in range(args.warmup):
+        smp.run(n_seq, cores)
+    el = [smp.run(n_seq, cores) for _ in range(args.steps)]
+    total = sum(el)
+    rate = n_seq * args.steps / total
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / rate * B,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "sequences_per_step": n_seq,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8 codes, f64 arithmetic",
-        "data": "synthetic", "config": {"workload": WORKLOAD},
+        "data": "synthetic", "config": bench_config(),
         "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "whole decode sequences (1 query token x 128 heads over 8192 cached tokens) "
-                                   "of the same shape, one at a time, numpy"},
+                         "sample": f"each step decodes {n_seq} whole sequences of the workload's shape (1 query "
+                                   f"token x 128 heads over 8192 cached tokens), {cores} at a time on {cores} "
+                                   f"threads, numpy; ms_per_step is the measured time of such a step"},
         "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -228,7 +306,7 @@ def run_gpu(args):
     qmn = torch.full((H,), float("inf"), device=dev); qmx = torch.full((H,), float("-inf"), device=dev)
     kmn = torch.full((1,), float("inf"), device=dev); kmx = torch.full((1,), float("-inf"), device=dev)
     # big calibration batch (B=4, H=128, S=2048, D=192 bf16) for the calibration throughput figure
-    cal_big = (torch.randn(4, H, 2048, 192, generator=gen, device=dev) * 2).to(torch.bfloat16)
+    cal_big = calib_batch_law(gen, dev)
     cmn = torch.full((H,), float("inf"), device=dev); cmx = torch.full((H,), float("-inf"), device=dev)
     for _ in range(3):
         F.calibrate_perhead(cal_big, 0.9999, cmn, cmx)
@@ -392,18 +470,13 @@ def run_gpu(args):
     traffic = recorded_traffic()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        rate, n, el = oracle_sample(seconds_hint=args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": f"{n} whole decode sequences of the same shape (1 token x 128 heads x 8192 ctx), "
-                         f"{el:.1f} s, numpy (int64 matmul single-threaded, float64 BLAS threads)"}
+        cpu = cpu_baseline(seconds=args.cpu_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "i8 KV codes; f16 tensor-core MMA (exact integer latent partials); f32 softmax/accum",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": B, "heads": H, "latent": DL, "rope": DR, "context": T,
-                   "step": "quantize-append of the new token + MLA decode (+ split-K combine)",
-                   "l2": "inputs larger than L2: 167.8 MB of KV per step, two cache copies rotated"},
+        "config": bench_config(),
         "kv_gbs": kv_gbs, "kv_hbm_frac_of_measured": kv_gbs / hbm,
         "roofline": {"bound": "tensor", "achieved": k_tflops, "peak": bf16, "unit": "TFLOP/s",
                      "frac": k_tflops / bf16, "traffic": traffic,
@@ -421,7 +494,8 @@ def run_gpu(args):
         "decode_call": {"ms": mla_ms, "kv_gbs": kv_gbs, "tflops": flops_per_step() / (mla_ms / 1e3) / 1e12,
                         "kernels": "query pre-pass + mla_decode_kernel + split-K combine",
                         "timing": "CUDA events around the call, second timed pass"},
-        "calibration": {"workload": "B=4 H=128 S=2048 D=192 bf16, ratio 0.9999", "ms_per_batch": cal_ms,
+        "calibration": {"workload": "B=4 H=128 S=2048 D=192 bf16, ratio 0.9999, Student-t nu=3 x per-head "
+                                    "log-uniform [0.1, 10] sigma", "ms_per_batch": cal_ms,
                         "gbs": 4 * H * 2048 * 192 * 2 / (cal_ms / 1e3) / 1e9},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -498,7 +572,7 @@ def run_kernel(args):
         fn = lambda: F.decode_attn_gqa(q8, kc, vc, s1, s2, s2, lens, 1 / math.sqrt(128))
         unit = ("KV GB/s", Bq * Tq * Hkv * D * 2)
     elif k == "calib":
-        x = (torch.randn(4, H, 2048, 192, device=dev, generator=g) * 2).to(torch.bfloat16)
+        x = calib_batch_law(g, dev)
         mn, mx = torch.full((H,), float("inf"), device=dev), torch.full((H,), float("-inf"), device=dev)
         fn = lambda: F.calibrate_perhead(x, 0.9999, mn, mx)
         unit = ("GB/s", x.numel() * 2)
@@ -533,7 +607,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--kernel", choices=["mla", "mla_paged", "gqa", "gqa_paged", "calib", "append"],
                     help="run one kernel alone (for profiling) instead of the benchmark step")
     ap.add_argument("--t-new", type=int, default=64, help="new tokens per sequence for --kernel append")

@@ -83,12 +83,15 @@ int fa3_set_kernel_timing(void* start_event, void* stop_event);
  * Step 2 (Recall Window): sort the N values, target_num = int(ratio * N)
  *   (float64 product, truncated, at least 1), and among the windows
  *   [sorted[i], sorted[i + target_num - 1]], i = 0 .. N - target_num, take
- *   the narrowest (width computed in float64; ties -> smallest i).
+ *   the narrowest (exact width: the true difference of the two values, not
+ *   a rounded one; ties -> smallest i).
  * Step 3: min_io[h] = min(min_io[h], lo[h]), max_io[h] = max(max_io[h], hi[h]).
  *   -0.0 orders before +0.0 in both the sort and the min/max.
  *
  * x        bf16 values; element (b, h, l) at x[b*stride_b + h*stride_h + l]
- *          (strides in elements; l is contiguous).  Values must be finite.
+ *          (strides in elements; l is contiguous).  Values must be finite and
+ *          of magnitude below 2^127, so that every window width is below the
+ *          largest float (not checked).
  * B, H, L  B >= 1, 1 <= H, L >= 1, B*L < 2^32.
  * ratio    in (0, 1]; the pages' default is 0.9999.
  * min_io, max_io  float[H], in/out.  Initialise to +inf / -inf before the

@@ -5,20 +5,19 @@
 // reads them directly; deq_scale restores floating point.  Scales are the
 // per-head symmetric ones of msModelSlim "FA3量化" 原理 / 算法流程 step 4.
 //
-// The path is HBM-bound (about 16 operations per KV byte), so the design keeps
-// every KV byte on its way from HBM to the tensor pipe in registers:
+// The path is HBM-bound (about 16 operations per KV byte):
 //   * grid = (split, kv head g, batch b); 4 warps per CTA, each warp walking
 //     16-token steps of the CTA's token range with its own online softmax;
-//   * scores  S^T[16 tok x 8 heads] = K[16 x 128] . Q^T  as m16n8k16 f16 MMAs:
-//     int8 codes are exact in fp16 and 128-term sums of products < 2^24 are
-//     exact in the fp32 accumulator, so the score is the exact integer dot;
-//     the contraction order is permuted so that each thread converts 4
-//     contiguous K bytes per k-step (Q is permuted the same way);
+//   * each warp streams its steps through a 2-stage cp.async ring in shared
+//     memory (K then V rows, 16-byte chunks swizzled so that the fragment loads
+//     are free of bank conflicts);
+//   * scores  S^T[16 tok x 8 heads] = K[16 x 128] . Q^T  as exact integer
+//     m16n8k32 s8 MMAs (s32 accumulate); the contraction order is permuted so
+//     that each thread's K and Q words are the bytes it already holds;
 //   * P^T (fp16) comes from the score fragment by movmatrix.trans;
-//   * O^T[128 x 8] += V^T . P^T, the 16 output dims of a thread contiguous so
-//     every thread loads 16 contiguous V bytes per token; V enters the f16 MMA as
-//     code + 1152 (two byte permutes per four codes, no subtraction), and the bias
-//     times the row sum of P is taken off once at the end;
+//   * O^T[128 x 8] += V^T . P^T as m16n8k16 f16 MMAs; V enters as code + 1152
+//     (two byte permutes per four codes, no subtraction), and the bias times the
+//     row sum of P is taken off once at the end;
 //   * split-K partials (unnormalised O, running max m, sum l) are merged by a
 //     small combine kernel with log-sum-exp weights.
 #include "fa3_common.cuh"
@@ -27,6 +26,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <atomic>
 
 namespace fa3 {
 namespace {
@@ -506,8 +506,10 @@ constexpr size_t kGqaStaticScratchBytes = size_t(8) << 20;   // 8 MiB
 static __device__ __align__(256) unsigned char g_gqa_static_scratch[kGqaStaticScratchBytes];
 
 // Device address of the array, looked up once per device.  In host code the
-// array's name is only a host-side stand-in, never a device address.
-void* g_gqa_static_scratch_addr[64] = {nullptr};
+// array's name is only a host-side stand-in, never a device address.  Atomic
+// slots: two host threads making their first call at once may both look the
+// address up, and both store the same value.
+std::atomic<void*> g_gqa_static_scratch_addr[64];
 }  // namespace
 }  // namespace fa3
 
@@ -521,13 +523,13 @@ FA3_API int fa3_decode_attn_gqa_noalloc(const int8_t* q, const int8_t* k, const 
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA3_ECUDA;
   const size_t need = fa3_gqa_workspace_size(B, Hq, Hkv, D, T_max);
   if (need > kGqaStaticScratchBytes) return FA3_EWORKSPACE;   // beyond the fixed 8 MiB scratch
-  if (g_gqa_static_scratch_addr[dev] == nullptr) {
+  void* scratch = g_gqa_static_scratch_addr[dev].load(std::memory_order_acquire);
+  if (scratch == nullptr) {
     // Set-up, once per device, with that device current.
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_gqa_static_scratch) != cudaSuccess || ptr == nullptr) return FA3_ECUDA;
-    g_gqa_static_scratch_addr[dev] = ptr;
+    if (cudaGetSymbolAddress(&scratch, g_gqa_static_scratch) != cudaSuccess || scratch == nullptr) return FA3_ECUDA;
+    g_gqa_static_scratch_addr[dev].store(scratch, std::memory_order_release);
   }
   // Every slot of the partials is written before it is read, so nothing needs clearing.
   return fa3_decode_attn_gqa(q, k, v, q_scale, k_scale, v_scale, lens, out, B, Hq, Hkv, D, T_max, softmax_scale,
-                             g_gqa_static_scratch_addr[dev], kGqaStaticScratchBytes, dev_err, stream);
+                             scratch, kGqaStaticScratchBytes, dev_err, stream);
 }

@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+from collections import OrderedDict
 from typing import Optional
 
 import torch
@@ -100,7 +101,18 @@ def _need_contig(t: torch.Tensor, dtype, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
-_ws_cache = {}
+# Cached scratch buffers, one per (call kind, device, stream), at most
+# _WS_PER_KIND streams per (call kind, device): the least recently used entry is
+# dropped when another stream needs one.  Callers that manage memory themselves
+# pass workspace= explicitly and the cache is never touched.
+_ws_cache: "OrderedDict" = OrderedDict()
+_WS_PER_KIND = 4
+
+
+def _ws_key(key, device, stream=None):
+    dev = device.index if device.index is not None else torch.cuda.current_device()
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    return (key, dev, s.cuda_stream), s
 
 
 def _workspace(key, nbytes: int, device, zero: bool = False, stream=None) -> Optional[torch.Tensor]:
@@ -109,15 +121,22 @@ def _workspace(key, nbytes: int, device, zero: bool = False, stream=None) -> Opt
     (and zeroed) on that stream, so its first use is ordered after the fill."""
     if nbytes == 0:
         return None
-    dev = device.index if device.index is not None else torch.cuda.current_device()
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
-    k = (key, dev, s.cuda_stream)
+    k, s = _ws_key(key, device, stream)
     ws = _ws_cache.get(k)
     if ws is None or ws.numel() < nbytes:
         with torch.cuda.stream(s):
             ws = (torch.zeros if zero else torch.empty)(nbytes, dtype=torch.uint8, device=device)
         _ws_cache[k] = ws
+        same = [c for c in _ws_cache if c[:2] == k[:2]]
+        for old in same[:-_WS_PER_KIND]:
+            if old != k:
+                del _ws_cache[old]
+    _ws_cache.move_to_end(k)
     return ws
+
+
+def _forget_workspace(key, device, stream=None) -> None:
+    _ws_cache.pop(_ws_key(key, device, stream)[0], None)
 
 
 # --------------------------------------------------------------------- calls
@@ -158,10 +177,14 @@ def calibrate_perhead(x: torch.Tensor, ratio: float, min_io: torch.Tensor, max_i
     if min_io.numel() != H or max_io.numel() != H:
         raise ValueError("min_io/max_io must hold H values")
     nbytes = calibrate_workspace_size(H)
-    if workspace is None:
+    cached = workspace is None
+    if cached:
         workspace = _workspace("calib", nbytes, x.device, zero=True, stream=stream)
     st = lib().fa3_calibrate_perhead(_ptr(x), B, H, L, sb, sh, float(ratio), _ptr(min_io), _ptr(max_io),
                                      _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != 0 and cached:
+        # The key counts may not have been cleared: never hand this buffer out again.
+        _forget_workspace("calib", x.device, stream)
     _check("fa3_calibrate_perhead", st)
 
 
