@@ -571,6 +571,18 @@ def run_kernel(args):
         lens = torch.full((Bq,), Tq, dtype=torch.int32, device=dev)
         fn = lambda: F.decode_attn_gqa(q8, kc, vc, s1, s2, s2, lens, 1 / math.sqrt(128))
         unit = ("KV GB/s", Bq * Tq * Hkv * D * 2)
+    elif k == "prefill":
+        # Llama-3.1-70B-shaped causal prefill: S = T new rows per sequence, 64 / 8 heads
+        Bp, S_, Hq, Hkv, D = args.prefill_batch, args.prefill_len, 64, 8, 128
+        q8 = torch.randint(-127, 128, (Bp, S_, Hq, D), dtype=torch.int8, device=dev, generator=g)
+        kc = torch.randint(-127, 128, (Bp, S_, Hkv, D), dtype=torch.int8, device=dev, generator=g)
+        vc = torch.randint(-127, 128, (Bp, S_, Hkv, D), dtype=torch.int8, device=dev, generator=g)
+        s1, s2 = torch.full((Hq,), 0.003, device=dev), torch.full((Hkv,), 0.003, device=dev)
+        ql = torch.full((Bp,), S_, dtype=torch.int32, device=dev)
+        out = torch.empty(Bp, S_, Hq, D, dtype=torch.bfloat16, device=dev)
+        fn = lambda: F.prefill_attn_gqa(q8, kc, vc, s1, s2, s2, ql, ql, 1 / math.sqrt(128), out=out)
+        # causal: row i sees i + 1 keys; 2 contractions of 2*D flop per (row, head, key)
+        unit = ("TFLOP/s", Bp * Hq * (S_ * (S_ + 1) // 2) * 4 * D / 1e3)
     elif k == "calib":
         x = calib_batch_law(g, dev)
         mn, mx = torch.full((H,), float("inf"), device=dev), torch.full((H,), float("-inf"), device=dev)
@@ -608,7 +620,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--kernel", choices=["mla", "mla_paged", "gqa", "gqa_paged", "calib", "append"],
+    ap.add_argument("--prefill-len", type=int, default=4096, help="S = T for --kernel prefill")
+    ap.add_argument("--prefill-batch", type=int, default=2, help="sequences for --kernel prefill")
+    ap.add_argument("--kernel", choices=["mla", "mla_paged", "gqa", "gqa_paged", "calib", "append", "prefill"],
                     help="run one kernel alone (for profiling) instead of the benchmark step")
     ap.add_argument("--t-new", type=int, default=64, help="new tokens per sequence for --kernel append")
     args = ap.parse_args()

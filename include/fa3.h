@@ -65,9 +65,10 @@ const char* fa3_status_string(int status);
 int fa3_version(void);
 
 /* Measurement aid (no counterpart in the pages).  When both events are
- * non-NULL, every later call of fa3_decode_attn_mla, fa3_decode_attn_gqa and
- * fa3_calibrate_perhead records start_event on its stream just before its
- * main kernel (the MLA decode, the GQA decode, the calibration histogram) and
+ * non-NULL, every later call of fa3_decode_attn_mla, fa3_decode_attn_gqa,
+ * fa3_prefill_attn_gqa and fa3_calibrate_perhead records start_event on its
+ * stream just before its main kernel (the MLA decode, the GQA decode, the
+ * prefill attention, the calibration histogram) and
  * stop_event just after it, so that the caller can time that kernel alone
  * (cudaEventElapsedTime).  The events are cudaEvent_t passed as void*, owned
  * by the caller and must outlive their use; NULL, NULL turns this off.  One
@@ -192,6 +193,34 @@ int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v,
                         const int32_t* lens, uint16_t* out, int B, int Hq, int Hkv, int D, int T_max,
                         float softmax_scale, void* workspace, size_t workspace_bytes,
                         int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Prefill-phase GQA attention with INT8 q, k and v -- MindIE "Attention
+ * Quantization", Overview, and MindIE Turbo "Attention量化" (q, k, v all 8-bit
+ * with per-head scales; deq_scale restores floating point); at long sequence
+ * lengths these activations dominate memory (msModelSlim "FA3量化", 简介).
+ *
+ * The q_lens[b] new rows of sequence b are the last tokens of its kv_lens[b]-
+ * token context (kv_lens[b] - q_lens[b] cached tokens, then the new rows); new
+ * row i sits at position pos = kv_lens[b] - q_lens[b] + i and attends causally
+ * to keys 0 .. pos.  Query head h reads KV head g = h / (Hq / Hkv):
+ *   s[t] = (q[b, i, h] . k[b, t, g]) * q_scale[h] * k_scale[g] * softmax_scale
+ *   out[b, i, h, :] = bf16( v_scale[g] * sum_{t <= pos} softmax(s)_t * v[b, t, g, :] )
+ *
+ * q        int8 [B][S][Hq][D] (rows i >= q_lens[b] are not read).
+ * k, v     int8 [B][T][Hkv][D] (rows t >= kv_lens[b] are not read).
+ * q_scale  float[Hq];  k_scale, v_scale  float[Hkv].
+ * q_lens, kv_lens  int32[B]; 0 <= q_lens[b] <= S and q_lens[b] <= kv_lens[b] <= T,
+ *          otherwise FA3_DEVERR_LENS is set and sequence b is skipped.
+ * out      bf16 [B][S][Hq][D]; rows i >= q_lens[b] are left untouched.
+ * Supported: D = 128, Hq / Hkv dividing 128; 16-byte aligned q, k, v, out.
+ * No workspace.
+ * ------------------------------------------------------------------------ */
+int fa3_prefill_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v,
+                         const float* q_scale, const float* k_scale, const float* v_scale,
+                         const int32_t* q_lens, const int32_t* kv_lens, uint16_t* out,
+                         int B, int S, int T, int Hq, int Hkv, int D, float softmax_scale,
+                         int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * Allocation-free GQA decode.  No counterpart in the pages: a convenience for

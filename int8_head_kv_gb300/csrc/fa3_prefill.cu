@@ -1,0 +1,396 @@
+// Prefill-phase GQA attention with INT8 q, k and v (tcgen05, sm_103a).
+//
+// MindIE "Attention Quantization", Overview, and MindIE Turbo "Attention量化":
+// q, k and v are quantized to 8 bits with per-head scales (msModelSlim "FA3量化"
+// 原理 / 算法流程 step 4) and the attention operator consumes the codes; at long
+// sequence lengths these activations dominate memory (msModelSlim "FA3量化",
+// 简介).  The prefill phase attends the q_len new rows of a sequence, the last
+// q_len tokens of its kv_len-token context, causally:
+//
+//   s[i, h, t] = (q8[i, h] . k8[t, g]) * q_scale[h] * k_scale[g] * softmax_scale,
+//                t <= pos(i) = kv_len - q_len + i,   g = h / (Hq / Hkv)
+//   out[i, h]  = bf16( v_scale[g] * sum_t softmax(s[i, h, :])_t * v8[t, g] )
+//
+// The contraction is dense (2 * 2 * D FLOP per (row, key) pair), so the kernel
+// is built around the tensor pipe:
+//   * one CTA per (block of 128 rows, KV head g, sequence b); its 128 rows are
+//     P = 128 / G query positions x the G query heads of the group, so every K/V
+//     tile feeds the whole group (row r = TMEM lane r: position r / G, head r % G);
+//   * int8 codes are exact in fp16 and a 128-term sum of their products stays
+//     below 2^24, so kind::f16 MMAs with fp32 accumulation give the exact integer
+//     score (sm_103a has no integer tcgen05 kind);
+//   * warp 0 issues the MMAs; warps 1-3 load 128-token int8 K and V tiles into
+//     registers one tile ahead and write them as fp16 core matrices into one of
+//     two shared-memory stages (K-major for Q.K^T, MN-major for P.V); warps 4-7
+//     own one row each for the online softmax;
+//   * TMEM: O [0,128), S double-buffered [128,384), the fp16 query codes as the
+//     A operand of Q.K^T [384,448); S(j+2) is computed while the softmax works
+//     on S(j+1) and P(j).V(j) runs;
+//   * the softmax writes P (fp16, unnormalised, relative to a lazily moved row
+//     maximum) into shared memory as the K-major A operand of P.V, sums the same
+//     fp16 weights for the row's normaliser (so the output is a weighted mean of
+//     V whatever the rounding of P), and rescales O in TMEM only when a row's
+//     maximum grows by more than 8 (log2 units);
+//   * blocks run longest first (the last positions see the most keys).
+// Every wait is bounded; on time-out the kernel sets FA3_DEVERR_TIMEOUT, drains
+// its MMAs, frees its TMEM and returns.
+#include "fa3_common.cuh"
+#include "fa3_tc.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+namespace fa3 {
+namespace {
+
+constexpr int kD = 128;            // head dim
+constexpr int kKeys = 128;         // keys per tile
+constexpr int kRowsP = 128;        // rows (TMEM lanes) per CTA
+constexpr int kThreadsP = 256;     // warp 0: MMA, warps 1-3: converters, warps 4-7: softmax
+constexpr int kConvP = 96;
+constexpr uint32_t TMP_O = 0, TMP_S = 128, TMP_Q = 384;
+constexpr uint32_t KV_TILE = kKeys * kD * 2;           // 32 KB of fp16
+constexpr uint32_t OFFP_K = 0;                         // 2 stages
+constexpr uint32_t OFFP_V = OFFP_K + 2 * KV_TILE;      // 2 stages
+constexpr uint32_t OFFP_P = OFFP_V + 2 * KV_TILE;      // fp16 P, 128 rows x 128 keys (32 KB)
+constexpr uint32_t OFFP_BAR = OFFP_P + kRowsP * kKeys * 2;
+enum { PB_KV_FULL = 0, PB_KV_EMPTY = 2, PB_S_FULL = 4, PB_S_EMPTY = 6, PB_P_FULL = 8, PB_PV_DONE = 9,
+       PB_Q_READY = 10, PB_DRAIN = 11, PB_N = 12 };
+constexpr uint32_t OFFP_TSLOT = OFFP_BAR + 8 * PB_N;
+constexpr uint32_t OFFP_ABORT = OFFP_TSLOT + 4;
+constexpr uint32_t SMEM_PREFILL = OFFP_BAR + 256 + 1024;   // + alignment slack
+static_assert(OFFP_ABORT + 4 <= OFFP_BAR + 256, "barrier area");
+static_assert(SMEM_PREFILL <= 232448, "shared memory");
+
+struct PrefillParams {
+  const int8_t* q;         // [B][S][Hq][128]
+  const int8_t* k;         // [B][T][Hkv][128]
+  const int8_t* v;
+  const float* q_scale;    // [Hq]
+  const float* k_scale;    // [Hkv]
+  const float* v_scale;
+  const int32_t* q_lens;   // [B]
+  const int32_t* kv_lens;  // [B]
+  uint16_t* out;           // bf16 [B][S][Hq][128]
+  int32_t* err;
+  int B, S, T, Hq, Hkv, G, P;
+  float sm_log2;           // softmax_scale * log2(e)
+};
+
+__global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rb = (int)gridDim.x - 1 - (int)blockIdx.x;      // longest blocks first
+  const int g = blockIdx.y, b = blockIdx.z;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFFP_ABORT);
+  auto bar = [&](int i) { return sbase + OFFP_BAR + 8u * (uint32_t)i; };
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int nq = p.q_lens[b], nkv = p.kv_lens[b];
+  if (nq < 0 || nq > p.S || nkv < nq || nkv > p.T) {
+    if (rb == 0 && g == 0 && tid == 0) set_dev_err(p.err, FA3_DEVERR_LENS);
+    return;
+  }
+  const int i0 = rb * p.P;
+  if (i0 >= nq) return;                                    // no row of this block is a new row
+  const int prefix = nkv - nq;
+  const int n_keys = prefix + min(nq, i0 + p.P);           // keys up to the block's last position
+  const int nt = (n_keys + kKeys - 1) / kKeys;
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(PB_KV_FULL + s), kConvP);
+      mbar_init(bar(PB_KV_EMPTY + s), 1);
+      mbar_init(bar(PB_S_FULL + s), 1);
+      mbar_init(bar(PB_S_EMPTY + s), 4);
+    }
+    mbar_init(bar(PB_P_FULL), 4);
+    mbar_init(bar(PB_PV_DONE), 1);
+    mbar_init(bar(PB_Q_READY), 4);
+    mbar_init(bar(PB_DRAIN), 1);
+    *abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(sbase + OFFP_TSLOT), "r"(512) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + OFFP_TSLOT);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_f16(kRowsP, kKeys, false, false);
+      const uint32_t id_pv = idesc_f16(kRowsP, kD, false, true);
+      bool ok = wait_bar(bar(PB_Q_READY), 0, abort_flag, p.err);
+      // S[j % 2] = Q . K_j^T; K is the K-major B operand (8-token core groups 128 B
+      // apart, 8-wide d groups 2048 B apart).
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j & 1;
+        if (!(wait_bar(bar(PB_KV_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err) &&
+              wait_bar(bar(PB_S_EMPTY + s), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, p.err)))
+          return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t bd = sdesc(sbase + OFFP_K + s * KV_TILE + kk * 4096, 2048, 128);
+          mma_f16_ts(tmem + TMP_S + s * 128, tmem + TMP_Q + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(PB_S_FULL + s));
+        return true;
+      };
+      // O += P_j . V_j: P is the K-major A operand, V the MN-major B operand (token
+      // groups 128 B apart, d groups 2048 B apart).  Completion frees P and stage j % 2.
+      auto issue_pv = [&](int j) -> bool {
+        const int s = j & 1;
+        if (!wait_bar(bar(PB_P_FULL), (uint32_t)j & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t a = sdesc(sbase + OFFP_P + kk * 4096, 2048, 128);
+          const uint64_t bd = sdesc(sbase + OFFP_V + s * KV_TILE + kk * 256, 128, 2048);
+          mma_f16(tmem + TMP_O, a, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(PB_PV_DONE));
+        mma_commit(bar(PB_KV_EMPTY + s));
+        return true;
+      };
+      ok = ok && issue_qk(0) && (nt < 2 || issue_qk(1));
+      for (int j = 0; j < nt && ok; ++j) {
+        ok = issue_pv(j);
+        if (ok && j + 2 < nt) ok = issue_qk(j + 2);
+      }
+      // Drain: every MMA issued has completed before TMEM is freed.
+      mma_commit(bar(PB_DRAIN));
+      wait_bar(bar(PB_DRAIN), 0, abort_flag, p.err);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------ int8 -> fp16 converters
+    // A tile is 2 x 128 rows x 8 chunks of 16 bytes (K, then V).  Each group of 32
+    // consecutive units is 16 tokens x 2 chunks, lane l taking token l % 16 and
+    // chunk l / 16: a warp loads 16 full 32-byte sectors and its fp16 stores hit
+    // every bank once per 128 bytes.  fp16 element (token n, d) lands at
+    // (d / 8) * 2048 + n * 16 + (d % 8) * 2.
+    constexpr int kUnits = 2 * kKeys * (kD / 16);                 // 2048
+    constexpr int kPer = (kUnits + kConvP - 1) / kConvP;           // 22
+    const int ct = tid - 32;
+    const int64_t row_stride = (int64_t)p.Hkv * kD;
+    const int8_t* kb = p.k + (int64_t)b * p.T * row_stride + (int64_t)g * kD;
+    const int8_t* vb = p.v + (int64_t)b * p.T * row_stride + (int64_t)g * kD;
+    auto unit = [&](int i, int& kv, int& n, int& cc) {
+      const int u = ct + kConvP * i;
+      const int grp = u >> 5, l = u & 31;                          // grp < 64 for u < kUnits
+      kv = grp >> 5;
+      n = (grp & 7) * 16 + (l & 15);
+      cc = ((grp >> 3) & 3) * 2 + (l >> 4);
+      return u < kUnits;
+    };
+    for (int j = 0; j < nt; ++j) {
+      const int s = j & 1;
+      uint4 w[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        int kv, n, cc;
+        const bool in = unit(i, kv, n, cc);
+        const int t = j * kKeys + n;
+        w[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (in && t < n_keys) w[i] = __ldg(reinterpret_cast<const uint4*>((kv ? vb : kb) + t * row_stride) + cc);
+      }
+      if (!wait_bar(bar(PB_KV_EMPTY + s), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, p.err)) break;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        int kv, n, cc;
+        if (unit(i, kv, n, cc)) {
+          uint8_t* dst = smem + (kv ? OFFP_V : OFFP_K) + s * KV_TILE;
+          uint4 o0, o1;
+          i8x4_to_f16x4(w[i].x, o0.x, o0.y);
+          i8x4_to_f16x4(w[i].y, o0.z, o0.w);
+          i8x4_to_f16x4(w[i].z, o1.x, o1.y);
+          i8x4_to_f16x4(w[i].w, o1.z, o1.w);
+          *reinterpret_cast<uint4*>(dst + (2 * cc) * 2048 + n * 16) = o0;
+          *reinterpret_cast<uint4*>(dst + (2 * cc + 1) * 2048 + n * 16) = o1;
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(bar(PB_KV_FULL + s));
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int r = (warp - 4) * 32 + lane;                  // row == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const int i = i0 + r / p.G, h = g * p.G + r % p.G;
+    const bool active = i < nq;
+    const int pos = active ? prefix + i : -1;               // last key this row sees
+    const float c = active ? p.q_scale[h] * p.k_scale[g] * p.sm_log2 : 0.f;
+    auto warp_arrive = [&](int which) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(which));
+    };
+    // The row's query codes as fp16 pairs in TMEM (column k holds d = 2k, 2k + 1).
+    {
+      uint32_t qw[64];
+      const int8_t* qrow = p.q + (((int64_t)b * p.S + (active ? i : 0)) * p.Hq + h) * kD;
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (active) x = *reinterpret_cast<const uint4*>(qrow + 16 * c16);
+        i8x4_to_f16x4(x.x, qw[8 * c16 + 0], qw[8 * c16 + 1]);
+        i8x4_to_f16x4(x.y, qw[8 * c16 + 2], qw[8 * c16 + 3]);
+        i8x4_to_f16x4(x.z, qw[8 * c16 + 4], qw[8 * c16 + 5]);
+        i8x4_to_f16x4(x.w, qw[8 * c16 + 6], qw[8 * c16 + 7]);
+      }
+      FA3_TMEM_ST32(tmem + lane_base + TMP_Q, qw);
+      FA3_TMEM_ST32(tmem + lane_base + TMP_Q + 32, (qw + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(PB_Q_READY);
+    }
+    float m_run = -CUDART_INF_F, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt && ok; ++j) {
+      const int s = j & 1;
+      if (!warp_all(wait_bar(bar(PB_S_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err))) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t scol = tmem + lane_base + TMP_S + s * 128;
+      // pass 1: the tile's row maximum (log2 units)
+      float mx = -CUDART_INF_F;
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
+        FA3_TMEM_LD32(scol + c4 * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int t = j * kKeys + c4 * 32 + e;
+          mx = fmaxf(mx, t <= pos ? __uint_as_float(v[e]) * c : -CUDART_INF_F);
+        }
+      }
+      const float m_new = fmaxf(m_run, mx);
+      // O and P are free once P.V of the previous tile is done.
+      if (j > 0 && !warp_all(wait_bar(bar(PB_PV_DONE), (uint32_t)(j - 1) & 1u, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // Lazy rescale: the reference maximum moves only when the row maximum grew by more than 8.
+      const bool grow = m_new != -CUDART_INF_F && (m_run == -CUDART_INF_F || m_new > m_run + 8.f);
+      if (__any_sync(0xffffffffu, grow && m_run != -CUDART_INF_F)) {
+        const float f = (grow && m_run != -CUDART_INF_F) ? ex2_approx(m_run - m_new) : 1.f;
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          FA3_TMEM_LD32(tmem + lane_base + TMP_O + c4 * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+          FA3_TMEM_ST32(tmem + lane_base + TMP_O + c4 * 32, v);
+        }
+        tmem_wait_st();
+      }
+      if (grow) {
+        l_run = m_run == -CUDART_INF_F ? 0.f : l_run * ex2_approx(m_run - m_new);
+        m_run = m_new;
+      }
+      // pass 2: P = exp2(s - m_run) as fp16 into shared memory (K-major A operand of P.V)
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
+        FA3_TMEM_LD32(scol + c4 * 32, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int t = j * kKeys + c4 * 32 + e;
+          const float p0 = t <= pos ? ex2_approx(__uint_as_float(v[e]) * c - m_run) : 0.f;
+          const float p1 = t + 1 <= pos ? ex2_approx(__uint_as_float(v[e + 1]) * c - m_run) : 0.f;
+          pk[e / 2] = pack_f16x2(p0, p1);
+          // the row sum of the fp16 weights P.V uses: the output stays a weighted mean of V
+          const float2 pr = __half22float2(*reinterpret_cast<const __half2*>(&pk[e / 2]));
+          l_run += pr.x + pr.y;
+        }
+#pragma unroll
+        for (int k8 = 0; k8 < 4; ++k8)       // 8 keys (16 bytes) per core-matrix row
+          *reinterpret_cast<uint4*>(smem + OFFP_P + (c4 * 4 + k8) * 2048 + r * 16) =
+              make_uint4(pk[4 * k8], pk[4 * k8 + 1], pk[4 * k8 + 2], pk[4 * k8 + 3]);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      warp_arrive(PB_S_EMPTY + s);
+      warp_arrive(PB_P_FULL);
+    }
+    // epilogue: out = v_scale * O / l
+    if (ok && warp_all(wait_bar(bar(PB_PV_DONE), (uint32_t)(nt - 1) & 1u, abort_flag, p.err))) {
+      tc_fence_after();
+      const float inv = (active && l_run > 0.f) ? p.v_scale[g] / l_run : 0.f;
+      uint16_t* orow = p.out + (((int64_t)b * p.S + (active ? i : 0)) * p.Hq + h) * kD;
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
+        FA3_TMEM_LD32(tmem + lane_base + TMP_O + c4 * 32, v);
+        tmem_wait_ld();
+        if (active) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const __nv_bfloat162 bb =
+                __floats2bfloat162_rn(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+            w[e / 2] = *reinterpret_cast<const uint32_t*>(&bb);
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(orow + c4 * 32 + q4 * 8) =
+                make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+  }
+}
+
+}  // namespace
+}  // namespace fa3
+
+using namespace fa3;
+
+FA3_API int fa3_prefill_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale,
+                                 const float* k_scale, const float* v_scale, const int32_t* q_lens,
+                                 const int32_t* kv_lens, uint16_t* out, int B, int S, int T, int Hq, int Hkv, int D,
+                                 float softmax_scale, int32_t* dev_err, void* stream) {
+  if (!q || !k || !v || !q_scale || !k_scale || !v_scale || !q_lens || !kv_lens || !out) return FA3_EINVAL;
+  if (B <= 0 || S <= 0 || T <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return FA3_EINVAL;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return FA3_EINVAL;
+  const int G = Hq / Hkv;
+  if (D != kD || kRowsP % G != 0 || B > 65535 || Hkv > 65535) return FA3_ERANGE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FA3_ERANGE;
+  int sms = 0;
+  const int st = check_device(&sms);
+  if (st != FA3_OK) return st;
+  PrefillParams prm;
+  prm.q = q; prm.k = k; prm.v = v; prm.q_scale = q_scale; prm.k_scale = k_scale; prm.v_scale = v_scale;
+  prm.q_lens = q_lens; prm.kv_lens = kv_lens; prm.out = out; prm.err = dev_err;
+  prm.B = B; prm.S = S; prm.T = T; prm.Hq = Hq; prm.Hkv = Hkv; prm.G = G; prm.P = kRowsP / G;
+  prm.sm_log2 = softmax_scale * 1.4426950408889634f;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaFuncSetAttribute(gqa_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_PREFILL) !=
+      cudaSuccess)
+    return FA3_ECUDA;
+  const dim3 grid((unsigned)((S + prm.P - 1) / prm.P), (unsigned)Hkv, (unsigned)B);
+  timing_begin(s);
+  const cudaError_t le = launch_pdl(gqa_prefill_kernel, grid, dim3(kThreadsP), SMEM_PREFILL, s, prm);
+  timing_end(s);
+  return le == cudaSuccess ? FA3_OK : FA3_ECUDA;
+}

@@ -48,6 +48,7 @@ _SIGS = {
     "fa3_decode_attn_mla": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
     "fa3_gqa_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "fa3_decode_attn_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
+    "fa3_prefill_attn_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "fa3_quantize_append_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
     "fa3_decode_attn_mla_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ,
                                        _P, _P]),
@@ -278,6 +279,32 @@ def decode_attn_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: 
                                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
                                    _ptr(dev_err), _stream(stream))
     _check("fa3_decode_attn_gqa", st)
+    return out
+
+
+def prefill_attn_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: torch.Tensor,
+                     k_scale: torch.Tensor, v_scale: torch.Tensor, q_lens: torch.Tensor, kv_lens: torch.Tensor,
+                     softmax_scale: float, out: Optional[torch.Tensor] = None,
+                     dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal prefill: q int8 [B][S][Hq][D], k/v int8 [B][T][Hkv][D] -> bf16 [B][S][Hq][D].
+
+    Rows i >= q_lens[b] of ``out`` are left untouched (zero-filled when ``out`` is
+    allocated here)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need_contig(t, torch.int8, n)
+    for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need_contig(t, torch.float32, n)
+    _need_contig(q_lens, torch.int32, "q_lens")
+    _need_contig(kv_lens, torch.int32, "kv_lens")
+    B, S, Hq, D = q.shape
+    T, Hkv = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.zeros(B, S, Hq, D, dtype=torch.bfloat16, device=q.device)
+    _need_contig(out, torch.bfloat16, "out")
+    st = lib().fa3_prefill_attn_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                    _ptr(q_lens), _ptr(kv_lens), _ptr(out), B, S, T, Hq, Hkv, D,
+                                    float(softmax_scale), _ptr(dev_err), _stream(stream))
+    _check("fa3_prefill_attn_gqa", st)
     return out
 
 

@@ -375,7 +375,8 @@ def gqa_decode(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, q_scale: np.ndarr
 
 
 def gqa_prefill(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, q_scale: np.ndarray, k_scale: np.ndarray,
-                v_scale: np.ndarray, q_lens: np.ndarray, kv_lens: np.ndarray, softmax_scale: float) -> np.ndarray:
+                v_scale: np.ndarray, q_lens: np.ndarray, kv_lens: np.ndarray, softmax_scale: float,
+                rows: Optional[Iterable[Tuple[int, int]]] = None) -> np.ndarray:
     """Prefill-phase attention with INT8 q, k, v (MindIE "Attention Quantization",
     Overview: q, k and v quantized to 8 bits), the same per-head scales as
     gqa_decode.  Reading where the pages are silent: the q_lens[b] new rows of
@@ -385,7 +386,8 @@ def gqa_prefill(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, q_scale: np.ndar
     position.
 
     q8: [B][S][Hq][D] (rows i >= q_lens[b] ignored), k8, v8: [B][T][Hkv][D].
-    Returns float64 [B][S][Hq][D]; ignored rows are zero.
+    Returns float64 [B][S][Hq][D]; ignored rows are zero.  With ``rows`` =
+    [(b, i), ...] only those rows (all heads) are computed.
     """
     B, S, Hq, D = q8.shape
     Hkv = k8.shape[2]
@@ -393,11 +395,18 @@ def gqa_prefill(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, q_scale: np.ndar
         raise ValueError("Hq must be a multiple of Hkv")
     G = Hq // Hkv
     out = np.zeros((B, S, Hq, D), np.float64)
+    want = None
+    if rows is not None:
+        want = {}
+        for b, i in rows:
+            want.setdefault(int(b), set()).add(int(i))
     for b in range(B):
         nq, nkv = int(q_lens[b]), int(kv_lens[b])
         if nq < 0 or nq > S or nkv < nq or nkv > k8.shape[1]:
             raise ValueError("bad q_lens / kv_lens")
         for i in range(nq):
+            if want is not None and i not in want.get(b, ()):
+                continue
             n = nkv - nq + i + 1                                   # keys 0 .. position of row i
             for h in range(Hq):
                 g = h // G

@@ -77,6 +77,20 @@ def test_gqa_validation(L):
     assert call(Hq=128, Hkv=8) == ERANGE  # 16 query heads per KV head
 
 
+def test_prefill_validation(L):
+    UNALIGNED = ctypes.c_void_p(4096 + 8)
+    call = lambda Hq=64, Hkv=8, D=128, q=FAKE, sc=0.09, out=FAKE, S=64: L.fa3_prefill_attn_gqa(
+        q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, out, 2, S, 64, Hq, Hkv, D, sc, None, None)
+    assert call(q=None) == EINVAL
+    assert call(out=None) == EINVAL
+    assert call(S=0) == EINVAL
+    assert call(sc=float("nan")) == EINVAL
+    assert call(Hq=60) == EINVAL          # not a multiple of Hkv
+    assert call(D=64) == ERANGE
+    assert call(Hq=24, Hkv=8) == ERANGE   # 3 query heads per KV head do not divide 128 rows
+    assert call(q=UNALIGNED) == ERANGE
+
+
 def test_paged_validation(L):
     mla = lambda bt=FAKE, npg=8, ps=64, mp=4: L.fa3_decode_attn_mla_paged(
         FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, bt, FAKE, 2, 128, 512, 64, npg, ps, mp, 0.07, FAKE, 1 << 30, None, None)

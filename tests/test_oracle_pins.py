@@ -478,3 +478,17 @@ def test_prefill_first_row_and_validation():
     with pytest.raises(ValueError):
         O.gqa_prefill(q8, k8, v8, qs, ks, vs, np.array([9, 4]), np.array([8, 6]), 0.3)   # kv_lens < q_lens
 
+
+
+def test_prefill_row_selection_equals_full_rows():
+    q8, k8, v8, qs, ks, vs = _prefill_case(seed=3)
+    q_lens, kv_lens = np.array([9, 4]), np.array([14, 6])
+    full = O.gqa_prefill(q8, k8, v8, qs, ks, vs, q_lens, kv_lens, 0.25)
+    rows = [(0, 0), (0, 8), (1, 3)]
+    part = O.gqa_prefill(q8, k8, v8, qs, ks, vs, q_lens, kv_lens, 0.25, rows=rows)
+    for b, i in rows:
+        assert np.array_equal(part[b, i], full[b, i])
+    mask = np.zeros(part.shape[:2], bool)
+    for b, i in rows:
+        mask[b, i] = True
+    assert not part[~mask].any()

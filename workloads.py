@@ -30,7 +30,7 @@ import torch
 
 # Stream tags so that every tensor of a workload has its own random stream.
 TAG_Q, TAG_CKV, TAG_KROPE, TAG_K, TAG_V, TAG_LENS, TAG_SIGMA, TAG_CALIB_Q, TAG_CALIB_KV, \
-    TAG_CALIB_K, TAG_CALIB_V, TAG_POS, TAG_APPEND = range(13)
+    TAG_CALIB_K, TAG_CALIB_V, TAG_POS, TAG_APPEND, TAG_PREFILL = range(14)
 
 
 def rng_for(seed: int, tag: int, k: int = 0, *more: int) -> np.random.Generator:
@@ -234,6 +234,67 @@ def gqa_inputs(w: GQAWorkload, with_calib: bool = True) -> GQAInputs:
             cv.append(bf16_round(student_t(rng_for(s, TAG_CALIB_V, kk), (1, w.Hkv, w.calib_S, w.D), w.nu,
                                            sv[None, :, None, None])))
     return GQAInputs(q=q, k=k, v=v, lens=lens, calib_q=cq, calib_k=ck, calib_v=cv)
+
+
+# ----------------------------------------------------------------------------
+# GQA prefill workloads (the Llama-3.1-70B GQA law over S new rows)
+# ----------------------------------------------------------------------------
+@dataclass
+class PrefillWorkload:
+    name: str
+    B: int
+    S: int                      # rows of the q / out arrays
+    T: int                      # rows of the k / v arrays
+    Hq: int
+    Hkv: int
+    D: int
+    softmax_scale: float
+    q_lens: Sequence[int]
+    kv_lens: Sequence[int]
+    nu: float = 4.0
+    sigma: Tuple[float, float] = (0.05, 5.0)
+    calib_S: int = 512
+    ratio: float = 0.9999
+    seed: int = 0
+
+
+def prefill_llama70b(B: int = 1, S: int = 4096, T: int = 4096, Hq: int = 64, Hkv: int = 8,
+                     q_lens: Optional[Sequence[int]] = None, kv_lens: Optional[Sequence[int]] = None,
+                     seed: int = 0) -> PrefillWorkload:
+    """Llama-3.1-70B-shaped prefill (64 query heads, 8 KV heads, head_dim 128): by
+    default every sequence attends S new rows over a T-token context."""
+    ql = list(q_lens) if q_lens is not None else [S] * B
+    kl = list(kv_lens) if kv_lens is not None else [T] * B
+    return PrefillWorkload(name=f"llama70b-prefill b{B} s{S} t{T} hq{Hq} hkv{Hkv} d128", B=B, S=S, T=T, Hq=Hq,
+                           Hkv=Hkv, D=128, softmax_scale=1.0 / math.sqrt(128.0), q_lens=ql, kv_lens=kl, seed=seed)
+
+
+@dataclass
+class PrefillInputs:
+    q: np.ndarray   # [B][S][Hq][D] bf16-exact float32
+    k: np.ndarray   # [B][T][Hkv][D]
+    v: np.ndarray   # [B][T][Hkv][D]
+    calib_q: List[np.ndarray]   # (1, Hq, calib_S, D)
+    calib_k: List[np.ndarray]   # (1, Hkv, calib_S, D)
+    calib_v: List[np.ndarray]
+
+
+def prefill_inputs(w: PrefillWorkload) -> PrefillInputs:
+    """Student-t (nu) activations, each head scaled by its own log-uniform sigma;
+    one calibration batch per tensor drawn from the same law."""
+    s = w.seed
+    sq = log_uniform(rng_for(s, TAG_PREFILL, 0), *w.sigma, size=w.Hq).astype(np.float32)
+    sk = log_uniform(rng_for(s, TAG_PREFILL, 1), *w.sigma, size=w.Hkv).astype(np.float32)
+    sv = log_uniform(rng_for(s, TAG_PREFILL, 2), *w.sigma, size=w.Hkv).astype(np.float32)
+    q = bf16_round(student_t(rng_for(s, TAG_PREFILL, 3), (w.B, w.S, w.Hq, w.D), w.nu, sq[None, None, :, None]))
+    k = bf16_round(student_t(rng_for(s, TAG_PREFILL, 4), (w.B, w.T, w.Hkv, w.D), w.nu, sk[None, None, :, None]))
+    v = bf16_round(student_t(rng_for(s, TAG_PREFILL, 5), (w.B, w.T, w.Hkv, w.D), w.nu, sv[None, None, :, None]))
+    cq = [bf16_round(student_t(rng_for(s, TAG_PREFILL, 6), (1, w.Hq, w.calib_S, w.D), w.nu, sq[None, :, None, None]))]
+    ck = [bf16_round(student_t(rng_for(s, TAG_PREFILL, 7), (1, w.Hkv, w.calib_S, w.D), w.nu,
+                               sk[None, :, None, None]))]
+    cv = [bf16_round(student_t(rng_for(s, TAG_PREFILL, 8), (1, w.Hkv, w.calib_S, w.D), w.nu,
+                               sv[None, :, None, None]))]
+    return PrefillInputs(q=q, k=k, v=v, calib_q=cq, calib_k=ck, calib_v=cv)
 
 
 # ----------------------------------------------------------------------------
