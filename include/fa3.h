@@ -111,6 +111,19 @@ int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L,
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Running-range merge -- msModelSlim FA3量化, 原理 / 算法流程 step 3 applied to
+ * R ranges at once (e.g. the ranges that R ranks computed on their shares of
+ * the calibration batches, gathered by the caller's collective):
+ *   min_io[h] = min(min_io[h], mins[r][h]),  max_io[h] = max(max_io[h], maxs[r][h])
+ * over r = 0 .. R-1, in IEEE totalOrder (-0.0 below +0.0).  min and max are
+ * associative and commutative, so sharding the batches over ranks and merging
+ * gives the same bits as accumulating every batch in one process.
+ * mins, maxs  float [R][H], device;  min_io, max_io  float[H], in/out.
+ * ------------------------------------------------------------------------ */
+int fa3_range_merge(const float* mins, const float* maxs, int R, int H, float* min_io, float* max_io,
+                    void* stream);
+
+/* ------------------------------------------------------------------------
  * Quantization parameters -- msModelSlim FA3量化, 原理 / 算法流程 step 4:
  *   abs_max[h] = max(|min[h]|, |max[h]|);  scale[h] = abs_max[h] / 127
  * (one IEEE float32 division).  min, max, scale: float[H].
@@ -139,6 +152,47 @@ int fa3_quantize_append(const uint16_t* kv, const float* scale, int8_t* cache, c
                         int B, int T_new, int H, int D, int T_max,
                         const uint16_t* rope_src, uint16_t* rope_cache, int Dr,
                         int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Per-channel parameters -- MindIE Turbo "Attention量化", 表1 / 表2: scale and
+ * offset tensors of shape [head_num, head_dim], one pair per (head, channel).
+ * The pages give the tensors' shapes, not the arithmetic; this library takes
+ * the plain readings below (float32 IEEE operations throughout):
+ *   symmetric   scale = max(|min|, |max|) / 127,  offset = 0
+ *               q = clamp(round_half_even(x / scale), -127, 127)
+ *   asymmetric  [lo, hi] = [min(min, 0), max(max, 0)]  (0 stays exact)
+ *               scale = (hi - lo) / 255,  offset = round_half_even(-lo / scale) - 128
+ *               q = clamp(round_half_even(x / scale) + offset, -128, 127)
+ *               dequantized value (q - offset) * scale
+ * scale = 0 (an all-zero channel) gives offset 0 and code 0 (symmetric) or
+ * offset (asymmetric).  min / max must be finite.
+ * ------------------------------------------------------------------------ */
+
+/* Per-channel Recall-Window calibration: msModelSlim FA3量化 算法流程 steps 2-3
+ * on each (head, channel) -- the N = B*S values x[b, h, s, d] of channel d of
+ * head h -- with the per-head call's readings (target_num = int(ratio * N),
+ * exact widths, ties to the smallest start, totalOrder running min/max).
+ * x        bf16; element (b, h, s, d) at x[b*stride_b + h*stride_h + s*stride_s + d].
+ * min_io, max_io  float [H][D], in/out (start at +inf / -inf).
+ * Supported: N - target_num + 1 <= 32 window starts (FA3_ERANGE otherwise),
+ *            H <= 65535.  No workspace. */
+int fa3_calibrate_perchannel(const uint16_t* x, int64_t B, int H, int64_t S, int D,
+                             int64_t stride_b, int64_t stride_h, int64_t stride_s, double ratio,
+                             float* min_io, float* max_io, void* stream);
+
+/* min_v, max_v, scale, offset: float[n] (n = heads * head_dim), device. */
+int fa3_qparams_channel(const float* min_v, const float* max_v, int n, int asymmetric,
+                        float* scale, float* offset, void* stream);
+
+/* Quantize-on-append with per-channel parameters (fa3_quantize_append's layout).
+ * kv bf16 [B][T_new][H][D]; scale, offset float [H][D] (offset may be NULL when
+ * asymmetric is 0); cache int8 [B][T_max][H][D] written at pos[b] + t.
+ * Supported: D % 8 == 0; kv, scale, offset 16-byte aligned, cache 8-byte aligned.
+ * A sequence with pos[b] < 0 or pos[b] + T_new > T_max is skipped and sets
+ * FA3_DEVERR_POS. */
+int fa3_quantize_append_channel(const uint16_t* kv, const float* scale, const float* offset,
+                                int asymmetric, int8_t* cache, const int32_t* pos,
+                                int B, int T_new, int H, int D, int T_max, int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * Absorbed-MLA decode attention over an INT8 latent cache -- MindIE
@@ -193,6 +247,24 @@ int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v,
                         const int32_t* lens, uint16_t* out, int B, int Hq, int Hkv, int D, int T_max,
                         float softmax_scale, void* workspace, size_t workspace_bytes,
                         int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * GQA decode with per-channel (asymmetric) INT8 q, k and v -- MindIE Turbo
+ * "Attention量化", 表1 / 表2 (q/k/v_scale and q/k/v_offset, [heads][head_dim]),
+ * with the dequantization of fa3_qparams_channel: x = (code - offset) * scale.
+ *   s[j] = sum_d xq[d] * xk_j[d] * softmax_scale,  out = bf16( sum_j softmax(s)_j * xv_j )
+ * q_scale, q_offset float [Hq][D]; k_scale, k_offset, v_scale, v_offset float [Hkv][D].
+ * k_offset moves every score of a row by the same amount, which the softmax
+ * removes: it must be passed and is not read.  Other arguments, layouts,
+ * limits and the workspace (fa3_gqa_workspace_size) as fa3_decode_attn_gqa.
+ * ------------------------------------------------------------------------ */
+int fa3_decode_attn_gqa_channel(const int8_t* q, const int8_t* k, const int8_t* v,
+                                const float* q_scale, const float* q_offset,
+                                const float* k_scale, const float* k_offset,
+                                const float* v_scale, const float* v_offset,
+                                const int32_t* lens, uint16_t* out, int B, int Hq, int Hkv, int D, int T_max,
+                                float softmax_scale, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * Prefill-phase GQA attention with INT8 q, k and v -- MindIE "Attention

@@ -19,8 +19,8 @@
 //             narrowest if it starts at the first copy of a value, so each
 //             occupied bin v with start position P(v) <= N - target_num is a
 //             candidate whose window ends in the bin holding position
-//             P(v) + target_num - 1.  Width in float64, argmin with ties to the
-//             smallest start, then the running min/max update.  The kernel
+//             P(v) + target_num - 1.  Exact widths (fp32 TwoSum pairs), argmin
+//             with ties to the smallest start, then the running min/max update.  The kernel
 //             zeroes the bins it read, leaving the workspace clean.
 // When few windows exist (N - target_num + 1 <= 16384, e.g. ratio 0.9999), every
 // window starts among the N - target_num + 1 smallest values and ends among the

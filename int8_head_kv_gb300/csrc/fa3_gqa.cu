@@ -50,9 +50,11 @@ struct GqaArgs {
   const int8_t* k;       // [B][T_max][Hkv][D], or a [pool rows][Hkv][D] page pool
   const int8_t* v;
   const int32_t* block_table;   // [B][max_pages] pool pages, or nullptr for the contiguous layout
-  const float* q_scale;
-  const float* k_scale;
-  const float* v_scale;
+  const float* q_scale;   // [Hq], or [Hq][D] per channel
+  const float* k_scale;   // [Hkv], or [Hkv][D]
+  const float* v_scale;   // [Hkv], or [Hkv][D]
+  const float* q_off;     // per channel only: [Hq][D] offsets of q and v (k's cancel in the softmax)
+  const float* v_off;
   const int32_t* lens;
   __nv_bfloat16* out;
   float* part_o;    // [B][Hkv][splits][8][D]
@@ -82,6 +84,13 @@ __device__ __forceinline__ void i8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, u
   const uint32_t u = w ^ 0x80808080u;
   lo = __byte_perm(u, 0x64646464u, 0x4140);
   hi = __byte_perm(u, 0x64646464u, 0x4342);
+}
+
+// Four signed int8 codes -> two f16x2 holding the codes themselves (exact).
+__device__ __forceinline__ void i8x4_to_f16x4_exact(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  i8x4_to_f16x4_biased(w, lo, hi);
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));    // - (1024 + 128)
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
 }
 
 // Exact integer m16n8k32 MMA on int8 codes (s32 accumulate).
@@ -128,7 +137,15 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-template <bool PAGED>
+// CHANNEL: per-channel asymmetric q, k, v (MindIE Turbo "Attention量化", 表1 / 表2:
+// [heads][D] scales and offsets).  The score of key j is
+//   sum_d (q8[d] - qo[d]) qs[d] * (k8_j[d] - ko[d]) ks[d]
+//     = sum_d w[d] k8_j[d] - sum_d w[d] ko[d],   w[d] = (q8[d] - qo[d]) qs[d] ks[d],
+// and the second term is the same for every key, so the softmax drops it: the
+// scores are K codes times the real vector w, taken as fp16 hi + lo parts (w
+// scaled per head by a power of two into fp16's range; the factor returns with
+// the softmax scale) in two f16 MMAs per 16 dims.  V: out[d] = vs[d] * (O[d] / l - vo[d]).
+template <bool PAGED, bool CHANNEL>
 __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -174,9 +191,54 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
     }
   }
   const int h0 = 2 * qd, h1 = 2 * qd + 1;
-  const float ks = p.k_scale[g] * p.sm_log2;
-  const float c0s = h0 < G ? p.q_scale[g * G + h0] * ks : 0.f;
-  const float c1s = h1 < G ? p.q_scale[g * G + h1] * ks : 0.f;
+  float c0s, c1s;
+  // per channel: the B fragments of w (hi, lo) for the 8 k16 steps; step s takes
+  // dims base(s) + 0..3, base(s) = 4s within the first 16-byte chunk of this
+  // thread (s < 4), then within its second chunk
+  uint32_t wh[8][2], wl[8][2];
+  if (!CHANNEL) {
+    const float ks = p.k_scale[g] * p.sm_log2;
+    c0s = h0 < G ? p.q_scale[g * G + h0] * ks : 0.f;
+    c1s = h1 < G ? p.q_scale[g * G + h1] * ks : 0.f;
+  } else {
+    float wv[32];
+    float amax = 0.f;
+    const int hq = g * G + r;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int d = (j < 16 ? 16 * qd : 64 + 16 * qd) + (j & 15);
+      const int code = (int)(int8_t)((qw[j >> 2] >> (8 * (j & 3))) & 0xffu);
+      float wj = 0.f;
+      if (r < G)
+        wj = ((float)code - p.q_off[(int64_t)hq * kD + d]) * p.q_scale[(int64_t)hq * kD + d] *
+             p.k_scale[(int64_t)g * kD + d];
+      wv[j] = wj;
+      amax = fmaxf(amax, fabsf(wj));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    // power-of-two factor putting the head's largest |w| into [2^13, 2^14)
+    int e = 0;
+    if (amax > 0.f) (void)frexpf(amax, &e);
+    const float down = amax > 0.f ? ldexpf(1.f, 14 - e) : 1.f;
+#pragma unroll
+    for (int s_ = 0; s_ < 8; ++s_) {
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int j = 4 * s_ + 2 * hlf;
+        const float a = wv[j] * down, b2 = wv[j + 1] * down;
+        const __half ah = __float2half_rn(a), bh = __float2half_rn(b2);
+        const __half al = __float2half_rn(a - __half2float(ah)), bl = __float2half_rn(b2 - __half2float(bh));
+        wh[s_][hlf] = (uint32_t)__half_as_ushort(ah) | ((uint32_t)__half_as_ushort(bh) << 16);
+        wl[s_][hlf] = (uint32_t)__half_as_ushort(al) | ((uint32_t)__half_as_ushort(bl) << 16);
+      }
+    }
+    const float up = 1.f / down;                       // exact: a power of two
+    const float up0 = __shfl_sync(0xffffffffu, up, 4 * h0);
+    const float up1 = __shfl_sync(0xffffffffu, up, 4 * h1);
+    c0s = h0 < G ? up0 * p.sm_log2 : 0.f;
+    c1s = h1 < G ? up1 * p.sm_log2 : 0.f;
+  }
 
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
   float o[8][4];
@@ -249,20 +311,36 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
     vr[2] = lds128(chunk_addr(vst, 2 * qd + 8, r));
     vr[3] = lds128(chunk_addr(vst, 2 * qd + 9, r));
     __syncwarp();   // every lane has its fragments: the stage may be refilled
-    // ---- scores S^T = K . Q^T: exact integer dot products (int8 MMA, s32)
-    int c[4] = {0, 0, 0, 0};
+    float cf[4];
+    if (!CHANNEL) {
+      // ---- scores S^T = K . Q^T: exact integer dot products (int8 MMA, s32)
+      int c[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const uint4& ka = kr[s < 2 ? 0 : 1];
-      const uint4& kb = kr[s < 2 ? 2 : 3];
-      const int w0 = (2 * s) & 3, w1 = (2 * s + 1) & 3;
-      mma16832_s8(c, word(ka, w0), word(kb, w0), word(ka, w1), word(kb, w1), qw[2 * s], qw[2 * s + 1]);
+      for (int s = 0; s < 4; ++s) {
+        const uint4& ka = kr[s < 2 ? 0 : 1];
+        const uint4& kb = kr[s < 2 ? 2 : 3];
+        const int w0 = (2 * s) & 3, w1 = (2 * s + 1) & 3;
+        mma16832_s8(c, word(ka, w0), word(kb, w0), word(ka, w1), word(kb, w1), qw[2 * s], qw[2 * s + 1]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cf[e] = (float)c[e];
+    } else {
+      // ---- scores S^T = K . w (fp16 codes x fp16 hi + lo parts, fp32 accumulate)
+      cf[0] = cf[1] = cf[2] = cf[3] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        uint32_t a0, a1, a2, a3;
+        i8x4_to_f16x4_exact(word(kr[s >> 2], s & 3), a0, a2);          // row r:     dims base(s) + 0..3
+        i8x4_to_f16x4_exact(word(kr[2 + (s >> 2)], s & 3), a1, a3);    // row r + 8
+        mma16816(cf, a0, a1, a2, a3, wh[s][0], wh[s][1]);
+        mma16816(cf, a0, a1, a2, a3, wl[s][0], wl[s][1]);
+      }
     }
     const bool va = t0 + r < t_end, vb = t0 + r + 8 < t_end;
-    float x0 = va ? (float)c[0] * c0s : -CUDART_INF_F;
-    float x1 = va ? (float)c[1] * c1s : -CUDART_INF_F;
-    float x2 = vb ? (float)c[2] * c0s : -CUDART_INF_F;
-    float x3 = vb ? (float)c[3] * c1s : -CUDART_INF_F;
+    float x0 = va ? cf[0] * c0s : -CUDART_INF_F;
+    float x1 = va ? cf[1] * c1s : -CUDART_INF_F;
+    float x2 = vb ? cf[2] * c0s : -CUDART_INF_F;
+    float x3 = vb ? cf[3] * c1s : -CUDART_INF_F;
 
     // ---- online softmax (log2 domain); rows of a head live in the 8 lanes sharing qd
     float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
@@ -336,7 +414,10 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
       }
     }
     if (p.splits == 1) {
-      const float val = L > 0.f ? p.v_scale[g] * (O / L - kVBias) : 0.f;
+      float val = 0.f;
+      if (L > 0.f)
+        val = CHANNEL ? p.v_scale[(int64_t)g * kD + d] * (O / L - kVBias - p.v_off[(int64_t)g * kD + d])
+                      : p.v_scale[g] * (O / L - kVBias);
       p.out[((int64_t)b * p.Hq + g * G + hh) * kD + d] = __float2bfloat16_rn(val);
     } else {
       const int64_t slot = (((int64_t)b * p.Hkv + g) * p.splits + split) * kHeadsPerTile + hh;
@@ -346,6 +427,7 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
   }
 }
 
+template <bool CHANNEL>
 __global__ void __launch_bounds__(kD) gqa_combine_kernel(const GqaArgs p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -369,7 +451,10 @@ __global__ void __launch_bounds__(kD) gqa_combine_kernel(const GqaArgs p) {
       }
     }
   }
-  const float val = L > 0.f ? p.v_scale[g] * (O / L - kVBias) : 0.f;
+  float val = 0.f;
+  if (L > 0.f)
+    val = CHANNEL ? p.v_scale[(int64_t)g * kD + d] * (O / L - kVBias - p.v_off[(int64_t)g * kD + d])
+                  : p.v_scale[g] * (O / L - kVBias);
   p.out[((int64_t)b * p.Hq + h) * kD + d] = __float2bfloat16_rn(val);
 }
 
@@ -396,9 +481,9 @@ int gqa_blocks_per_sm() {
   static int cached = 0;
   if (cached <= 0) {
     int n = 0;
-    if (cudaFuncSetAttribute(gqa_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+    if (cudaFuncSetAttribute(gqa_decode_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<false>, kThreads, kSmemBytes) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<false, false>, kThreads, kSmemBytes) !=
             cudaSuccess ||
         n <= 0)
       n = 3;
@@ -429,8 +514,11 @@ namespace {
 int gqa_decode(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale, const float* k_scale,
                const float* v_scale, const int32_t* lens, const int32_t* block_table, uint16_t* out, int B, int Hq,
                int Hkv, int D, int T_max, int num_pages, int page_size, int max_pages, float softmax_scale,
-               void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
+               void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream,
+               const float* q_off = nullptr, const float* v_off = nullptr) {
+  const bool channel = q_off != nullptr;
   if (!q || !k || !v || !q_scale || !k_scale || !v_scale || !lens || !out) return FA3_EINVAL;
+  if (channel && (!v_off || block_table)) return FA3_EINVAL;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || T_max <= 0) return FA3_EINVAL;
   if (Hq % Hkv != 0) return FA3_EINVAL;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return FA3_EINVAL;
@@ -446,6 +534,7 @@ int gqa_decode(const int8_t* q, const int8_t* k, const int8_t* v, const float* q
   if (need && (!workspace || workspace_bytes < need || !aligned16(workspace))) return FA3_EWORKSPACE;
   GqaArgs a;
   a.q = q; a.k = k; a.v = v; a.q_scale = q_scale; a.k_scale = k_scale; a.v_scale = v_scale; a.lens = lens;
+  a.q_off = q_off; a.v_off = v_off;
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
   const size_t slots = (size_t)B * Hkv * splits * kHeadsPerTile;
   a.part_o = static_cast<float*>(workspace);
@@ -456,14 +545,16 @@ int gqa_decode(const int8_t* q, const int8_t* k, const int8_t* v, const float* q
   a.div_ps = make_divu32((uint32_t)(page_size > 0 ? page_size : 1));
   a.sm_log2 = softmax_scale * 1.4426950408889634f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto* kernel = block_table ? gqa_decode_kernel<true> : gqa_decode_kernel<false>;
+  auto* kernel = channel ? gqa_decode_kernel<false, true>
+                         : block_table ? gqa_decode_kernel<true, false> : gqa_decode_kernel<false, false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return FA3_ECUDA;
   timing_begin(s);
   const cudaError_t le = launch_pdl(kernel, dim3(splits, Hkv, B), dim3(kThreads), kSmemBytes, s, a);
   timing_end(s);
   if (le != cudaSuccess) return FA3_ECUDA;
-  if (splits > 1 && launch_pdl(gqa_combine_kernel, dim3(Hq, B), dim3(kD), 0, s, a) != cudaSuccess)
+  if (splits > 1 && launch_pdl(channel ? gqa_combine_kernel<true> : gqa_combine_kernel<false>, dim3(Hq, B),
+                              dim3(kD), 0, s, a) != cudaSuccess)
     return FA3_ECUDA;
   return FA3_OK;
 }
@@ -475,6 +566,18 @@ FA3_API int fa3_decode_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* 
                                 size_t workspace_bytes, int32_t* dev_err, void* stream) {
   return gqa_decode(q, k, v, q_scale, k_scale, v_scale, lens, nullptr, out, B, Hq, Hkv, D, T_max, 0, 0, 0,
                     softmax_scale, workspace, workspace_bytes, dev_err, stream);
+}
+
+FA3_API int fa3_decode_attn_gqa_channel(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale,
+                                        const float* q_offset, const float* k_scale, const float* k_offset,
+                                        const float* v_scale, const float* v_offset, const int32_t* lens,
+                                        uint16_t* out, int B, int Hq, int Hkv, int D, int T_max, float softmax_scale,
+                                        void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  // k_offset shifts every score of a row by the same amount, which the softmax
+  // removes; it is part of the signature (the pages' tensor set) and not read.
+  if (!q_offset || !k_offset || !v_offset) return FA3_EINVAL;
+  return gqa_decode(q, k, v, q_scale, k_scale, v_scale, lens, nullptr, out, B, Hq, Hkv, D, T_max, 0, 0, 0,
+                    softmax_scale, workspace, workspace_bytes, dev_err, stream, q_offset, v_offset);
 }
 
 FA3_API int fa3_decode_attn_gqa_paged(const int8_t* q, const int8_t* k, const int8_t* v, const float* q_scale,

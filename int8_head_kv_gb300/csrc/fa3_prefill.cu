@@ -49,14 +49,18 @@ constexpr int kKeys = 128;         // keys per tile
 constexpr int kRowsP = 128;        // rows (TMEM lanes) per CTA
 constexpr int kThreadsP = 256;     // warp 0: MMA, warps 1-3: converters, warps 4-7: softmax
 constexpr int kConvP = 96;
-constexpr uint32_t TMP_O = 0, TMP_S = 128, TMP_Q = 384;
-constexpr uint32_t KV_TILE = kKeys * kD * 2;           // 32 KB of fp16
-constexpr uint32_t OFFP_K = 0;                         // 2 stages
-constexpr uint32_t OFFP_V = OFFP_K + 2 * KV_TILE;      // 2 stages
-constexpr uint32_t OFFP_P = OFFP_V + 2 * KV_TILE;      // fp16 P, 128 rows x 128 keys (32 KB)
-constexpr uint32_t OFFP_BAR = OFFP_P + kRowsP * kKeys * 2;
-enum { PB_KV_FULL = 0, PB_KV_EMPTY = 2, PB_S_FULL = 4, PB_S_EMPTY = 6, PB_P_FULL = 8, PB_PV_DONE = 9,
-       PB_Q_READY = 10, PB_DRAIN = 11, PB_N = 12 };
+constexpr int kNS = 3;             // S buffers in TMEM (P overwrites its own S)
+constexpr uint32_t TMP_O = 0, TMP_S = 128;                 // O [0,128), S[k] [128 + 128k, 256 + 128k)
+constexpr uint32_t KV_TILE = kKeys * kD * 2;               // 32 KB of fp16
+constexpr uint32_t OFFP_Q = 0;                             // fp16 query rows, K-major (32 KB)
+constexpr uint32_t OFFP_K = OFFP_Q + kRowsP * kD * 2;      // 2 stages
+constexpr uint32_t OFFP_V = OFFP_K + 2 * KV_TILE;          // 2 stages
+constexpr uint32_t OFFP_BAR = OFFP_V + 2 * KV_TILE;
+enum {
+  PB_K_FULL = 0, PB_K_EMPTY = 2, PB_V_FULL = 4, PB_V_EMPTY = 6,
+  PB_S_FULL = 8, PB_P_FULL = PB_S_FULL + kNS, PB_S_FREE = PB_P_FULL + kNS,
+  PB_PV_DONE = PB_S_FREE + kNS, PB_Q_READY, PB_DRAIN, PB_N
+};
 constexpr uint32_t OFFP_TSLOT = OFFP_BAR + 8 * PB_N;
 constexpr uint32_t OFFP_ABORT = OFFP_TSLOT + 4;
 constexpr uint32_t SMEM_PREFILL = OFFP_BAR + 256 + 1024;   // + alignment slack
@@ -103,12 +107,16 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(PB_KV_FULL + s), kConvP);
-      mbar_init(bar(PB_KV_EMPTY + s), 1);
-      mbar_init(bar(PB_S_FULL + s), 1);
-      mbar_init(bar(PB_S_EMPTY + s), 4);
+      mbar_init(bar(PB_K_FULL + s), kConvP);
+      mbar_init(bar(PB_K_EMPTY + s), 1);
+      mbar_init(bar(PB_V_FULL + s), kConvP);
+      mbar_init(bar(PB_V_EMPTY + s), 1);
     }
-    mbar_init(bar(PB_P_FULL), 4);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(bar(PB_S_FULL + s), 1);
+      mbar_init(bar(PB_P_FULL + s), 4);
+      mbar_init(bar(PB_S_FREE + s), 1);
+    }
     mbar_init(bar(PB_PV_DONE), 1);
     mbar_init(bar(PB_Q_READY), 4);
     mbar_init(bar(PB_DRAIN), 1);
@@ -131,36 +139,43 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
       const uint32_t id_qk = idesc_f16(kRowsP, kKeys, false, false);
       const uint32_t id_pv = idesc_f16(kRowsP, kD, false, true);
       bool ok = wait_bar(bar(PB_Q_READY), 0, abort_flag, p.err);
-      // S[j % 2] = Q . K_j^T; K is the K-major B operand (8-token core groups 128 B
-      // apart, 8-wide d groups 2048 B apart).
+      // S[j % 3] = Q . K_j^T: Q is the K-major A operand in shared memory (8-row core
+      // groups 128 B apart, 8-wide d groups 2048 B apart), K the K-major B operand
+      // (8-token groups 128 B apart, d groups 2048 B apart).  The buffer is free once
+      // P.V of tile j - 3 has read the P that overwrote its S.
       auto issue_qk = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!(wait_bar(bar(PB_KV_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err) &&
-              wait_bar(bar(PB_S_EMPTY + s), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, p.err)))
+        const int s = j & 1, sb = j % kNS;
+        if (!(wait_bar(bar(PB_K_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err) &&
+              wait_bar(bar(PB_S_FREE + sb), ((uint32_t)(j / kNS) & 1u) ^ 1u, abort_flag, p.err)))
           return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t a = sdesc(sbase + OFFP_Q + kk * 4096, 2048, 128);
           const uint64_t bd = sdesc(sbase + OFFP_K + s * KV_TILE + kk * 4096, 2048, 128);
-          mma_f16_ts(tmem + TMP_S + s * 128, tmem + TMP_Q + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
+          mma_f16(tmem + TMP_S + sb * 128, a, bd, id_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(PB_S_FULL + s));
+        mma_commit(bar(PB_S_FULL + sb));
+        mma_commit(bar(PB_K_EMPTY + s));
         return true;
       };
-      // O += P_j . V_j: P is the K-major A operand, V the MN-major B operand (token
-      // groups 128 B apart, d groups 2048 B apart).  Completion frees P and stage j % 2.
+      // O += P_j . V_j: P (fp16, written over S[j % 3]: column k holds keys 2k, 2k + 1)
+      // is the A operand in TMEM, V the MN-major B operand (token groups 128 B apart,
+      // d groups 2048 B apart).
       auto issue_pv = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!wait_bar(bar(PB_P_FULL), (uint32_t)j & 1u, abort_flag, p.err)) return false;
+        const int s = j & 1, sb = j % kNS;
+        if (!(wait_bar(bar(PB_P_FULL + sb), (uint32_t)(j / kNS) & 1u, abort_flag, p.err) &&
+              wait_bar(bar(PB_V_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err)))
+          return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t a = sdesc(sbase + OFFP_P + kk * 4096, 2048, 128);
           const uint64_t bd = sdesc(sbase + OFFP_V + s * KV_TILE + kk * 256, 128, 2048);
-          mma_f16(tmem + TMP_O, a, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + TMP_O, tmem + TMP_S + sb * 128 + kk * 8, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(PB_PV_DONE));
-        mma_commit(bar(PB_KV_EMPTY + s));
+        mma_commit(bar(PB_V_EMPTY + s));
+        mma_commit(bar(PB_S_FREE + sb));
         return true;
       };
       ok = ok && issue_qk(0) && (nt < 2 || issue_qk(1));
@@ -178,7 +193,8 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
     // consecutive units is 16 tokens x 2 chunks, lane l taking token l % 16 and
     // chunk l / 16: a warp loads 16 full 32-byte sectors and its fp16 stores hit
     // every bank once per 128 bytes.  fp16 element (token n, d) lands at
-    // (d / 8) * 2048 + n * 16 + (d % 8) * 2.
+    // (d / 8) * 2048 + n * 16 + (d % 8) * 2.  K(j) may be written once Q.K^T of
+    // tile j - 2 is done, V(j) once P.V of tile j - 2 is.
     constexpr int kUnits = 2 * kKeys * (kD / 16);                 // 2048
     constexpr int kPer = (kUnits + kConvP - 1) / kConvP;           // 22
     const int ct = tid - 32;
@@ -195,6 +211,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
     };
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1;
+      const uint32_t par = ((uint32_t)(j >> 1) & 1u) ^ 1u;
       uint4 w[kPer];
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
@@ -204,23 +221,28 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
         w[i] = make_uint4(0u, 0u, 0u, 0u);
         if (in && t < n_keys) w[i] = __ldg(reinterpret_cast<const uint4*>((kv ? vb : kb) + t * row_stride) + cc);
       }
-      if (!wait_bar(bar(PB_KV_EMPTY + s), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, p.err)) break;
+      bool ok = true;
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        int kv, n, cc;
-        if (unit(i, kv, n, cc)) {
-          uint8_t* dst = smem + (kv ? OFFP_V : OFFP_K) + s * KV_TILE;
-          uint4 o0, o1;
-          i8x4_to_f16x4(w[i].x, o0.x, o0.y);
-          i8x4_to_f16x4(w[i].y, o0.z, o0.w);
-          i8x4_to_f16x4(w[i].z, o1.x, o1.y);
-          i8x4_to_f16x4(w[i].w, o1.z, o1.w);
-          *reinterpret_cast<uint4*>(dst + (2 * cc) * 2048 + n * 16) = o0;
-          *reinterpret_cast<uint4*>(dst + (2 * cc + 1) * 2048 + n * 16) = o1;
+      for (int half = 0; half < 2 && ok; ++half) {
+        if (!wait_bar(bar((half ? PB_V_EMPTY : PB_K_EMPTY) + s), par, abort_flag, p.err)) { ok = false; break; }
+        uint8_t* dst = smem + (half ? OFFP_V : OFFP_K) + s * KV_TILE;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          int kv, n, cc;
+          if (unit(i, kv, n, cc) && kv == half) {
+            uint4 o0, o1;
+            i8x4_to_f16x4(w[i].x, o0.x, o0.y);
+            i8x4_to_f16x4(w[i].y, o0.z, o0.w);
+            i8x4_to_f16x4(w[i].z, o1.x, o1.y);
+            i8x4_to_f16x4(w[i].w, o1.z, o1.w);
+            *reinterpret_cast<uint4*>(dst + (2 * cc) * 2048 + n * 16) = o0;
+            *reinterpret_cast<uint4*>(dst + (2 * cc + 1) * 2048 + n * 16) = o1;
+          }
         }
+        fence_proxy_async();
+        mbar_arrive(bar((half ? PB_V_FULL : PB_K_FULL) + s));
       }
-      fence_proxy_async();
-      mbar_arrive(bar(PB_KV_FULL + s));
+      if (!ok) break;
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -229,60 +251,73 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
     const int i = i0 + r / p.G, h = g * p.G + r % p.G;
     const bool active = i < nq;
     const int pos = active ? prefix + i : -1;               // last key this row sees
-    const float c = active ? p.q_scale[h] * p.k_scale[g] * p.sm_log2 : 0.f;
+    // an inactive row masks every key (its scale stays finite so that -inf * c is -inf)
+    const float c = active ? p.q_scale[h] * p.k_scale[g] * p.sm_log2 : 1.f;
+    const int pos_min = prefix + i0;                        // the block's first position
+    const bool ragged = i0 + p.P > nq;                      // the block has inactive rows
     auto warp_arrive = [&](int which) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(which));
     };
-    // The row's query codes as fp16 pairs in TMEM (column k holds d = 2k, 2k + 1).
+    // The row's query codes as fp16 into the K-major A operand (chunk of 8 d at
+    // (d / 8) * 2048 + row * 16).
     {
-      uint32_t qw[64];
       const int8_t* qrow = p.q + (((int64_t)b * p.S + (active ? i : 0)) * p.Hq + h) * kD;
 #pragma unroll
       for (int c16 = 0; c16 < 8; ++c16) {
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
         if (active) x = *reinterpret_cast<const uint4*>(qrow + 16 * c16);
-        i8x4_to_f16x4(x.x, qw[8 * c16 + 0], qw[8 * c16 + 1]);
-        i8x4_to_f16x4(x.y, qw[8 * c16 + 2], qw[8 * c16 + 3]);
-        i8x4_to_f16x4(x.z, qw[8 * c16 + 4], qw[8 * c16 + 5]);
-        i8x4_to_f16x4(x.w, qw[8 * c16 + 6], qw[8 * c16 + 7]);
+        uint4 o0, o1;
+        i8x4_to_f16x4(x.x, o0.x, o0.y);
+        i8x4_to_f16x4(x.y, o0.z, o0.w);
+        i8x4_to_f16x4(x.z, o1.x, o1.y);
+        i8x4_to_f16x4(x.w, o1.z, o1.w);
+        *reinterpret_cast<uint4*>(smem + OFFP_Q + (2 * c16) * 2048 + r * 16) = o0;
+        *reinterpret_cast<uint4*>(smem + OFFP_Q + (2 * c16 + 1) * 2048 + r * 16) = o1;
       }
-      FA3_TMEM_ST32(tmem + lane_base + TMP_Q, qw);
-      FA3_TMEM_ST32(tmem + lane_base + TMP_Q + 32, (qw + 32));
-      tmem_wait_st();
-      tc_fence_before();
+      fence_proxy_async();
       warp_arrive(PB_Q_READY);
     }
     float m_run = -CUDART_INF_F, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nt && ok; ++j) {
-      const int s = j & 1;
-      if (!warp_all(wait_bar(bar(PB_S_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err))) { ok = false; break; }
+      const int sb = j % kNS;
+      if (!warp_all(wait_bar(bar(PB_S_FULL + sb), (uint32_t)(j / kNS) & 1u, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const uint32_t scol = tmem + lane_base + TMP_S + s * 128;
-      // pass 1: the tile's row maximum (log2 units)
+      const uint32_t scol = tmem + lane_base + TMP_S + sb * 128;
+      const int t0 = j * kKeys;
+      // keys of this tile beyond some row's position (the diagonal) or inactive rows
+      const bool masked = ragged || t0 + kKeys - 1 > pos_min;
+      // pass 1: the tile's row maximum of the raw integer scores, then scaled (c > 0)
       float mx = -CUDART_INF_F;
 #pragma unroll 1
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t v[32];
         FA3_TMEM_LD32(scol + c4 * 32, v);
         tmem_wait_ld();
+        if (masked) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int t = j * kKeys + c4 * 32 + e;
-          mx = fmaxf(mx, t <= pos ? __uint_as_float(v[e]) * c : -CUDART_INF_F);
+          for (int e = 0; e < 32; ++e)
+            mx = fmaxf(mx, t0 + c4 * 32 + e <= pos ? __uint_as_float(v[e]) : -CUDART_INF_F);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) mx = max3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
         }
       }
+      mx *= c;
       const float m_new = fmaxf(m_run, mx);
-      // O and P are free once P.V of the previous tile is done.
-      if (j > 0 && !warp_all(wait_bar(bar(PB_PV_DONE), (uint32_t)(j - 1) & 1u, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // Lazy rescale: the reference maximum moves only when the row maximum grew by more than 8.
+      // Lazy rescale: the reference maximum moves only when the row maximum grew by
+      // more than 8; then O (holding P.V up to tile j - 1) is scaled in place.
       const bool grow = m_new != -CUDART_INF_F && (m_run == -CUDART_INF_F || m_new > m_run + 8.f);
       if (__any_sync(0xffffffffu, grow && m_run != -CUDART_INF_F)) {
+        if (!warp_all(wait_bar(bar(PB_PV_DONE), (uint32_t)(j - 1) & 1u, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         const float f = (grow && m_run != -CUDART_INF_F) ? ex2_approx(m_run - m_new) : 1.f;
 #pragma unroll 1
         for (int c4 = 0; c4 < 4; ++c4) {
@@ -293,13 +328,15 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
           FA3_TMEM_ST32(tmem + lane_base + TMP_O + c4 * 32, v);
         }
-        tmem_wait_st();
       }
       if (grow) {
         l_run = m_run == -CUDART_INF_F ? 0.f : l_run * ex2_approx(m_run - m_new);
         m_run = m_new;
       }
-      // pass 2: P = exp2(s - m_run) as fp16 into shared memory (K-major A operand of P.V)
+      const float mc = m_run == -CUDART_INF_F ? 0.f : m_run;
+      // pass 2: P = exp2(s c - m) as fp16 pairs over the S columns already read
+      // (keys 32 c4 .. 32 c4 + 31 go to columns 16 c4 .. 16 c4 + 15); the row sum
+      // takes the same fp16 weights, so the output is a weighted mean of V.
 #pragma unroll 1
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t v[32];
@@ -308,23 +345,22 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int t = j * kKeys + c4 * 32 + e;
-          const float p0 = t <= pos ? ex2_approx(__uint_as_float(v[e]) * c - m_run) : 0.f;
-          const float p1 = t + 1 <= pos ? ex2_approx(__uint_as_float(v[e + 1]) * c - m_run) : 0.f;
+          const int t = t0 + c4 * 32 + e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), c, -mc));
+          float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), c, -mc));
+          if (masked) {
+            p0 = t <= pos ? p0 : 0.f;
+            p1 = t + 1 <= pos ? p1 : 0.f;
+          }
           pk[e / 2] = pack_f16x2(p0, p1);
-          // the row sum of the fp16 weights P.V uses: the output stays a weighted mean of V
           const float2 pr = __half22float2(*reinterpret_cast<const __half2*>(&pk[e / 2]));
           l_run += pr.x + pr.y;
         }
-#pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8)       // 8 keys (16 bytes) per core-matrix row
-          *reinterpret_cast<uint4*>(smem + OFFP_P + (c4 * 4 + k8) * 2048 + r * 16) =
-              make_uint4(pk[4 * k8], pk[4 * k8 + 1], pk[4 * k8 + 2], pk[4 * k8 + 3]);
+        FA3_TMEM_ST16(scol + c4 * 16, pk);
       }
-      fence_proxy_async();
+      tmem_wait_st();
       tc_fence_before();
-      warp_arrive(PB_S_EMPTY + s);
-      warp_arrive(PB_P_FULL);
+      warp_arrive(PB_P_FULL + sb);
     }
     // epilogue: out = v_scale * O / l
     if (ok && warp_all(wait_bar(bar(PB_PV_DONE), (uint32_t)(nt - 1) & 1u, abort_flag, p.err))) {

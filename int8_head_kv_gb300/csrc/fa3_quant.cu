@@ -7,6 +7,8 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 namespace fa3 {
 
 namespace {
@@ -40,6 +42,28 @@ __global__ void qparams_kernel(const float* __restrict__ mn, const float* __rest
   pdl_launch_dependents();
   int h = blockIdx.x * blockDim.x + threadIdx.x;
   if (h < H) scale[h] = __fdiv_rn(fmaxf(fabsf(mn[h]), fabsf(mx[h])), 127.0f);
+}
+
+// Step 3 over R ranges at once: min_io[h] = min(min_io[h], mins[r][h]) and max
+// likewise for every r, in IEEE totalOrder (-0.0 below +0.0), so the result does
+// not depend on how the calibration batches were split or ordered.
+__device__ __forceinline__ bool range_less(float a, float b) {
+  return a < b || (a == b && signbit(a) && !signbit(b));
+}
+__global__ void range_merge_kernel(const float* __restrict__ mins, const float* __restrict__ maxs, int R, int H,
+                                   float* __restrict__ min_io, float* __restrict__ max_io) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= H) return;
+  float lo = min_io[h], hi = max_io[h];
+  for (int r = 0; r < R; ++r) {
+    const float a = mins[(int64_t)r * H + h], b = maxs[(int64_t)r * H + h];
+    if (range_less(a, lo)) lo = a;
+    if (range_less(hi, b)) hi = b;
+  }
+  min_io[h] = lo;
+  max_io[h] = hi;
 }
 
 // Paged cache: position x of sequence b is row block_table[b][x / page_size] *
@@ -219,6 +243,18 @@ FA3_API int fa3_qparams(const float* min_v, const float* max_v, float* scale, in
   return cuda_status(launch_pdl(qparams_kernel, dim3((H + 127) / 128), dim3(128), 0, s, min_v, max_v, scale, H));
 }
 
+FA3_API int fa3_range_merge(const float* mins, const float* maxs, int R, int H, float* min_io, float* max_io,
+                            void* stream) {
+  if (!mins || !maxs || !min_io || !max_io) return FA3_EINVAL;
+  if (R <= 0 || H <= 0) return FA3_EINVAL;
+  int sms = 0;
+  const int st = check_device(&sms);
+  if (st != FA3_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch_pdl(range_merge_kernel, dim3((H + 127) / 128), dim3(128), 0, s, mins, maxs, R, H,
+                                min_io, max_io));
+}
+
 namespace {
 // Both layouts: pm == nullptr is the contiguous [B][T_max] cache; otherwise the
 // cache (and the RoPE cache) are page pools addressed through *pm.
@@ -301,4 +337,122 @@ FA3_API int fa3_quantize_append_paged(const uint16_t* kv, const float* scale, in
   pm.div_rope = make_divu32((uint32_t)std::max(1, Dr / 8));
   return quantize_append(kv, scale, cache, pos, B, T_new, H, D, max_pages * page_size, rope_src, rope_cache, Dr,
                          dev_err, stream, &pm);
+}
+
+// ---------------------------------------------------------------------------
+// Per-channel parameters -- MindIE Turbo "Attention量化", 表1 / 表2: q/k/v_scale
+// and q/k/v_offset of shape [head_num, head_dim].
+//
+// Symmetric: scale = max(|min|, |max|) / 127 (msModelSlim FA3量化 step 4 per
+// channel), offset 0.  Asymmetric: the range widened to contain 0,
+// [lo, hi] = [min(min, 0), max(max, 0)], maps onto the codes -128 .. 127:
+//   scale = (hi - lo) / 255,  offset = round_half_even(-lo / scale) - 128
+// (float32 IEEE subtraction and divisions; scale 0 gives offset 0).  Codes:
+//   symmetric  q = clamp(round_half_even(x / scale), -127, 127)
+//   asymmetric q = clamp(round_half_even(x / scale) + offset, -128, 127)
+// ---------------------------------------------------------------------------
+namespace fa3 {
+namespace {
+
+__global__ void qparams_channel_kernel(const float* __restrict__ mn, const float* __restrict__ mx, int n,
+                                       int asym, float* __restrict__ scale, float* __restrict__ offset) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  if (!asym) {
+    scale[i] = __fdiv_rn(fmaxf(fabsf(mn[i]), fabsf(mx[i])), 127.0f);
+    offset[i] = 0.f;
+    return;
+  }
+  const float lo = fminf(mn[i], 0.f), hi = fmaxf(mx[i], 0.f);
+  const float s = __fdiv_rn(__fsub_rn(hi, lo), 255.0f);
+  scale[i] = s;
+  offset[i] = s == 0.f ? 0.f : rintf(__fdiv_rn(-lo, s)) - 128.f;
+}
+
+__device__ __forceinline__ int channel_code(float x, float s, float o, bool asym) {
+  float r = s == 0.f ? 0.f : __fdiv_rn(x, s);
+  if (!asym) return __float2int_rn(fminf(fmaxf(r, -127.f), 127.f));
+  r = fminf(fmaxf(r, -1e9f), 1e9f);
+  return max(-128, min(127, __float2int_rn(r) + (int)o));
+}
+
+// One thread per 8 consecutive values (16 bytes of bf16) of the new rows; the
+// channel parameters of those 8 values are read as two float4 pairs.
+__global__ void quantize_append_channel_kernel(const uint16_t* __restrict__ kv, const float* __restrict__ scale,
+                                               const float* __restrict__ offset, int asym,
+                                               int8_t* __restrict__ cache, const int32_t* __restrict__ pos,
+                                               int B, int T_new, int HD, int T_max, int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t groups_row = HD / 8, groups_seq = (int64_t)T_new * groups_row;
+  const int64_t total = (int64_t)B * groups_seq;
+  for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < total;
+       gi += (int64_t)gridDim.x * blockDim.x) {
+    const int b = (int)(gi / groups_seq);
+    const int64_t rem = gi - (int64_t)b * groups_seq;
+    const int t = (int)(rem / groups_row);
+    const int c8 = (int)(rem - (int64_t)t * groups_row) * 8;     // first of the 8 values in the row
+    const int p0 = pos[b];
+    if (p0 < 0 || p0 + T_new > T_max) {
+      if (rem == 0) set_dev_err(err, FA3_DEVERR_POS);
+      continue;
+    }
+    const uint4 v = *reinterpret_cast<const uint4*>(kv + gi * 8);
+    const float4 s0 = *reinterpret_cast<const float4*>(scale + c8);
+    const float4 s1 = *reinterpret_cast<const float4*>(scale + c8 + 4);
+    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f), o1 = o0;
+    if (asym) {
+      o0 = *reinterpret_cast<const float4*>(offset + c8);
+      o1 = *reinterpret_cast<const float4*>(offset + c8 + 4);
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const float oo[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float x = bf16_to_float((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+      const int q = channel_code(x, ss[e], oo[e], asym != 0);
+      packed[e >> 2] |= ((uint32_t)(q & 0xFF)) << (8 * (e & 3));
+    }
+    int8_t* dst = cache + (((int64_t)b * T_max + p0 + t) * HD + c8);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+  }
+}
+
+}  // namespace
+}  // namespace fa3
+
+using namespace fa3;
+
+FA3_API int fa3_qparams_channel(const float* min_v, const float* max_v, int n, int asymmetric, float* scale,
+                                float* offset, void* stream) {
+  if (!min_v || !max_v || !scale || !offset || n <= 0) return FA3_EINVAL;
+  int sms = 0;
+  const int st = check_device(&sms);
+  if (st != FA3_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch_pdl(qparams_channel_kernel, dim3((n + 127) / 128), dim3(128), 0, s, min_v, max_v, n,
+                                asymmetric ? 1 : 0, scale, offset));
+}
+
+FA3_API int fa3_quantize_append_channel(const uint16_t* kv, const float* scale, const float* offset,
+                                        int asymmetric, int8_t* cache, const int32_t* pos, int B, int T_new, int H,
+                                        int D, int T_max, int32_t* dev_err, void* stream) {
+  if (!kv || !scale || !cache || !pos || (asymmetric && !offset)) return FA3_EINVAL;
+  if (B <= 0 || T_new <= 0 || H <= 0 || D <= 0 || T_max <= 0 || T_new > T_max) return FA3_EINVAL;
+  if (D % 8 != 0 || !aligned16(kv) || !aligned16(scale) || (asymmetric && !aligned16(offset)) ||
+      (reinterpret_cast<uintptr_t>(cache) & 7u) != 0)
+    return FA3_ERANGE;
+  if ((int64_t)H * D >= ((int64_t)1 << 31)) return FA3_ERANGE;
+  int sms = 0;
+  const int st = check_device(&sms);
+  if (st != FA3_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t total = (int64_t)B * T_new * H * D / 8;
+  const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8);
+  return cuda_status(launch_pdl(quantize_append_channel_kernel, dim3(blocks), dim3(256), 0, s, kv, scale, offset,
+                                asymmetric ? 1 : 0, cache, pos, B, T_new, H * D, T_max, dev_err));
 }

@@ -6,6 +6,7 @@ library has not been built, every call raises; there is no fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from collections import OrderedDict
@@ -43,11 +44,16 @@ _SIGS = {
     "fa3_calibrate_workspace_size": (_SZ, [_I]),
     "fa3_calibrate_perhead": (_I, [_P, _I64, _I, _I64, _I64, _I64, _D, _P, _P, _P, _SZ, _P]),
     "fa3_qparams": (_I, [_P, _P, _P, _I, _P]),
+    "fa3_range_merge": (_I, [_P, _P, _I, _I, _P, _P, _P]),
+    "fa3_qparams_channel": (_I, [_P, _P, _I, _I, _P, _P, _P]),
+    "fa3_calibrate_perchannel": (_I, [_P, _I64, _I, _I64, _I, _I64, _I64, _I64, _D, _P, _P, _P]),
+    "fa3_quantize_append_channel": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "fa3_quantize_append": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
     "fa3_mla_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "fa3_decode_attn_mla": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
     "fa3_gqa_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "fa3_decode_attn_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
+    "fa3_decode_attn_gqa_channel": (_I, [_P] * 11 + [_I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
     "fa3_prefill_attn_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "fa3_quantize_append_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P]),
     "fa3_decode_attn_mla_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ,
@@ -189,6 +195,46 @@ def calibrate_perhead(x: torch.Tensor, ratio: float, min_io: torch.Tensor, max_i
     _check("fa3_calibrate_perhead", st)
 
 
+def range_merge(mins: torch.Tensor, maxs: torch.Tensor, min_io: torch.Tensor, max_io: torch.Tensor,
+                stream=None) -> None:
+    """Folds R ranges mins/maxs [R][H] into the running range min_io/max_io [H] (in place)."""
+    _need_contig(mins, torch.float32, "mins")
+    _need_contig(maxs, torch.float32, "maxs")
+    _need_contig(min_io, torch.float32, "min_io")
+    _need_contig(max_io, torch.float32, "max_io")
+    H = min_io.numel()
+    if mins.dim() != 2 or mins.shape != maxs.shape or mins.shape[1] != H or max_io.numel() != H:
+        raise ValueError("mins/maxs must be [R][H] with H = min_io.numel()")
+    st = lib().fa3_range_merge(_ptr(mins), _ptr(maxs), mins.shape[0], H, _ptr(min_io), _ptr(max_io),
+                               _stream(stream))
+    _check("fa3_range_merge", st)
+
+
+def calibrate_perhead_sharded(batches, ratio: float, min_io: torch.Tensor, max_io: torch.Tensor,
+                              group=None, stream=None) -> None:
+    """Recall-Window calibration with the batches sharded over the ranks of a
+    torch.distributed group: each rank calibrates its own batches into a local
+    range (fa3_calibrate_perhead), the ranks all-gather their [H] ranges (the one
+    exchange step), and every rank folds them into min_io/max_io
+    (fa3_range_merge).  Step 3 is associative, so the result is bit-identical to
+    one process accumulating every batch in any order."""
+    import torch.distributed as dist
+    H = min_io.numel()
+    dev = min_io.device
+    loc_mn = torch.full((H,), float("inf"), dtype=torch.float32, device=dev)
+    loc_mx = torch.full((H,), float("-inf"), dtype=torch.float32, device=dev)
+    for x in batches:
+        calibrate_perhead(x, ratio, loc_mn, loc_mx, stream=stream)
+    world = dist.get_world_size(group)
+    mins = torch.empty(world, H, dtype=torch.float32, device=dev)
+    maxs = torch.empty(world, H, dtype=torch.float32, device=dev)
+    ctx = torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+    with ctx:                                   # the collective is ordered on the calls' stream
+        dist.all_gather(list(mins.unbind(0)), loc_mn, group=group)    # rows of mins / maxs
+        dist.all_gather(list(maxs.unbind(0)), loc_mx, group=group)
+    range_merge(mins, maxs, min_io, max_io, stream=stream)
+
+
 def qparams(min_v: torch.Tensor, max_v: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
     _need_contig(min_v, torch.float32, "min")
     _need_contig(max_v, torch.float32, "max")
@@ -198,6 +244,58 @@ def qparams(min_v: torch.Tensor, max_v: torch.Tensor, out: Optional[torch.Tensor
     st = lib().fa3_qparams(_ptr(min_v), _ptr(max_v), _ptr(out), H, _stream(stream))
     _check("fa3_qparams", st)
     return out
+
+
+def calibrate_perchannel(x: torch.Tensor, ratio: float, min_io: torch.Tensor, max_io: torch.Tensor,
+                         stream=None) -> None:
+    """Recall-Window calibration per (head, channel) of one batch x bf16 (B, H, S, D)
+    (D contiguous); updates min_io / max_io [H][D] in place."""
+    _need(x, torch.bfloat16, "x")
+    _need_contig(min_io, torch.float32, "min_io")
+    _need_contig(max_io, torch.float32, "max_io")
+    if x.dim() != 4 or x.stride(3) != 1:
+        raise ValueError("x must be (B, H, S, D) with D contiguous")
+    B, H, S, D = x.shape
+    if min_io.numel() != H * D or max_io.numel() != H * D:
+        raise ValueError("min_io / max_io must hold H * D values")
+    st = lib().fa3_calibrate_perchannel(_ptr(x), B, H, S, D, x.stride(0), x.stride(1), x.stride(2), float(ratio),
+                                        _ptr(min_io), _ptr(max_io), _stream(stream))
+    _check("fa3_calibrate_perchannel", st)
+
+
+def qparams_channel(min_v: torch.Tensor, max_v: torch.Tensor, asymmetric: bool, stream=None):
+    """Per-(head, channel) scale and offset from per-channel ranges [H][D]; returns (scale, offset)."""
+    _need_contig(min_v, torch.float32, "min")
+    _need_contig(max_v, torch.float32, "max")
+    if min_v.shape != max_v.shape:
+        raise ValueError("min and max must have the same shape")
+    scale = torch.empty_like(min_v)
+    offset = torch.empty_like(min_v)
+    st = lib().fa3_qparams_channel(_ptr(min_v), _ptr(max_v), min_v.numel(), int(bool(asymmetric)), _ptr(scale),
+                                   _ptr(offset), _stream(stream))
+    _check("fa3_qparams_channel", st)
+    return scale, offset
+
+
+def quantize_append_channel(kv: torch.Tensor, scale: torch.Tensor, offset: Optional[torch.Tensor], asymmetric: bool,
+                            cache: torch.Tensor, pos: torch.Tensor, dev_err: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    """kv bf16 [B][T_new][H][D] -> cache int8 [B][T_max][H][D] at pos[b], per-channel scale/offset [H][D]."""
+    _need_contig(kv, torch.bfloat16, "kv")
+    _need_contig(scale, torch.float32, "scale")
+    if asymmetric:
+        _need_contig(offset, torch.float32, "offset")
+    _need_contig(cache, torch.int8, "cache")
+    _need_contig(pos, torch.int32, "pos")
+    B, T_new, H, D = kv.shape
+    if cache.dim() != 4 or cache.shape[0] != B or cache.shape[2] != H or cache.shape[3] != D:
+        raise ValueError("cache must be [B][T_max][H][D]")
+    if scale.numel() != H * D or (asymmetric and offset.numel() != H * D):
+        raise ValueError("scale / offset must hold H * D values")
+    st = lib().fa3_quantize_append_channel(_ptr(kv), _ptr(scale), _ptr(offset) if asymmetric else None,
+                                           int(bool(asymmetric)), _ptr(cache), _ptr(pos), B, T_new, H, D,
+                                           cache.shape[1], _ptr(dev_err), _stream(stream))
+    _check("fa3_quantize_append_channel", st)
 
 
 def quantize_append(kv: torch.Tensor, scale: torch.Tensor, cache: torch.Tensor, pos: torch.Tensor,
@@ -279,6 +377,37 @@ def decode_attn_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: 
                                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
                                    _ptr(dev_err), _stream(stream))
     _check("fa3_decode_attn_gqa", st)
+    return out
+
+
+def decode_attn_gqa_channel(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: torch.Tensor,
+                            q_offset: torch.Tensor, k_scale: torch.Tensor, k_offset: torch.Tensor,
+                            v_scale: torch.Tensor, v_offset: torch.Tensor, lens: torch.Tensor, softmax_scale: float,
+                            out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """GQA decode with per-channel scales / offsets ([heads][D] each): q int8 [B][Hq][D],
+    k/v int8 [B][T_max][Hkv][D] -> bf16 [B][Hq][D]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need_contig(t, torch.int8, n)
+    for t, n in ((q_scale, "q_scale"), (q_offset, "q_offset"), (k_scale, "k_scale"), (k_offset, "k_offset"),
+                 (v_scale, "v_scale"), (v_offset, "v_offset")):
+        _need_contig(t, torch.float32, n)
+    _need_contig(lens, torch.int32, "lens")
+    B, Hq, D = q.shape
+    T_max, Hkv = k.shape[1], k.shape[2]
+    if q_scale.numel() != Hq * D or k_scale.numel() != Hkv * D or v_scale.numel() != Hkv * D:
+        raise ValueError("per-channel parameters must be [heads][D]")
+    if out is None:
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=q.device)
+    nbytes = gqa_workspace_size(B, Hq, Hkv, D, T_max)
+    if workspace is None:
+        workspace = _workspace("gqa", nbytes, q.device, stream=stream)
+    st = lib().fa3_decode_attn_gqa_channel(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(q_offset), _ptr(k_scale),
+                                           _ptr(k_offset), _ptr(v_scale), _ptr(v_offset), _ptr(lens), _ptr(out), B,
+                                           Hq, Hkv, D, T_max, float(softmax_scale), _ptr(workspace),
+                                           0 if workspace is None else workspace.numel(), _ptr(dev_err),
+                                           _stream(stream))
+    _check("fa3_decode_attn_gqa_channel", st)
     return out
 
 

@@ -272,6 +272,113 @@ def quantize_append_paged(kv: np.ndarray, scale: np.ndarray, pool: np.ndarray, b
     return out
 
 
+# ---------------------------------------------------------------------------
+# Per-channel parameters: MindIE Turbo "Attention量化", 表1 / 表2 -- q/k/v_scale
+# and q/k/v_offset of shape [head_num, head_dim].  The Recall Window of FA3量化
+# 算法流程 steps 2-3 runs per (head, channel) over the B*S values of that channel.
+# ---------------------------------------------------------------------------
+def calibrate_channel_batch(x_bhsd: np.ndarray, ratio: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-(head, channel) (min_val, max_val) of one batch (B, H, S, D): step 2 on
+    the N = B*S values x[:, h, :, d] of each channel."""
+    x = np.asarray(x_bhsd)
+    if x.ndim != 4:
+        raise ValueError("x must be (B, H, S, D)")
+    _, H, _, D = x.shape
+    lo = np.empty((H, D), np.float32)
+    hi = np.empty((H, D), np.float32)
+    for h in range(H):
+        for d in range(D):
+            a, b = recall_window(x[:, h, :, d].reshape(-1), ratio)
+            lo[h, d], hi[h, d] = a, b
+    return lo, hi
+
+
+def calibrate_channel(batches: Iterable[np.ndarray], ratio: float):
+    """Steps 2-3 per (head, channel) over calibration batches; returns ([H][D], [H][D])."""
+    mn = mx = None
+    for x in batches:
+        lo, hi = calibrate_channel_batch(x, ratio)
+        if mn is None:
+            mn, mx = init_range(lo.size)
+            mn, mx = mn.reshape(lo.shape), mx.reshape(lo.shape)
+        accumulate(mn.reshape(-1), mx.reshape(-1), lo.reshape(-1), hi.reshape(-1))
+    return mn, mx
+
+
+def qparams_channel(min_v: np.ndarray, max_v: np.ndarray, asymmetric: bool) -> Tuple[np.ndarray, np.ndarray]:
+    """scale and offset per (head, channel), float32.
+
+    Symmetric: step 4 per channel, scale = max(|min|, |max|) / 127, offset 0.
+    Asymmetric (the pages give the offset tensor's shape, not its formula; the
+    plain reading): the range is widened to contain 0, [lo, hi] = [min(min, 0),
+    max(max, 0)], so that 0 stays exact, and mapped onto the codes -128 .. 127:
+      scale  = (hi - lo) / 255                 (float32 subtraction, then division)
+      offset = round_half_even(-lo / scale) - 128   (an integer; 0 when scale = 0)
+    """
+    mn = np.asarray(min_v, np.float32)
+    mx = np.asarray(max_v, np.float32)
+    if not asymmetric:
+        return qparams(mn, mx), np.zeros(mn.shape, np.float32)
+    lo = np.minimum(mn, np.float32(0))
+    hi = np.maximum(mx, np.float32(0))
+    width = np.subtract(hi, lo, dtype=np.float32)                                    # float32 IEEE subtraction
+    scale = np.divide(width, np.float32(255), dtype=np.float32)                      # float32 IEEE division
+    with np.errstate(divide="ignore", invalid="ignore"):
+        z = np.divide(-lo, scale, dtype=np.float32)                                 # float32 IEEE division
+    offset = np.where(scale == 0, np.float32(0), np.rint(z) - np.float32(128)).astype(np.float32)
+    return scale, offset
+
+
+def quantize_channel(x: np.ndarray, scale: np.ndarray, offset: np.ndarray, asymmetric: bool) -> np.ndarray:
+    """Codes with per-channel parameters broadcast against x (..., D).
+
+    Symmetric: q = clamp(round_half_even(x / scale), -127, 127).
+    Asymmetric: q = clamp(round_half_even(x / scale) + offset, -128, 127).
+    x / scale is one float32 division; scale = 0 gives code 0 (symmetric) or
+    offset (asymmetric, where offset is then 0)."""
+    if not asymmetric:
+        return quantize(x, scale)
+    x32 = np.asarray(x, np.float32)
+    s32 = np.broadcast_to(np.asarray(scale, np.float32), x32.shape)
+    o32 = np.broadcast_to(np.asarray(offset, np.float32), x32.shape)
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        r = np.divide(x32, s32, dtype=np.float32)
+    r = np.where(s32 == 0, np.float32(0), r)
+    r = np.clip(r, -1e9, 1e9)                       # +-inf -> large finite before the integer step
+    q = np.rint(r).astype(np.float64) + o32.astype(np.float64)
+    return np.clip(q, -128, 127).astype(np.int8)
+
+
+def dequantize_channel(q: np.ndarray, scale: np.ndarray, offset: np.ndarray) -> np.ndarray:
+    """deq: (code - offset) * scale, float64."""
+    return (np.asarray(q, np.float64) - np.asarray(offset, np.float64)) * np.asarray(scale, np.float64)
+
+
+def gqa_decode_channel(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, qs: np.ndarray, qo: np.ndarray,
+                       ks: np.ndarray, ko: np.ndarray, vs: np.ndarray, vo: np.ndarray, lens: np.ndarray,
+                       softmax_scale: float) -> np.ndarray:
+    """GQA decode on per-channel (asymmetric) INT8 q, k, v: every tensor is
+    dequantized with its [heads][D] scale and offset, then plain attention.
+
+    q8: [B][Hq][D] (qs, qo: [Hq][D]); k8, v8: [B][T][Hkv][D] (ks, ko, vs, vo: [Hkv][D]).
+    Returns float64 [B][Hq][D]."""
+    B, Hq, D = q8.shape
+    Hkv = k8.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, D), np.float64)
+    for b in range(B):
+        n = int(lens[b])
+        if n <= 0:
+            continue
+        for h in range(Hq):
+            g = h // G
+            qv = dequantize_channel(q8[b, h], qs[h], qo[h])
+            kv = dequantize_channel(k8[b, :n, g], ks[g], ko[g])
+            vv = dequantize_channel(v8[b, :n, g], vs[g], vo[g])
+            out[b, h] = _softmax_weights((kv @ qv) * float(softmax_scale)) @ vv
+    return out
+
+
 def dequantize(q: np.ndarray, scale) -> np.ndarray:
     """deq_scale: code * scale, in float64."""
     return np.asarray(q, np.float64) * np.asarray(scale, np.float64)

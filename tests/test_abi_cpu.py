@@ -77,6 +77,30 @@ def test_gqa_validation(L):
     assert call(Hq=128, Hkv=8) == ERANGE  # 16 query heads per KV head
 
 
+def test_range_merge_validation(L):
+    call = lambda mins=FAKE, R=2, H=4: L.fa3_range_merge(mins, FAKE, R, H, FAKE, FAKE, None)
+    assert call(mins=None) == EINVAL
+    assert call(R=0) == EINVAL
+    assert call(H=0) == EINVAL
+
+
+def test_channel_validation(L):
+    q = lambda mn=FAKE, n=8: L.fa3_qparams_channel(mn, FAKE, n, 1, FAKE, FAKE, None)
+    assert q(mn=None) == EINVAL and q(n=0) == EINVAL
+    a = lambda off=FAKE, asym=1, D=128: L.fa3_quantize_append_channel(FAKE, FAKE, off, asym, FAKE, FAKE, 2, 4, 8, D,
+                                                                      64, None, None)
+    assert a(off=None) == EINVAL             # asymmetric without offsets
+    assert a(D=12) == ERANGE                 # not a multiple of 8
+    c = lambda ratio=0.9999, S=1000: L.fa3_calibrate_perchannel(FAKE, 3, 4, S, 40, 1, 1, 1, ratio, FAKE, FAKE, None)
+    assert c(ratio=0.0) == EINVAL
+    assert c(ratio=0.9, S=1000) == ERANGE    # 301 window starts > 32
+    g = lambda ko=FAKE, D=128: L.fa3_decode_attn_gqa_channel(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ko, FAKE, FAKE,
+                                                             FAKE, FAKE, 2, 64, 8, D, 64, 0.09, FAKE, 1 << 30,
+                                                             None, None)
+    assert g(ko=None) == EINVAL
+    assert g(D=64) == ERANGE
+
+
 def test_prefill_validation(L):
     UNALIGNED = ctypes.c_void_p(4096 + 8)
     call = lambda Hq=64, Hkv=8, D=128, q=FAKE, sc=0.09, out=FAKE, S=64: L.fa3_prefill_attn_gqa(

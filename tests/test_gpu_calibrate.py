@@ -194,3 +194,45 @@ def test_thin_tails_fall_back_to_full_count(vec):
         torch.cuda.synchronize()
         assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn))
         assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx))
+
+
+def test_range_merge_matches_step_3_in_any_split():
+    # R ranges folded into the running range in one call: the same bits as step 3
+    # applied batch by batch (signed zeros ordered, infinities kept).
+    F = fa3()
+    rng = np.random.default_rng(31)
+    R, H = 5, 300
+    mins = rng.standard_normal((R, H)).astype(np.float32)
+    maxs = rng.standard_normal((R, H)).astype(np.float32)
+    mins[:, :8] = np.array([0.0, -0.0, 0.0, -0.0, np.inf, -np.inf, 1.0, -1.0], np.float32)
+    maxs[:, :8] = np.array([-0.0, 0.0, -0.0, 0.0, -np.inf, np.inf, -1.0, 1.0], np.float32)
+    mins[1, :4] = np.array([-0.0, 0.0, 0.0, -0.0], np.float32)
+    mn0, mx0 = O.init_range(H)
+    mn0[10:20] = -0.5
+    mx0[10:20] = 0.5
+    omn, omx = mn0.copy(), mx0.copy()
+    for r in range(R):
+        O.accumulate(omn, omx, mins[r], maxs[r])
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    mn, mx = t(mn0), t(mx0)
+    F.range_merge(t(mins), t(maxs), mn, mx)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn))
+    assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx))
+
+
+def test_batches_split_over_shards_then_merged_equal_one_pass():
+    # What calibrate_perhead_sharded does on each rank, with the ranks' shares
+    # calibrated one after another on this GPU: local ranges, then one merge.
+    F = fa3()
+    w = W.mla_tiny()
+    batches = W.mla_inputs(w).calib_q
+    omn, omx = O.calibrate(batches, w.ratio)
+    shards = [batches[0::2], batches[1::2]]
+    locs = [_gpu_calibrate(F, sh, w.ratio, w.H) for sh in shards]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    mn = torch.full((w.H,), float("inf"), device="cuda")
+    mx = torch.full((w.H,), float("-inf"), device="cuda")
+    F.range_merge(t(np.stack([l[0] for l in locs])), t(np.stack([l[1] for l in locs])), mn, mx)
+    assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn))
+    assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx))

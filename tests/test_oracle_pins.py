@@ -492,3 +492,96 @@ def test_prefill_row_selection_equals_full_rows():
     for b, i in rows:
         mask[b, i] = True
     assert not part[~mask].any()
+
+
+# ------------------------------------------------------------ per-channel / asymmetric
+def test_qparams_channel_hand_example():
+    # channel 0: [-1, 3] -> width 4, scale 4/255, offset RNE(1 / (4/255)) - 128 = RNE(63.75) - 128 = -64
+    # channel 1: [2, 5]  -> widened to [0, 5]: scale 5/255, offset 0 - 128 = -128
+    # channel 2: [-6, -2] -> widened to [-6, 0]: scale 6/255, offset 255 - 128 = 127
+    # channel 3: all zero -> scale 0, offset 0
+    mn = np.array([-1.0, 2.0, -6.0, 0.0], np.float32)
+    mx = np.array([3.0, 5.0, -2.0, 0.0], np.float32)
+    sc, of = O.qparams_channel(mn, mx, asymmetric=True)
+    assert np.array_equal(sc, np.array([4, 5, 6, 0], np.float32) / np.float32(255))
+    assert of.tolist() == [-64.0, -128.0, 127.0, 0.0]
+    ssc, sof = O.qparams_channel(mn, mx, asymmetric=False)
+    assert np.array_equal(ssc, np.array([3, 5, 6, 0], np.float32) / np.float32(127)) and not sof.any()
+    # the ends of the range land on (or next to) the extreme codes, and 0 is exact
+    q = O.quantize_channel(np.stack([np.minimum(mn, 0), np.maximum(mx, 0), np.zeros(4, np.float32)]), sc, of, True)
+    assert q[0, :3].tolist() == [-128, -128, -128] and q[1, :3].tolist() == [127, 127, 127]
+    assert np.all(O.dequantize_channel(q[2], sc, of) == 0.0)
+
+
+def test_quantize_channel_matches_torch_affine_quantizer():
+    # torch's per-channel affine quantizer computes clamp(round(x * (1 / scale)) +
+    # zero_point) with half-to-even rounding: an independent implementation of the
+    # rule, which multiplies by a rounded reciprocal instead of dividing, so the two
+    # may differ where x / scale lies within a hair of a half-integer (checked rare).
+    rng = np.random.default_rng(12)
+    H, D = 3, 16
+    x = _bf16(rng.standard_normal((50, H, D)) * rng.uniform(0.1, 4, (1, H, D)))
+    mn = x.min(axis=0) * 1.2
+    mx = x.max(axis=0) * 0.9
+    sc, of = O.qparams_channel(mn, mx, asymmetric=True)
+    q = O.quantize_channel(x, sc, of, True)
+    ref = torch.quantize_per_channel(torch.from_numpy(x.reshape(50, H * D)), torch.from_numpy(sc.reshape(-1)).double(),
+                                     torch.from_numpy(of.reshape(-1).astype(np.int64)), 1, torch.qint8).int_repr()
+    r = x.reshape(50, H * D).astype(np.float64) / sc.reshape(-1).astype(np.float64)
+    near_tie = np.abs(r - np.floor(r) - 0.5) < 1e-3
+    diff = q.reshape(50, H * D) != ref.numpy()
+    assert not np.any(diff & ~near_tie) and np.count_nonzero(near_tie) < 0.01 * r.size
+    # dequantization error inside the range is at most half a step
+    inside = (x >= np.minimum(mn, 0)) & (x <= np.maximum(mx, 0))
+    err = np.abs(O.dequantize_channel(q, sc, of) - x.astype(np.float64))
+    assert np.all(err[inside] <= 0.5 * sc.astype(np.float64)[None].repeat(50, 0)[inside] * (1 + 1e-6))
+
+
+def test_channel_calibration_is_per_head_on_each_channel():
+    rng = np.random.default_rng(13)
+    x = _bf16(rng.standard_t(3, (2, 3, 40, 5)) * rng.uniform(0.1, 3, (1, 3, 1, 5)))
+    lo, hi = O.calibrate_channel_batch(x, 0.95)
+    for h in range(3):
+        for d in range(5):
+            col = x[:, h, :, d].reshape(-1)
+            assert (lo[h, d], hi[h, d]) == O.recall_window_bruteforce(col, 0.95)
+    # a channel-constant layout reduces to the per-head calibration of that channel
+    x2 = np.repeat(x[..., :1], 4, axis=-1)
+    lo2, hi2 = O.calibrate_channel_batch(x2, 0.95)
+    plo, phi = O.calibrate_batch(x[..., :1], 0.95)
+    assert np.array_equal(lo2, np.repeat(plo[:, None], 4, 1)) and np.array_equal(hi2, np.repeat(phi[:, None], 4, 1))
+    # accumulation over batches
+    b2 = _bf16(rng.standard_normal((2, 3, 40, 5)) * 9)
+    mn, mx = O.calibrate_channel([x, b2], 0.95)
+    l2, h2 = O.calibrate_channel_batch(b2, 0.95)
+    assert np.array_equal(mn, np.minimum(lo, l2)) and np.array_equal(mx, np.maximum(hi, h2))
+
+
+def test_gqa_decode_channel_reduces_and_matches_sdpa():
+    rng = np.random.default_rng(14)
+    B, Hq, Hkv, T, D = 2, 4, 2, 9, 8
+    q8 = rng.integers(-128, 128, (B, Hq, D)).astype(np.int8)
+    k8 = rng.integers(-128, 128, (B, T, Hkv, D)).astype(np.int8)
+    v8 = rng.integers(-128, 128, (B, T, Hkv, D)).astype(np.int8)
+    qs, ks, vs = (rng.uniform(0.005, 0.02, (n, D)).astype(np.float32) for n in (Hq, Hkv, Hkv))
+    qo, ko, vo = (rng.integers(-20, 20, (n, D)).astype(np.float32) for n in (Hq, Hkv, Hkv))
+    lens = np.array([9, 4])
+    out = O.gqa_decode_channel(q8, k8, v8, qs, qo, ks, ko, vs, vo, lens, 0.3)
+    for b in range(B):
+        n = lens[b]
+        q = O.dequantize_channel(q8[b], qs, qo)                                     # [Hq][D]
+        k = np.repeat(O.dequantize_channel(k8[b, :n], ks, ko), 2, axis=1)          # [n][Hq][D]
+        v = np.repeat(O.dequantize_channel(v8[b, :n], vs, vo), 2, axis=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[:, None, :]), torch.from_numpy(k.transpose(1, 0, 2)),
+            torch.from_numpy(v.transpose(1, 0, 2)), scale=0.3).numpy()[:, 0]
+        assert np.allclose(out[b], ref, rtol=1e-9, atol=1e-12)
+    # per-head scales broadcast along D with zero offsets: the per-head decode
+    qh, kh, vh = qs[:, :1], ks[:, :1], vs[:, :1]
+    z = lambda a: np.zeros_like(a)
+    a = O.gqa_decode_channel(np.clip(q8, -127, 127), np.clip(k8, -127, 127), np.clip(v8, -127, 127),
+                             np.repeat(qh, D, 1), z(qo), np.repeat(kh, D, 1), z(ko), np.repeat(vh, D, 1), z(vo),
+                             lens, 0.3)
+    bb = O.gqa_decode(np.clip(q8, -127, 127), np.clip(k8, -127, 127), np.clip(v8, -127, 127), qh[:, 0], kh[:, 0],
+                      vh[:, 0], lens, 0.3)
+    assert np.allclose(a, bb, rtol=1e-12, atol=1e-12)
