@@ -57,6 +57,8 @@ enum fa3_status {
 #define FA3_DEVERR_LENS 2     /* decode: lens[b] < 0 or lens[b] > T_max (output row set to 0) */
 #define FA3_DEVERR_TIMEOUT 4  /* a bounded wait inside a kernel gave up (output not valid)    */
 #define FA3_DEVERR_PAGE 8     /* paged calls: a block-table entry outside [0, num_pages)       */
+#define FA3_DEVERR_CALIB 16   /* float32 calibration: a head's tail counts disagreed (non-finite
+                                 input); that head's range is left unchanged                  */
 
 /* Human-readable name of a status code (static string). */
 const char* fa3_status_string(int status);
@@ -109,6 +111,24 @@ int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L,
                           int64_t stride_b, int64_t stride_h, double ratio,
                           float* min_io, float* max_io,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Calibration of float32 activations -- the same steps and readings as
+ * fa3_calibrate_perhead (msModelSlim FA3量化, 原理 / 算法流程 steps 1-3) for
+ * float32 input: x float32, element (b, h, l) at x[b*stride_b + h*stride_h + l].
+ * Supported: N - target_num + 1 <= 4096 window starts (the pages' ratio 0.9999
+ * keeps that up to N = 40.96 million values per head), N < 2^31, H <= 65535;
+ * values finite with magnitude below 2^127 (not checked: a head whose internal
+ * counts then disagree sets FA3_DEVERR_CALIB and keeps its range).
+ * workspace  fa3_calibrate_f32_workspace_size(H) bytes, 16-byte aligned,
+ *            ZERO-FILLED before its first use; every call leaves it zeroed.
+ * ------------------------------------------------------------------------ */
+size_t fa3_calibrate_f32_workspace_size(int H);
+
+int fa3_calibrate_perhead_f32(const float* x, int64_t B, int H, int64_t L,
+                              int64_t stride_b, int64_t stride_h, double ratio,
+                              float* min_io, float* max_io, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err, void* stream);
 
 /* ------------------------------------------------------------------------
  * Running-range merge -- msModelSlim FA3量化, 原理 / 算法流程 step 3 applied to

@@ -13,21 +13,21 @@
 //
 // The contraction is dense (2 * 2 * D FLOP per (row, key) pair), so the kernel
 // is built around the tensor pipe:
-//   * one CTA per (block of 128 rows, KV head g, sequence b); its 128 rows are
-//     P = 128 / G query positions x the G query heads of the group, so every K/V
-//     tile feeds the whole group (row r = TMEM lane r: position r / G, head r % G);
+//   * one CTA per (block of 2 x 128 rows, KV head g, sequence b): two query tiles
+//     A and B of 128 rows, each P = 128 / G query positions x the G query heads of
+//     the group, so that every converted K/V tile feeds 256 rows (row r of a tile
+//     = TMEM lane r: position r / G, head r % G);
 //   * int8 codes are exact in fp16 and a 128-term sum of their products stays
 //     below 2^24, so kind::f16 MMAs with fp32 accumulation give the exact integer
 //     score (sm_103a has no integer tcgen05 kind);
 //   * warp 0 issues the MMAs; warps 1-3 load 128-token int8 K and V tiles into
 //     registers one tile ahead and write them as fp16 core matrices into one of
 //     two shared-memory stages (K-major for Q.K^T, MN-major for P.V); warps 4-7
-//     own one row each for the online softmax;
-//   * TMEM: O [0,128), S double-buffered [128,384), the fp16 query codes as the
-//     A operand of Q.K^T [384,448); S(j+2) is computed while the softmax works
-//     on S(j+1) and P(j).V(j) runs;
+//     (tile A) and 8-11 (tile B) own one row each for the online softmax;
+//   * TMEM: O_A, O_B, S_A, S_B, 128 columns each; while one tile's softmax runs
+//     the tensor pipe works on the other tile's S or P.V;
 //   * the softmax writes P (fp16, unnormalised, relative to a lazily moved row
-//     maximum) into shared memory as the K-major A operand of P.V, sums the same
+//     maximum) over its own S in TMEM, the A operand of P.V; it sums the same
 //     fp16 weights for the row's normaliser (so the output is a weighted mean of
 //     V whatever the rounding of P), and rescales O in TMEM only when a row's
 //     maximum grows by more than 8 (log2 units);
@@ -46,20 +46,22 @@ namespace {
 
 constexpr int kD = 128;            // head dim
 constexpr int kKeys = 128;         // keys per tile
-constexpr int kRowsP = 128;        // rows (TMEM lanes) per CTA
-constexpr int kThreadsP = 256;     // warp 0: MMA, warps 1-3: converters, warps 4-7: softmax
+constexpr int kRowsP = 128;        // rows (TMEM lanes) per query tile
+constexpr int kThreadsP = 384;     // warp 0: MMA, warps 1-3: converters, 4-7: softmax A, 8-11: softmax B
 constexpr int kConvP = 96;
-constexpr int kNS = 3;             // S buffers in TMEM (P overwrites its own S)
-constexpr uint32_t TMP_O = 0, TMP_S = 128;                 // O [0,128), S[k] [128 + 128k, 256 + 128k)
+constexpr uint32_t TMP_O = 0, TMP_S = 256;                 // O_x [128x, +128), S_x [256 + 128x, +128)
 constexpr uint32_t KV_TILE = kKeys * kD * 2;               // 32 KB of fp16
-constexpr uint32_t OFFP_Q = 0;                             // fp16 query rows, K-major (32 KB)
-constexpr uint32_t OFFP_K = OFFP_Q + kRowsP * kD * 2;      // 2 stages
+constexpr uint32_t Q_TILE = kRowsP * kD * 2;               // 32 KB of fp16
+constexpr uint32_t OFFP_Q = 0;                             // 2 x fp16 query rows, K-major
+constexpr uint32_t OFFP_K = OFFP_Q + 2 * Q_TILE;           // 2 stages
 constexpr uint32_t OFFP_V = OFFP_K + 2 * KV_TILE;          // 2 stages
 constexpr uint32_t OFFP_BAR = OFFP_V + 2 * KV_TILE;
 enum {
   PB_K_FULL = 0, PB_K_EMPTY = 2, PB_V_FULL = 4, PB_V_EMPTY = 6,
-  PB_S_FULL = 8, PB_P_FULL = PB_S_FULL + kNS, PB_S_FREE = PB_P_FULL + kNS,
-  PB_PV_DONE = PB_S_FREE + kNS, PB_Q_READY, PB_DRAIN, PB_N
+  PB_S_FULL = 8,                   // [2]: tile x's scores of the current key tile
+  PB_P_FULL = 10,                  // [2]: tile x's P written over its S
+  PB_PV_DONE = 12,                 // [2]: P_x.V done (O_x holds it; S_x free)
+  PB_Q_READY = 14, PB_DRAIN, PB_N
 };
 constexpr uint32_t OFFP_TSLOT = OFFP_BAR + 8 * PB_N;
 constexpr uint32_t OFFP_ABORT = OFFP_TSLOT + 4;
@@ -99,10 +101,10 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
     if (rb == 0 && g == 0 && tid == 0) set_dev_err(p.err, FA3_DEVERR_LENS);
     return;
   }
-  const int i0 = rb * p.P;
+  const int i0 = rb * 2 * p.P;                             // first position of tile A; tile B follows
   if (i0 >= nq) return;                                    // no row of this block is a new row
   const int prefix = nkv - nq;
-  const int n_keys = prefix + min(nq, i0 + p.P);           // keys up to the block's last position
+  const int n_keys = prefix + min(nq, i0 + 2 * p.P);       // keys up to the block's last position
   const int nt = (n_keys + kKeys - 1) / kKeys;
 
   if (tid == 0) {
@@ -111,14 +113,11 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
       mbar_init(bar(PB_K_EMPTY + s), 1);
       mbar_init(bar(PB_V_FULL + s), kConvP);
       mbar_init(bar(PB_V_EMPTY + s), 1);
-    }
-    for (int s = 0; s < kNS; ++s) {
       mbar_init(bar(PB_S_FULL + s), 1);
       mbar_init(bar(PB_P_FULL + s), 4);
-      mbar_init(bar(PB_S_FREE + s), 1);
+      mbar_init(bar(PB_PV_DONE + s), 1);
     }
-    mbar_init(bar(PB_PV_DONE), 1);
-    mbar_init(bar(PB_Q_READY), 4);
+    mbar_init(bar(PB_Q_READY), 8);
     mbar_init(bar(PB_DRAIN), 1);
     *abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -139,49 +138,46 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
       const uint32_t id_qk = idesc_f16(kRowsP, kKeys, false, false);
       const uint32_t id_pv = idesc_f16(kRowsP, kD, false, true);
       bool ok = wait_bar(bar(PB_Q_READY), 0, abort_flag, p.err);
-      // S[j % 3] = Q . K_j^T: Q is the K-major A operand in shared memory (8-row core
-      // groups 128 B apart, 8-wide d groups 2048 B apart), K the K-major B operand
-      // (8-token groups 128 B apart, d groups 2048 B apart).  The buffer is free once
-      // P.V of tile j - 3 has read the P that overwrote its S.
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j & 1, sb = j % kNS;
-        if (!(wait_bar(bar(PB_K_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err) &&
-              wait_bar(bar(PB_S_FREE + sb), ((uint32_t)(j / kNS) & 1u) ^ 1u, abort_flag, p.err)))
-          return false;
+      // S_x = Q_x . K_j^T: Q_x the K-major A operand in shared memory (8-row core
+      // groups 128 B apart, 8-wide d groups 2048 B apart), K the K-major B operand.
+      // S_x holds the P of key tile j - 1 until P_x.V(j - 1) is done.
+      auto issue_qk = [&](int j, int x) -> bool {
+        const int s = j & 1;
+        if (!wait_bar(bar(PB_K_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err)) return false;
+        if (j > 0 && !wait_bar(bar(PB_PV_DONE + x), (uint32_t)(j - 1) & 1u, abort_flag, p.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t a = sdesc(sbase + OFFP_Q + kk * 4096, 2048, 128);
+          const uint64_t a = sdesc(sbase + OFFP_Q + x * Q_TILE + kk * 4096, 2048, 128);
           const uint64_t bd = sdesc(sbase + OFFP_K + s * KV_TILE + kk * 4096, 2048, 128);
-          mma_f16(tmem + TMP_S + sb * 128, a, bd, id_qk, kk > 0 ? 1u : 0u);
+          mma_f16(tmem + TMP_S + x * 128, a, bd, id_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(PB_S_FULL + sb));
-        mma_commit(bar(PB_K_EMPTY + s));
+        mma_commit(bar(PB_S_FULL + x));
+        if (x == 1) mma_commit(bar(PB_K_EMPTY + s));         // both tiles are done with K_j
         return true;
       };
-      // O += P_j . V_j: P (fp16, written over S[j % 3]: column k holds keys 2k, 2k + 1)
+      // O_x += P_x . V_j: P_x (fp16, written over S_x: column k holds keys 2k, 2k + 1)
       // is the A operand in TMEM, V the MN-major B operand (token groups 128 B apart,
       // d groups 2048 B apart).
-      auto issue_pv = [&](int j) -> bool {
-        const int s = j & 1, sb = j % kNS;
-        if (!(wait_bar(bar(PB_P_FULL + sb), (uint32_t)(j / kNS) & 1u, abort_flag, p.err) &&
-              wait_bar(bar(PB_V_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err)))
-          return false;
+      auto issue_pv = [&](int j, int x) -> bool {
+        const int s = j & 1;
+        if (!wait_bar(bar(PB_P_FULL + x), (uint32_t)j & 1u, abort_flag, p.err)) return false;
+        if (x == 0 && !wait_bar(bar(PB_V_FULL + s), (uint32_t)(j >> 1) & 1u, abort_flag, p.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           const uint64_t bd = sdesc(sbase + OFFP_V + s * KV_TILE + kk * 256, 128, 2048);
-          mma_f16_ts(tmem + TMP_O, tmem + TMP_S + sb * 128 + kk * 8, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + TMP_O + x * 128, tmem + TMP_S + x * 128 + kk * 8, bd, id_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(PB_PV_DONE));
-        mma_commit(bar(PB_V_EMPTY + s));
-        mma_commit(bar(PB_S_FREE + sb));
+        mma_commit(bar(PB_PV_DONE + x));
+        if (x == 1) mma_commit(bar(PB_V_EMPTY + s));          // both tiles are done with V_j
         return true;
       };
-      ok = ok && issue_qk(0) && (nt < 2 || issue_qk(1));
+      ok = ok && issue_qk(0, 0) && issue_qk(0, 1);
       for (int j = 0; j < nt && ok; ++j) {
-        ok = issue_pv(j);
-        if (ok && j + 2 < nt) ok = issue_qk(j + 2);
+        ok = issue_pv(j, 0) && issue_pv(j, 1);
+        if (ok && j + 1 < nt) ok = issue_qk(j + 1, 0) && issue_qk(j + 1, 1);
       }
       // Drain: every MMA issued has completed before TMEM is freed.
       mma_commit(bar(PB_DRAIN));
@@ -193,8 +189,8 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
     // consecutive units is 16 tokens x 2 chunks, lane l taking token l % 16 and
     // chunk l / 16: a warp loads 16 full 32-byte sectors and its fp16 stores hit
     // every bank once per 128 bytes.  fp16 element (token n, d) lands at
-    // (d / 8) * 2048 + n * 16 + (d % 8) * 2.  K(j) may be written once Q.K^T of
-    // tile j - 2 is done, V(j) once P.V of tile j - 2 is.
+    // (d / 8) * 2048 + n * 16 + (d % 8) * 2.  K(j) may be written once both
+    // Q.K^T of tile j - 2 are done, V(j) once both P.V of tile j - 2 are.
     constexpr int kUnits = 2 * kKeys * (kD / 16);                 // 2048
     constexpr int kPer = (kUnits + kConvP - 1) / kConvP;           // 22
     const int ct = tid - 32;
@@ -246,34 +242,38 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int r = (warp - 4) * 32 + lane;                  // row == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
-    const int i = i0 + r / p.G, h = g * p.G + r % p.G;
+    const int x = (warp - 4) >> 2;                          // query tile: 0 = A, 1 = B
+    const int r = ((warp - 4) & 3) * 32 + lane;             // row == TMEM lane
+    const uint32_t lane_base = (uint32_t)(((warp - 4) & 3) * 32) << 16;
+    const int i = i0 + x * p.P + r / p.G, h = g * p.G + r % p.G;
     const bool active = i < nq;
     const int pos = active ? prefix + i : -1;               // last key this row sees
     // an inactive row masks every key (its scale stays finite so that -inf * c is -inf)
     const float c = active ? p.q_scale[h] * p.k_scale[g] * p.sm_log2 : 1.f;
-    const int pos_min = prefix + i0;                        // the block's first position
-    const bool ragged = i0 + p.P > nq;                      // the block has inactive rows
+    const int pos_min = prefix + i0 + x * p.P;              // the tile's first position
+    const bool ragged = i0 + (x + 1) * p.P > nq;            // the tile has inactive rows
+    const uint32_t o_col = tmem + lane_base + TMP_O + x * 128;
+    const uint32_t scol = tmem + lane_base + TMP_S + x * 128;
     auto warp_arrive = [&](int which) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(which));
     };
-    // The row's query codes as fp16 into the K-major A operand (chunk of 8 d at
+    // The row's query codes as fp16 into tile x's K-major A operand (chunk of 8 d at
     // (d / 8) * 2048 + row * 16).
     {
       const int8_t* qrow = p.q + (((int64_t)b * p.S + (active ? i : 0)) * p.Hq + h) * kD;
+      uint8_t* qdst = smem + OFFP_Q + x * Q_TILE + r * 16;
 #pragma unroll
       for (int c16 = 0; c16 < 8; ++c16) {
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (active) x = *reinterpret_cast<const uint4*>(qrow + 16 * c16);
+        uint4 xq = make_uint4(0u, 0u, 0u, 0u);
+        if (active) xq = *reinterpret_cast<const uint4*>(qrow + 16 * c16);
         uint4 o0, o1;
-        i8x4_to_f16x4(x.x, o0.x, o0.y);
-        i8x4_to_f16x4(x.y, o0.z, o0.w);
-        i8x4_to_f16x4(x.z, o1.x, o1.y);
-        i8x4_to_f16x4(x.w, o1.z, o1.w);
-        *reinterpret_cast<uint4*>(smem + OFFP_Q + (2 * c16) * 2048 + r * 16) = o0;
-        *reinterpret_cast<uint4*>(smem + OFFP_Q + (2 * c16 + 1) * 2048 + r * 16) = o1;
+        i8x4_to_f16x4(xq.x, o0.x, o0.y);
+        i8x4_to_f16x4(xq.y, o0.z, o0.w);
+        i8x4_to_f16x4(xq.z, o1.x, o1.y);
+        i8x4_to_f16x4(xq.w, o1.z, o1.w);
+        *reinterpret_cast<uint4*>(qdst + (2 * c16) * 2048) = o0;
+        *reinterpret_cast<uint4*>(qdst + (2 * c16 + 1) * 2048) = o1;
       }
       fence_proxy_async();
       warp_arrive(PB_Q_READY);
@@ -281,13 +281,11 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
     float m_run = -CUDART_INF_F, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nt && ok; ++j) {
-      const int sb = j % kNS;
-      if (!warp_all(wait_bar(bar(PB_S_FULL + sb), (uint32_t)(j / kNS) & 1u, abort_flag, p.err))) {
+      if (!warp_all(wait_bar(bar(PB_S_FULL + x), (uint32_t)j & 1u, abort_flag, p.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t scol = tmem + lane_base + TMP_S + sb * 128;
       const int t0 = j * kKeys;
       // keys of this tile beyond some row's position (the diagonal) or inactive rows
       const bool masked = ragged || t0 + kKeys - 1 > pos_min;
@@ -310,10 +308,10 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
       mx *= c;
       const float m_new = fmaxf(m_run, mx);
       // Lazy rescale: the reference maximum moves only when the row maximum grew by
-      // more than 8; then O (holding P.V up to tile j - 1) is scaled in place.
+      // more than 8; then O (holding P.V up to key tile j - 1) is scaled in place.
       const bool grow = m_new != -CUDART_INF_F && (m_run == -CUDART_INF_F || m_new > m_run + 8.f);
       if (__any_sync(0xffffffffu, grow && m_run != -CUDART_INF_F)) {
-        if (!warp_all(wait_bar(bar(PB_PV_DONE), (uint32_t)(j - 1) & 1u, abort_flag, p.err))) {
+        if (!warp_all(wait_bar(bar(PB_PV_DONE + x), (uint32_t)(j - 1) & 1u, abort_flag, p.err))) {
           ok = false;
           break;
         }
@@ -322,11 +320,11 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
 #pragma unroll 1
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t v[32];
-          FA3_TMEM_LD32(tmem + lane_base + TMP_O + c4 * 32, v);
+          FA3_TMEM_LD32(o_col + c4 * 32, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-          FA3_TMEM_ST32(tmem + lane_base + TMP_O + c4 * 32, v);
+          FA3_TMEM_ST32(o_col + c4 * 32, v);
         }
       }
       if (grow) {
@@ -360,17 +358,17 @@ __global__ void __launch_bounds__(kThreadsP, 1) gqa_prefill_kernel(const __grid_
       }
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(PB_P_FULL + sb);
+      warp_arrive(PB_P_FULL + x);
     }
     // epilogue: out = v_scale * O / l
-    if (ok && warp_all(wait_bar(bar(PB_PV_DONE), (uint32_t)(nt - 1) & 1u, abort_flag, p.err))) {
+    if (ok && warp_all(wait_bar(bar(PB_PV_DONE + x), (uint32_t)(nt - 1) & 1u, abort_flag, p.err))) {
       tc_fence_after();
       const float inv = (active && l_run > 0.f) ? p.v_scale[g] / l_run : 0.f;
       uint16_t* orow = p.out + (((int64_t)b * p.S + (active ? i : 0)) * p.Hq + h) * kD;
 #pragma unroll 1
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t v[32];
-        FA3_TMEM_LD32(tmem + lane_base + TMP_O + c4 * 32, v);
+        FA3_TMEM_LD32(o_col + c4 * 32, v);
         tmem_wait_ld();
         if (active) {
           uint32_t w[16];
@@ -424,7 +422,7 @@ FA3_API int fa3_prefill_attn_gqa(const int8_t* q, const int8_t* k, const int8_t*
   if (cudaFuncSetAttribute(gqa_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_PREFILL) !=
       cudaSuccess)
     return FA3_ECUDA;
-  const dim3 grid((unsigned)((S + prm.P - 1) / prm.P), (unsigned)Hkv, (unsigned)B);
+  const dim3 grid((unsigned)((S + 2 * prm.P - 1) / (2 * prm.P)), (unsigned)Hkv, (unsigned)B);
   timing_begin(s);
   const cudaError_t le = launch_pdl(gqa_prefill_kernel, grid, dim3(kThreadsP), SMEM_PREFILL, s, prm);
   timing_end(s);

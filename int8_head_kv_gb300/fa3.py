@@ -22,6 +22,7 @@ FA3_DEVERR_POS = 1
 FA3_DEVERR_LENS = 2
 FA3_DEVERR_TIMEOUT = 4
 FA3_DEVERR_PAGE = 8
+FA3_DEVERR_CALIB = 16
 
 
 class FA3Error(RuntimeError):
@@ -45,6 +46,8 @@ _SIGS = {
     "fa3_calibrate_perhead": (_I, [_P, _I64, _I, _I64, _I64, _I64, _D, _P, _P, _P, _SZ, _P]),
     "fa3_qparams": (_I, [_P, _P, _P, _I, _P]),
     "fa3_range_merge": (_I, [_P, _P, _I, _I, _P, _P, _P]),
+    "fa3_calibrate_f32_workspace_size": (_SZ, [_I]),
+    "fa3_calibrate_perhead_f32": (_I, [_P, _I64, _I, _I64, _I64, _I64, _D, _P, _P, _P, _SZ, _P, _P]),
     "fa3_qparams_channel": (_I, [_P, _P, _I, _I, _P, _P, _P]),
     "fa3_calibrate_perchannel": (_I, [_P, _I64, _I, _I64, _I, _I64, _I64, _I64, _D, _P, _P, _P]),
     "fa3_quantize_append_channel": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
@@ -193,6 +196,39 @@ def calibrate_perhead(x: torch.Tensor, ratio: float, min_io: torch.Tensor, max_i
         # The key counts may not have been cleared: never hand this buffer out again.
         _forget_workspace("calib", x.device, stream)
     _check("fa3_calibrate_perhead", st)
+
+
+def calibrate_perhead_f32(x: torch.Tensor, ratio: float, min_io: torch.Tensor, max_io: torch.Tensor,
+                          workspace: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """Per-head Recall-Window calibration of float32 activations, (B, H, S, D) with
+    (S, D) contiguous or (H, N); updates min_io / max_io in place."""
+    _need(x, torch.float32, "x")
+    _need_contig(min_io, torch.float32, "min_io")
+    _need_contig(max_io, torch.float32, "max_io")
+    if x.dim() == 4:
+        B, H, S, D = x.shape
+        if x.stride(3) != 1 or x.stride(2) != D:
+            raise ValueError("x must have contiguous (S, D) planes")
+        L, sb, sh = S * D, x.stride(0), x.stride(1)
+    elif x.dim() == 2:
+        H, L = x.shape
+        if x.stride(1) != 1:
+            raise ValueError("x rows must be contiguous")
+        B, sb, sh = 1, 0, x.stride(0)
+    else:
+        raise ValueError("x must be (B, H, S, D) or (H, N)")
+    if min_io.numel() != H or max_io.numel() != H:
+        raise ValueError("min_io/max_io must hold H values")
+    nbytes = int(lib().fa3_calibrate_f32_workspace_size(H))
+    cached = workspace is None
+    if cached:
+        workspace = _workspace("calib_f32", nbytes, x.device, zero=True, stream=stream)
+    st = lib().fa3_calibrate_perhead_f32(_ptr(x), B, H, L, sb, sh, float(ratio), _ptr(min_io), _ptr(max_io),
+                                         _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream(stream))
+    if st != 0 and cached:
+        _forget_workspace("calib_f32", x.device, stream)
+    _check("fa3_calibrate_perhead_f32", st)
 
 
 def range_merge(mins: torch.Tensor, maxs: torch.Tensor, min_io: torch.Tensor, max_io: torch.Tensor,

@@ -101,6 +101,15 @@ def test_channel_validation(L):
     assert g(D=64) == ERANGE
 
 
+def test_calibrate_f32_validation(L):
+    ws = L.fa3_calibrate_f32_workspace_size(4)
+    call = lambda ratio=0.9999, N=1000, wsb=ws: L.fa3_calibrate_perhead_f32(FAKE, 1, 4, N, 0, N, ratio, FAKE, FAKE,
+                                                                           FAKE, wsb, None, None)
+    assert call(ratio=0.0) == EINVAL
+    assert call(ratio=0.9, N=100000) == ERANGE     # 10001 window starts > 4096
+    assert call(wsb=ws - 1) == EWORKSPACE
+
+
 def test_prefill_validation(L):
     UNALIGNED = ctypes.c_void_p(4096 + 8)
     call = lambda Hq=64, Hkv=8, D=128, q=FAKE, sc=0.09, out=FAKE, S=64: L.fa3_prefill_attn_gqa(

@@ -236,3 +236,58 @@ def test_batches_split_over_shards_then_merged_equal_one_pass():
     F.range_merge(t(np.stack([l[0] for l in locs])), t(np.stack([l[1] for l in locs])), mn, mx)
     assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn))
     assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx))
+
+
+# ------------------------------------------------------------------ float32 input
+def _f32_heads(rng, H, N):
+    x = np.empty((H, N), np.float32)
+    x[0] = rng.standard_normal(N) * 3
+    x[1] = rng.standard_t(3, N) * 0.01
+    x[2] = rng.integers(-3, 4, N)                                  # heavy duplicates
+    x[3] = 0.625                                                   # constant
+    x[4] = np.where(rng.random(N) < 0.5, 0.0, -0.0)                # signed zeros
+    x[5] = np.ldexp(rng.standard_normal(N), rng.integers(-120, 100, N)).astype(np.float32)   # ~220 binades
+    x[6] = rng.standard_normal(N).astype(np.float32) * 1e-30 + 1.0  # fp32 detail below bf16's
+    return x
+
+
+@pytest.mark.parametrize("ratio", [1.0, 0.9999, 0.999, 0.99])
+def test_float32_calibration_bit_exact(ratio):
+    # (B, H, L) = (3, 7, 40000) per batch: N = 120000 values per head; 1 .. 1201 window starts
+    F = fa3()
+    rng = np.random.default_rng(51)
+    B, H, L = 3, 7, 40000
+    batches = [np.stack([_f32_heads(rng, H, L) for _ in range(B)]) for _ in range(2)]   # (B, H, L)
+    omn, omx = O.init_range(H)
+    for x in batches:
+        for h in range(H):
+            lo, hi = O.recall_window(x[:, h].reshape(-1), ratio)
+            O.accumulate(omn[h:h + 1], omx[h:h + 1], np.float32([lo]), np.float32([hi]))
+    mn = torch.full((H,), float("inf"), device="cuda")
+    mx = torch.full((H,), float("-inf"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for k, x in enumerate(batches):
+        if k == 0:                                     # a strided view: (B, H) rows inside a larger array
+            big = torch.zeros(B, H + 2, 1, L, dtype=torch.float32, device="cuda")
+            big[:, 1:H + 1, 0] = torch.from_numpy(x).cuda()
+            xd = big[:, 1:H + 1]
+        else:
+            xd = torch.from_numpy(x).cuda().reshape(B, H, 1, L)
+        F.calibrate_perhead_f32(xd, ratio, mn, mx, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn)), (mn.cpu().numpy(), omn)
+    assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx)), (mx.cpu().numpy(), omx)
+
+
+def test_float32_input_of_bf16_values_matches_the_bf16_path():
+    F = fa3()
+    w = W.mla_tiny()
+    batches = W.mla_inputs(w).calib_q
+    g16 = _gpu_calibrate(F, batches, w.ratio, w.H)
+    mn = torch.full((w.H,), float("inf"), device="cuda")
+    mx = torch.full((w.H,), float("-inf"), device="cuda")
+    for x in batches:
+        F.calibrate_perhead_f32(torch.from_numpy(np.ascontiguousarray(x)).cuda(), w.ratio, mn, mx)
+    assert np.array_equal(_bits(mn.cpu().numpy()), _bits(g16[0]))
+    assert np.array_equal(_bits(mx.cpu().numpy()), _bits(g16[1]))
