@@ -1,7 +1,6 @@
-// Warp-level mma.sync rates on sm_103a: m16n8k32 s8 x s8 -> s32 (the GQA decode
-// score path) and m16n8k16 f16 x f16 -> f32 (its P.V path).  Every warp of every
-// SM runs chains of independent MMAs from registers; reports dense ops per second
-// (2*16*8*32 and 2*16*8*16 per instruction).
+// Warp-level mma.sync m16n8k32 s8 x s8 -> s32 rate on sm_103a (the GQA decode
+// score path).  Every warp of every SM runs chains of independent MMAs from
+// registers; reports dense integer ops per second (2*16*8*32 per instruction).
 #include <cstdio>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -20,39 +19,25 @@ __global__ void __launch_bounds__(256) s8(int* out) {
   for (int k = 0; k < kChains; ++k) s += c[k][0] ^ c[k][1] ^ c[k][2] ^ c[k][3];
   if (s == 0x7fffffff) out[threadIdx.x] = s;
 }
-__global__ void __launch_bounds__(256) f16(float* out) {
-  float c[kChains][4] = {};
-  uint32_t a0 = 0x3c003c00u, a1 = a0, a2 = a0, a3 = a0, b0 = 0x00010001u, b1 = b0;
-  for (int it = 0; it < kIters; ++it)
-#pragma unroll
-    for (int k = 0; k < kChains; ++k)
-      asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-                   : "+f"(c[k][0]), "+f"(c[k][1]), "+f"(c[k][2]), "+f"(c[k][3])
-                   : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  float s = 0;
-#pragma unroll
-  for (int k = 0; k < kChains; ++k) s += c[k][0] + c[k][1] + c[k][2] + c[k][3];
-  if (s == -1.f) out[threadIdx.x] = s;
-}
 int main() {
   int sms = 0; cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
   void* out; cudaMalloc(&out, 4096);
   cudaEvent_t e0, e1; cudaEventCreate(&e0); cudaEventCreate(&e1);
   const int blocks = sms * 4;
-  for (int kind = 0; kind < 2; ++kind) {
+  for (int kind = 0; kind < 1; ++kind) {
     float best = 1e30f;
     for (int rep = 0; rep < 4; ++rep) {
       cudaEventRecord(e0);
-      if (kind == 0) s8<<<blocks, 256>>>((int*)out); else f16<<<blocks, 256>>>((float*)out);
+      s8<<<blocks, 256>>>((int*)out);
       cudaEventRecord(e1);
       cudaEventSynchronize(e1);
       float ms = 0; cudaEventElapsedTime(&ms, e0, e1);
       if (rep > 0 && ms < best) best = ms;
     }
     const double instr = (double)blocks * 8 * kIters * kChains;          // warps x instructions each
-    const double ops = instr * (kind == 0 ? 2.0 * 16 * 8 * 32 : 2.0 * 16 * 8 * 16);
+    const double ops = instr * 2.0 * 16 * 8 * 32;
     printf("{\"probe\": \"mma_sync_%s\", \"best_ms\": %.4f, \"TOPS\": %.1f, \"status\": \"%s\"}\n",
-           kind == 0 ? "s8_m16n8k32" : "f16_m16n8k16", best, ops / (best * 1e-3) / 1e12,
+           "s8_m16n8k32", best, ops / (best * 1e-3) / 1e12,
            cudaGetErrorString(cudaGetLastError()));
   }
   return 0;
