@@ -327,6 +327,36 @@ def run_gpu(args):
     kv_scale = F.qparams(kmn, kmx)
     del cal_big
 
+    # ---- the other attention calls at their workloads' shapes (reported beside the step)
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(z) / n
+
+    def i8(shape):
+        return torch.randint(-127, 128, shape, dtype=torch.int8, device=dev, generator=gen)
+
+    gB, gHq, gHkv, gD, gT = 16, 64, 8, 128, 4096
+    gk, gv, gq = i8((gB, gT, gHkv, gD)), i8((gB, gT, gHkv, gD)), i8((gB, gHq, gD))
+    gs1, gs2 = torch.full((gHq,), 0.01, device=dev), torch.full((gHkv,), 0.01, device=dev)
+    glens = torch.full((gB,), gT, dtype=torch.int32, device=dev)
+    gqa_ms = timed(lambda: F.decode_attn_gqa(gq, gk, gv, gs1, gs2, gs2, glens, 1 / math.sqrt(128)), 50)
+    del gk, gv
+    pS = 4096
+    pq, pk, pv = i8((1, pS, gHq, gD)), i8((1, pS, gHkv, gD)), i8((1, pS, gHkv, gD))
+    pl = torch.full((1,), pS, dtype=torch.int32, device=dev)
+    pout = torch.empty(1, pS, gHq, gD, dtype=torch.bfloat16, device=dev)
+    pre_ms = timed(lambda: F.prefill_attn_gqa(pq, pk, pv, gs1, gs2, gs2, pl, pl, 1 / math.sqrt(128), out=pout), 5)
+    pre_flop = gHq * (pS * (pS + 1) // 2) * 4 * gD
+    del pq, pk, pv, pout
+
     # ---- two independent INT8 caches (rotated per step so consecutive steps share no data)
     NC = 2
     caches, ropes, qs = [], [], []
@@ -494,6 +524,12 @@ def run_gpu(args):
         "decode_call": {"ms": mla_ms, "kv_gbs": kv_gbs, "tflops": flops_per_step() / (mla_ms / 1e3) / 1e12,
                         "kernels": "query pre-pass + mla_decode_kernel + split-K combine",
                         "timing": "CUDA events around the call, second timed pass"},
+        "gqa_decode": {"workload": "llama70b-gqa b16 hq64 hkv8 d128 ctx4096, int8 q/k/v (one call: decode + combine)",
+                       "us_per_call": gqa_ms * 1e3, "kv_gbs": gB * gT * gHkv * gD * 2 / (gqa_ms / 1e3) / 1e9,
+                       "hbm_frac_of_measured": gB * gT * gHkv * gD * 2 / (gqa_ms / 1e3) / 1e9 / hbm},
+        "prefill": {"workload": "llama70b-prefill b1 s4096 t4096 hq64 hkv8 d128 causal, int8 q/k/v",
+                    "us_per_call": pre_ms * 1e3, "tflops": pre_flop / (pre_ms / 1e3) / 1e12,
+                    "frac_of_measured_bf16": pre_flop / (pre_ms / 1e3) / 1e12 / bf16},
         "calibration": {"workload": "B=4 H=128 S=2048 D=192 bf16, ratio 0.9999, Student-t nu=3 x per-head "
                                     "log-uniform [0.1, 10] sigma", "ms_per_batch": cal_ms,
                         "gbs": 4 * H * 2048 * 192 * 2 / (cal_ms / 1e3) / 1e9},

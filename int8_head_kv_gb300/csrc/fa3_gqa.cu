@@ -103,6 +103,12 @@ __device__ __forceinline__ void mma16832_s8(int (&c)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -349,21 +355,29 @@ __global__ void __launch_bounds__(kThreads) gqa_decode_kernel(const GqaArgs p) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o_));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o_));
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float ref0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-    const float ref1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-    const float al0 = exp2f(m0 - ref0), al1 = exp2f(m1 - ref1);
-    m0 = mn0;
-    m1 = mn1;
-    const uint32_t X = pack_f16x2(exp2f(x0 - ref0), exp2f(x1 - ref1));   // token r
-    const uint32_t Y = pack_f16x2(exp2f(x2 - ref0), exp2f(x3 - ref1));   // token r + 8
-    const float2 fx = unpack_f16x2(X), fy = unpack_f16x2(Y);
-    l0 = l0 * al0 + (fx.x + fy.x);
-    l1 = l1 * al1 + (fx.y + fy.y);
+    // Lazy reference: m moves only when a head's maximum grows by more than 8 (so P
+    // stays below 2^8 in fp16), and only then are O and l rescaled.
+    const bool g0 = mx0 > m0 + 8.f, g1 = mx1 > m1 + 8.f;
+    if (__any_sync(0xffffffffu, g0 || g1)) {
+      const float n0 = g0 ? mx0 : m0, n1 = g1 ? mx1 : m1;
+      const float al0 = g0 ? (m0 == -CUDART_INF_F ? 0.f : ex2_approx(m0 - n0)) : 1.f;
+      const float al1 = g1 ? (m1 == -CUDART_INF_F ? 0.f : ex2_approx(m1 - n1)) : 1.f;
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      o[i][0] *= al0; o[i][1] *= al1; o[i][2] *= al0; o[i][3] *= al1;
+      for (int i = 0; i < 8; ++i) {
+        o[i][0] *= al0; o[i][1] *= al1; o[i][2] *= al0; o[i][3] *= al1;
+      }
+      m0 = n0;
+      m1 = n1;
     }
+    const float ref0 = m0 == -CUDART_INF_F ? 0.f : m0;
+    const float ref1 = m1 == -CUDART_INF_F ? 0.f : m1;
+    const uint32_t X = pack_f16x2(ex2_approx(x0 - ref0), ex2_approx(x1 - ref1));   // token r
+    const uint32_t Y = pack_f16x2(ex2_approx(x2 - ref0), ex2_approx(x3 - ref1));   // token r + 8
+    const float2 fx = unpack_f16x2(X), fy = unpack_f16x2(Y);
+    l0 += fx.x + fy.x;
+    l1 += fx.y + fy.y;
     const uint32_t b0 = movmatrix_trans(X), b1 = movmatrix_trans(Y);
 
     // ---- O^T += V^T . P^T; m-tile i covers dims 16r + 2i (row r) and 16r + 2i + 1 (row r + 8)

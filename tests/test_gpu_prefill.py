@@ -37,9 +37,9 @@ def _check_rows(got, ref, ql, what):
         assert not got[b, ql[b]:].any(), f"{what}: rows past q_lens written"
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (4, 4), (16, 8), (32, 8)])
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (4, 4), (16, 8), (32, 8), (128, 8), (64, 1)])
 def test_ragged_with_cached_prefix(Hq, Hkv):
-    # group sizes 8, 1, 2, 4; cached prefixes, a sequence with no new rows, ragged tile tails
+    # group sizes 8, 1, 2, 4, 16, 64; cached prefixes, a sequence with no new rows, ragged tile tails
     F = fa3()
     w = W.prefill_llama70b(B=4, S=200, T=333, Hq=Hq, Hkv=Hkv, q_lens=[200, 37, 0, 129], kv_lens=[333, 37, 5, 300])
     args = _case(w)
