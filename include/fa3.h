@@ -70,7 +70,7 @@ int fa3_version(void);
  * non-NULL, every later call of fa3_decode_attn_mla, fa3_decode_attn_gqa,
  * fa3_prefill_attn_gqa and fa3_calibrate_perhead records start_event on its
  * stream just before its main kernel (the MLA decode, the GQA decode, the
- * prefill attention, the calibration histogram) and
+ * prefill attention, the calibration's pass over its input) and
  * stop_event just after it, so that the caller can time that kernel alone
  * (cudaEventElapsedTime).  The events are cudaEvent_t passed as void*, owned
  * by the caller and must outlive their use; NULL, NULL turns this off.  One
@@ -101,8 +101,9 @@ int fa3_set_kernel_timing(void* start_event, void* stop_event);
  *          first batch; pass them back unchanged to accumulate more batches.
  * workspace  device buffer of fa3_calibrate_workspace_size(H) bytes, 256-byte
  *          aligned, ZERO-FILLED before its first use.  Every successful call
- *          leaves it zero-filled again, so it can be reused without clearing.
- *          (After an FA3_ECUDA error, zero it again.)
+ *          leaves it zero-filled again, so it can be reused without clearing,
+ *          also by a call with another H.  (After an FA3_ECUDA error, zero it
+ *          again.)
  * Results are exact: the same bits as the sorted definition above.
  * ------------------------------------------------------------------------ */
 size_t fa3_calibrate_workspace_size(int H);

@@ -7,31 +7,42 @@
 //   step 3  running min/max of the window ends across calibration batches.
 //
 // GB300 design.  bf16 has only 65536 bit patterns, and a monotone 16-bit key
-// maps them onto the total order of their values (-0 before +0).  Counting
-// each key (a counting sort) therefore carries the whole sorted sequence, so
-// one pass over HBM replaces the sort:
-//   kernel 1  persistent CTAs walk (head, 65528-value chunk) pairs: a 65536-bin
+// maps them onto the total order of their values (-0 before +0), so counting
+// keys (a counting sort) carries the whole sorted sequence and one pass over HBM
+// replaces the sort.  Two paths, both exact:
+//
+// Tail-list path (few windows: N - target_num + 1 small, e.g. the pages' ratio
+// 0.9999).  Every window then starts among the N - t + 1 smallest values and
+// ends among as many largest, so only the two tails of a head matter.
+//   tail_stream_kernel  one persistent CTA per SM walks a contiguous range of
+//             64 KB pieces of the input (head-major); each warp streams its 4 KB
+//             slice of every piece with bulk copies through its own 3-slot ring.
+//             The CTA draws each of its heads' tail thresholds from a fixed sample
+//             of the head (every CTA that meets the head draws the same ones),
+//             rules out most values with packed bf16 min/max tests, and appends the
+//             keys beyond the thresholds to two per-head lists (staged in shared
+//             memory, one global reservation per head and CTA).
+//   window_kernel  per head: counts the listed keys into a shared-memory
+//             histogram, prefix sums give each listed key its rank, and the
+//             windows i = 0 .. N - t pair the i-th smallest listed key with the
+//             matching one of the largest.  A head whose tails turn out too thin
+//             (fewer than N - t + 1 values in a list), whose lists overflow, or
+//             whose sample was degenerate is counted in full by the same CTA and
+//             searched like the histogram path's heads.
+// Histogram path (many windows, or input rows not 16-byte aligned):
+//   hist_kernel  persistent CTAs walk (head, 65528-value chunk) pairs: a 65536-bin
 //             histogram of 16-bit counters packed two per word in 128 KB of
 //             shared memory (a chunk is shorter than 65536, so no counter can
-//             overflow), then the non-zero bins are added into the per-head u32
-//             table in the workspace and cleared, while the next chunk loads.
-//   kernel 2  per head: prefix sums over the 65536 bins; a window can only be
-//             narrowest if it starts at the first copy of a value, so each
-//             occupied bin v with start position P(v) <= N - target_num is a
-//             candidate whose window ends in the bin holding position
-//             P(v) + target_num - 1.  Exact widths (fp32 TwoSum pairs), argmin
-//             with ties to the smallest start, then the running min/max update.  The kernel
-//             zeroes the bins it read, leaving the workspace clean.
-// When few windows exist (N - target_num + 1 <= 16384, e.g. ratio 0.9999), every
-// window starts among the N - target_num + 1 smallest values and ends among the
-// as many largest, so only the two tails of a head need counting: a sampling
-// kernel picks per-head tail thresholds, kernel 1 counts only keys beyond them
-// (HBM-bound instead of atomic-bound), and kernel 2 places the uncounted middle
-// as one block of known size between the tails, checking that each tail holds
-// enough values.  A head that fails the check is counted again in full by a
-// second launch of kernel 2, which returns at once for every other head; the
-// result is the same exact window either way.
+//             overflow), flushed into the per-head u32 table in the workspace.
+//   window_kernel  per head: prefix sums over the 65536 bins; a window can only
+//             be narrowest if it starts at the first copy of a value, so each
+//             occupied bin v with start position P(v) <= N - t is a candidate
+//             whose window ends in the bin holding position P(v) + t - 1.
+// Widths are exact (fp32 TwoSum pairs), the argmin takes ties to the smallest
+// start, and the running min/max update follows.  Every call leaves the
+// workspace zero-filled again for the next one.
 #include "fa3_common.cuh"
+#include "fa3_tc.cuh"
 
 #include <math_constants.h>
 
@@ -39,23 +50,37 @@ namespace fa3 {
 namespace {
 
 constexpr int kBins = 65536;
+// histogram path
 constexpr int kHistThreads = 1024;
 constexpr int kChunk = 65528;                       // values per histogram CTA (multiple of 8, < 65536)
 constexpr int kGroupsPerThread = (kChunk / 8 + kHistThreads - 1) / kHistThreads;   // 8
 constexpr int kScalarPerThread = (kChunk + kHistThreads - 1) / kHistThreads;       // 64
+// window search
 constexpr int kWinThreads = 1024;
 constexpr int kBinsPerThread = kBins / kWinThreads;  // 64
-constexpr int kCandCap = 16384;     // window starts the fast search can table (N - t + 1 <= kCandCap)
-constexpr int kSampleUnits = 512;   // strided samples per head for the tail thresholds (16-byte groups or values)
-constexpr int kSampleThreads = 256;
-constexpr int kTailThreads = 256;
-constexpr int kTailGroups = 8;      // 16-byte groups per thread of the tail-count kernel
+constexpr int kCandCap = 16384;     // window starts the table search handles (N - t + 1 <= kCandCap)
+// tail-list path
+constexpr int kStreamThreads = 512;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStageBytes = 65536;  // one piece of a row
+constexpr int kStages = 3;          // ring depth (per warp: each warp streams its own slices)
+constexpr int kSliceBytes = kStageBytes / kStreamWarps;              // a warp's 4 KB share of a piece
+constexpr int kGroupsPerStage = kStageBytes / 16 / kStreamThreads;   // 8 groups of 8 values per lane
+constexpr int kListCap = 16384;     // tail keys per list and head in the workspace
+constexpr int kStageCap = 4096;     // tail keys per list a CTA stages for one head
+constexpr int kSampleGroups = 2048; // strided 16-byte groups per head for the tail thresholds
+constexpr int kMaxRank = 64;        // largest sample rank the tail thresholds are drawn at
+// ring, then two staging buffers (two heads) of two lists each
+constexpr size_t kStreamSmem = (size_t)kStages * kStageBytes + 4 * kStageCap * sizeof(uint16_t);
+static_assert(kGroupsPerStage == 8, "the per-thread min / max tree below takes eight groups");
 
-// Per-head state of the tail-only path, in the workspace after the counters.
-// key_lo / key_hi: count keys <= key_lo or >= key_hi (key_lo = 0xffff: all keys);
-// flag: the tails were too thin, count this head again in full.
+// Per-head state of the tail-list path, in the workspace after the counters:
+// n_lo / n_hi: keys appended to the low / high list (may exceed kListCap: then
+// the lists are incomplete); flag: the head's sample was degenerate, or one CTA
+// met more than kStageCap keys of one list (the head is then counted in full).
+// The window kernel reads and re-zeroes it.
 struct TailInfo {
-  uint32_t key_lo, key_hi, flag, pad;
+  uint32_t n_lo, n_hi, flag, pad;
 };
 
 // Order-preserving 16-bit key of a bf16 value: positive values get the top bit
@@ -77,10 +102,6 @@ __device__ __forceinline__ uint32_t bf16x2_keys(uint32_t w) {
 __device__ __forceinline__ void count16(uint32_t* bins, uint32_t key) {
   atomicAdd(&bins[key >> 1], 1u << ((key & 1u) << 4));
 }
-// Counts `key` only if it lies in a counted tail (key <= lo or key >= hi).
-__device__ __forceinline__ void count16_tails(uint32_t* bins, uint32_t key, uint32_t lo, uint32_t hi) {
-  if (key <= lo || key >= hi) count16(bins, key);
-}
 
 // Packed bf16x2 min / max (IEEE: -0 == +0).
 __device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
@@ -94,36 +115,26 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Counts the 8 values of one 16-byte group (only keys <= lo or >= hi).  The common
-// case, no counted key in the whole warp's groups, is ruled out by comparing the
-// group's bf16 min and max with the values of the thresholds (strictly, so a tie or
-// a signed zero at a threshold always takes the exact per-key path) and one vote.
-// When the whole warp holds one and the same 16 bytes made of a single repeated
-// value (a constant head), one lane adds 256 at once instead of 256 conflicting
-// atomics.
-__device__ __forceinline__ void count_group(uint32_t* bins, const uint4 v, bool valid, uint32_t lo, uint32_t hi,
-                                            float v_lo, float v_hi) {
-  const uint32_t mn = bmin2(bmin2(v.x, v.y), bmin2(v.z, v.w)), mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
-  const float gmin = fminf(__uint_as_float(mn << 16), __uint_as_float(mn & 0xffff0000u));
-  const float gmax = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
-  const bool maybe = valid && !(gmin > v_lo && gmax < v_hi);
-  if (!__any_sync(0xffffffffu, maybe)) return;
+// Counts the 8 values of one 16-byte group.  When the whole warp holds one and
+// the same 16 bytes made of a single repeated value (a constant head), one lane
+// adds 256 at once instead of 256 conflicting atomics.
+__device__ __forceinline__ void count_group(uint32_t* bins, const uint4 v, bool valid) {
   const uint32_t w0 = __shfl_sync(0xffffffffu, v.x, 0);
   const bool uniform = __all_sync(0xffffffffu, valid && v.x == w0 && v.y == w0 && v.z == w0 && v.w == w0 &&
                                                    (w0 >> 16) == (w0 & 0xffffu));
   if (uniform) {
     if ((threadIdx.x & 31) == 0) {
       const uint32_t key = bf16x2_keys(w0) & 0xffffu;
-      if (key <= lo || key >= hi) atomicAdd(&bins[key >> 1], 256u << ((key & 1u) << 4));
+      atomicAdd(&bins[key >> 1], 256u << ((key & 1u) << 4));
     }
     return;
   }
-  if (!maybe) return;
+  if (!valid) return;
   const uint32_t k[4] = {bf16x2_keys(v.x), bf16x2_keys(v.y), bf16x2_keys(v.z), bf16x2_keys(v.w)};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    count16_tails(bins, k[i] & 0xffffu, lo, hi);
-    count16_tails(bins, k[i] >> 16, lo, hi);
+    count16(bins, k[i] & 0xffffu);
+    count16(bins, k[i] >> 16);
   }
 }
 
@@ -132,8 +143,7 @@ __device__ __forceinline__ void count_group(uint32_t* bins, const uint4 v, bool 
 // the loads of the next chunk are already in flight.
 __global__ void __launch_bounds__(kHistThreads, 1)
 hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t N,
-            int chunks_per_head, int total_chunks, uint32_t* __restrict__ counts, int vec,
-            const TailInfo* __restrict__ tails) {
+            int chunks_per_head, int total_chunks, uint32_t* __restrict__ counts, int vec) {
   pdl_wait();
   pdl_launch_dependents();
   extern __shared__ uint4 smem_hist[];
@@ -171,16 +181,11 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
   while (ci < total_chunks) {
     int h; int64_t n0, n1;
     chunk_span(ci, h, n0, n1);
-    uint32_t lo = 0xffffu, hi = 0x10000u;       // count every key ...
-    if (tails) { lo = tails[h].key_lo; hi = tails[h].key_hi; }   // ... or only the tails
-    // the thresholds as values (-inf / +inf when everything is counted)
-    const float v_lo = lo >= 0xffffu ? CUDART_INF_F : key_value(lo);
-    const float v_hi = hi > 0xffffu ? -CUDART_INF_F : key_value(hi);
     if (vec) {
 #pragma unroll
       for (int k = 0; k < kGroupsPerThread; ++k) {
         const int64_t n = n0 + 8 * (int64_t)(tid + k * kHistThreads);
-        count_group(bins, v[k], n < n1, lo, hi, v_lo, v_hi);
+        count_group(bins, v[k], n < n1);
       }
     } else {
       const uint16_t* xh = x + (int64_t)h * stride_h;
@@ -188,20 +193,16 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
         const int64_t n = n0 + tid + (int64_t)k * kHistThreads;
         if (n < n1) {
           const int64_t b = n / L, l = n - b * L;
-          count16_tails(bins, bf16x2_keys(xh[b * stride_b + l]) & 0xffffu, lo, hi);
+          count16(bins, bf16x2_keys(xh[b * stride_b + l]) & 0xffffu);
         }
       }
     }
     __syncthreads();
     const int cn = ci + gridDim.x;
     if (vec && cn < total_chunks) load_chunk(cn, v);
-    // flush the non-zero counters into the head's table and clear them (only the
-    // counted key ranges can hold any: groups of 8 bins [0, lo] and [hi, 0xffff])
+    // flush the non-zero counters into the head's table and clear them
     uint32_t* ch = counts + (int64_t)h * kBins;
-    const int g_lo = lo >= 0xffffu ? kBins / 8 : (int)(lo >> 3) + 1, g_hi = hi > 0xffffu ? kBins / 8 : (int)(hi >> 3);
-    for (int i0 = tid; i0 < kBins / 8; i0 += kHistThreads) {
-      const int i = i0 < g_lo ? i0 : (g_hi > g_lo ? g_hi + (i0 - g_lo) : kBins / 8);
-      if (i >= kBins / 8) break;
+    for (int i = tid; i < kBins / 8; i += kHistThreads) {
       const uint4 q = smem_hist[i];
       if ((q.x | q.y | q.z | q.w) == 0u) continue;
       const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -218,186 +219,321 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
   }
 }
 
-// Tail-only counting for 16-byte aligned rows: grid (ranges of a row, rows b * H + h);
-// each thread loads kTailGroups groups of 8 values at once, rules most of them out
-// with the packed min / max test of count_group, and adds the keys of the rest
-// straight into the head's u32 table (they are rare: a few 1e-4 of the values).
-__global__ void __launch_bounds__(kTailThreads)
-tail_count_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int H,
-                  uint32_t* __restrict__ counts, const TailInfo* __restrict__ tails) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int row = blockIdx.y, h = row % H, b = row / H;
-  const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)b * stride_b + (int64_t)h * stride_h);
-  const int64_t groups = L / 8;
-  const int64_t g0 = (int64_t)blockIdx.x * (kTailThreads * kTailGroups) + threadIdx.x;
-  const uint32_t lo = tails[h].key_lo, hi = tails[h].key_hi;
-  const float v_lo = lo >= 0xffffu ? CUDART_INF_F : key_value(lo);
-  const float v_hi = hi > 0xffffu ? -CUDART_INF_F : key_value(hi);
-  uint32_t* ch = counts + (int64_t)h * kBins;
-  uint4 v[kTailGroups];
+// Shared state of tail_stream_kernel beside its dynamic buffers.
+struct StreamShared {
+  uint64_t full[kStreamWarps][kStages];  // a warp's ring slot filled (bulk copy bytes landed)
+  uint32_t part[2][2][kStreamWarps];  // per-warp counts of the threshold search (two heads), double-buffered
+  uint32_t gbase[2];               // global list positions reserved by a flush
+  uint32_t cnt[2][2];              // per staging buffer: keys met for the low / high list (staged: the first kStageCap)
+  uint32_t abort;                  // a bounded wait gave up: stop using the ring
+};
+
+// One thread's share of a head's sample: kSampleUnits strided 16-byte groups
+// (group g of the head's N / 8 at g * (N / 8) / kSampleGroups; the positions
+// depend only on the head's size, so every CTA that meets the head draws the
+// same sample).
+constexpr int kSampleUnits = kSampleGroups / kStreamThreads;   // 4 groups per thread
+__device__ __forceinline__ void load_sample(const uint16_t* __restrict__ xh, int64_t L, int64_t stride_b,
+                                            unsigned long long N, uint4 (&q)[kSampleUnits]) {
+  const unsigned long long units = N / 8;
 #pragma unroll
-  for (int k = 0; k < kTailGroups; ++k) {
-    const int64_t g = g0 + (int64_t)k * kTailThreads;
-    v[k] = g < groups ? __ldcs(src + g) : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int k = 0; k < kTailGroups; ++k) {
-    const bool valid = g0 + (int64_t)k * kTailThreads < groups;
-    const uint32_t mn = bmin2(bmin2(v[k].x, v[k].y), bmin2(v[k].z, v[k].w));
-    const uint32_t mx = bmax2(bmax2(v[k].x, v[k].y), bmax2(v[k].z, v[k].w));
-    const float gmin = fminf(__uint_as_float(mn << 16), __uint_as_float(mn & 0xffff0000u));
-    const float gmax = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
-    if (valid && !(gmin > v_lo && gmax < v_hi)) {
-      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t k2 = bf16x2_keys(w[i]);
-        const uint32_t a = k2 & 0xffffu, c = k2 >> 16;
-        if (a <= lo || a >= hi) atomicAdd(&ch[a], 1u);
-        if (c <= lo || c >= hi) atomicAdd(&ch[c], 1u);
-      }
-    }
+  for (int j = 0; j < kSampleUnits; ++j) {
+    const unsigned long long u = (unsigned long long)(threadIdx.x + j * kStreamThreads) * units / kSampleGroups;
+    const int64_t n = (int64_t)u * 8, b = n / L, l = n - b * L;
+    q[j] = *reinterpret_cast<const uint4*>(xh + b * stride_b + l);
   }
 }
-
-// Warp-wide: the bin of a 256-bin histogram holding its r-th smallest element
-// (from_top: r-th largest) and that element's 1-based rank inside the bin.  Lane l
-// owns 8 consecutive bins; r must not exceed the histogram's total.
-__device__ __forceinline__ void select_bin(const uint32_t* hist, uint32_t r, bool from_top, uint32_t& bin,
-                                           uint32_t& rank) {
-  const int lane = threadIdx.x & 31;
-  uint32_t c[8], sum = 0;
+// The smallest and largest key of the thread's sampled values.
+struct SampleExt {
+  uint32_t mn, mx;
+};
+__device__ __forceinline__ SampleExt sample_extremes(const uint4 (&q)[kSampleUnits]) {
+  SampleExt e{0xffffu, 0u};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int i = 8 * lane + j;
-    c[j] = hist[from_top ? 255 - i : i];
-    sum += c[j];
-  }
-  uint32_t incl = sum;
+  for (int j = 0; j < kSampleUnits; ++j) {
+    const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const uint32_t m = __ballot_sync(0xffffffffu, incl >= r);
-  const int owner = m ? __ffs(m) - 1 : 31;
-  uint32_t b = 0, rk = 1, acc = incl - sum;
-  if (lane == owner) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (acc + c[j] >= r) { const int i = 8 * lane + j; b = (uint32_t)(from_top ? 255 - i : i); rk = r - acc; break; }
-      acc += c[j];
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t k2 = bf16x2_keys(w[i]), a = k2 & 0xffffu, c = k2 >> 16;
+      e.mn = min(e.mn, min(a, c));
+      e.mx = max(e.mx, max(a, c));
     }
   }
-  bin = __shfl_sync(0xffffffffu, b, owner);
-  rank = __shfl_sync(0xffffffffu, rk, owner);
+  return e;
 }
 
-// Tail thresholds of head h from kSampleUnits strided samples (16-byte groups when
-// vec, single values otherwise).  With S sampled keys and p = (N - t + 1) / N, the
-// sample's r-th smallest key, r = 3 S p + 4, lies above the N - t + 1 smallest
-// values of the head unless the sample over-represents the low tail badly (the
-// window kernel checks and falls back); key_lo is that key, key_hi the r-th
-// largest.  The order statistics come from a two-level radix select on the key
-// bytes.  Overlapping tails count everything.
-__global__ void __launch_bounds__(kSampleThreads)
-tail_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t N,
-            unsigned long long span, int vec, TailInfo* __restrict__ tails) {
-  pdl_wait();
-  pdl_launch_dependents();
-  constexpr int kUnits = kSampleUnits / kSampleThreads;    // 16 samples per thread
-  constexpr int kWarps = kSampleThreads / 32;
-  __shared__ uint32_t whist[kWarps][256];        // per-warp high-byte histograms
-  __shared__ uint32_t hist[3][256];              // high byte; low byte in the low bin; low byte in the high bin
-  __shared__ uint32_t sel[4];                    // b_lo, b_hi, residual rank in b_lo, in b_hi
-  const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
-  for (int i = tid; i < kWarps * 256; i += kSampleThreads) (&whist[0][0])[i] = 0u;
-  for (int i = tid; i < 3 * 256; i += kSampleThreads) (&hist[0][0])[i] = 0u;
-  const uint16_t* xh = x + (int64_t)h * stride_h;
-  const int64_t units = vec ? N / 8 : N;
-  const int per = vec ? 8 : 1;
-  // all loads first (independent), keys kept in registers for both passes
-  uint4 q[kUnits];
-  bool ok[kUnits];
+// Tail thresholds of two heads at once, block-wide: key_lo = the r-th smallest of
+// the threads' sample minima, key_hi = the r-th largest of their maxima (binary
+// searches over the 16-bit keys, one ballot count per step).  r threads hold a
+// sampled key at or below key_lo, so at least r of the S sampled keys are; for r
+// well below the thread count it sits near the sample's r-th smallest key.  With
+// p = (N - t + 1) / N and r = 3 S p + 4, the low list (keys <= key_lo) then holds
+// the N - t + 1 smallest values of the head unless the sample over-represents the
+// low tail badly (the window kernel checks and falls back); likewise the high
+// list.  Thresholds that meet mark the head degenerate.
+struct Thresholds {
+  uint32_t lo, hi;
+  bool degenerate;
+};
+__device__ void select_tails(const SampleExt (&e)[2], uint32_t r, StreamShared& sh, Thresholds (&t)[2]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t a_lo[2] = {0u, 0u}, b_lo[2] = {0xffffu, 0xffffu}, a_hi[2] = {0u, 0u}, b_hi[2] = {0xffffu, 0xffffu};
+#pragma unroll 1
+  for (int it = 0; it < 16; ++it) {
+    uint32_t m_lo[2], m_hi[2];
 #pragma unroll
-  for (int j = 0; j < kUnits; ++j) {
-    const int g = tid + j * kSampleThreads;
-    const int64_t u = (int64_t)((unsigned long long)g * (unsigned long long)units / kSampleUnits);
-    ok[j] = u < units;
-    q[j] = make_uint4(0u, 0u, 0u, 0u);
-    if (ok[j]) {
-      const int64_t n = u * per, b = n / L, l = n - b * L;
-      if (vec) q[j] = *reinterpret_cast<const uint4*>(xh + b * stride_b + l);
-      else q[j].x = xh[b * stride_b + l];
+    for (int u = 0; u < 2; ++u) {
+      m_lo[u] = (a_lo[u] + b_lo[u]) >> 1;
+      m_hi[u] = (a_hi[u] + b_hi[u] + 1u) >> 1;
+      const uint32_t c = (uint32_t)__popc(__ballot_sync(0xffffffffu, e[u].mn <= m_lo[u])) |
+                         ((uint32_t)__popc(__ballot_sync(0xffffffffu, e[u].mx >= m_hi[u])) << 16);
+      if (lane == 0) sh.part[it & 1][u][warp] = c;
     }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      uint32_t tot = lane < kStreamWarps ? sh.part[it & 1][u][lane] : 0u;
+      tot = __reduce_add_sync(0xffffffffu, tot);
+      if ((tot & 0xffffu) >= r) b_lo[u] = m_lo[u]; else a_lo[u] = m_lo[u] + 1u;
+      if ((tot >> 16) >= r) a_hi[u] = m_hi[u]; else b_hi[u] = m_hi[u] - 1u;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) t[u] = Thresholds{a_lo[u], a_hi[u], !(a_lo[u] + 1u < a_hi[u])};
+}
+
+// Stages one tail key (one lane; the keys are rare) in staging buffer `buf`.  Keys
+// past kStageCap are counted, not kept: the flush then flags the head for the
+// full count.
+__device__ __forceinline__ void stage_key(uint16_t* loc, StreamShared& sh, int buf, int side, uint32_t key) {
+  const uint32_t pos = atomicAdd(&sh.cnt[buf][side], 1u);
+  if (pos < (uint32_t)kStageCap) loc[(2 * buf + side) * kStageCap + pos] = (uint16_t)key;
+}
+
+// Moves staging buffer `buf` (one head's keys) into the head's lists (block-wide):
+// one reservation of the full count per list, so the head's count stays exact.
+__device__ void flush_tails(uint16_t* loc, StreamShared& sh, int buf, TailInfo* ti, uint16_t* list) {
+  const int tid = threadIdx.x;
+  __syncthreads();
+  const uint32_t c0 = sh.cnt[buf][0], c1 = sh.cnt[buf][1];
+  if (tid == 0) {
+    sh.gbase[0] = c0 ? atomicAdd(&ti->n_lo, c0) : 0u;
+    sh.gbase[1] = c1 ? atomicAdd(&ti->n_hi, c1) : 0u;
+    if (c0 > (uint32_t)kStageCap || c1 > (uint32_t)kStageCap) ti->flag = 1u;
   }
   __syncthreads();
-  // fn(key, valid) is called by every lane the same number of times (warp-uniform)
-  auto for_keys = [&](auto&& fn) {
-#pragma unroll
-    for (int j = 0; j < kUnits; ++j) {
-      if (vec) {
-        const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t k2 = bf16x2_keys(w[i]);
-          fn(k2 & 0xffffu, ok[j]);
-          fn(k2 >> 16, ok[j]);
-        }
-      } else {
-        fn(bf16x2_keys(q[j].x) & 0xffffu, ok[j]);
-      }
+  const uint32_t g0 = sh.gbase[0], g1 = sh.gbase[1];
+  const uint32_t n0 = min(c0, (uint32_t)kStageCap), n1 = min(c1, (uint32_t)kStageCap);
+  const uint16_t* b = loc + 2 * buf * kStageCap;
+  for (uint32_t i = tid; i < n0 && g0 + i < (uint32_t)kListCap; i += kStreamThreads) list[g0 + i] = b[i];
+  for (uint32_t i = tid; i < n1 && g1 + i < (uint32_t)kListCap; i += kStreamThreads)
+    list[kListCap + g1 + i] = b[kStageCap + i];
+  __syncthreads();
+  if (tid == 0) { sh.cnt[buf][0] = 0u; sh.cnt[buf][1] = 0u; }
+}
+
+// Packed bf16 compares, 0xffff per true half (IEEE: -0 == +0).
+__device__ __forceinline__ uint32_t ble2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("set.le.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bge2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Tail-list pass (16-byte aligned rows).  The input is cut into items of up to
+// kStageBytes of one row, numbered head-major (head, batch row, piece); CTA g
+// takes the contiguous items [g T / G, (g + 1) T / G).  Warp w handles the 4 KB
+// slice w of every item: its lane 0 streams the slices with bulk copies into the
+// warp's own kStages-slot ring (one mbarrier per slot), so warps run independently
+// of one another between head changes (where the whole CTA meets only when it
+// meets a third head).  A bounded wait that gives up flags every head of the CTA
+// for the full count, so the result stays exact.
+__global__ void __launch_bounds__(kStreamThreads, 1)
+tail_stream_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t B,
+                   unsigned long long N, uint32_t rank, int64_t total_items, TailInfo* __restrict__ tails,
+                   uint16_t* __restrict__ lists) {
+  extern __shared__ __align__(128) uint8_t sm_stream[];
+  uint16_t* loc = reinterpret_cast<uint16_t*>(sm_stream + kStages * kStageBytes);   // [2][2][kStageCap]
+  __shared__ StreamShared sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint8_t* ring = sm_stream + warp * kStages * kSliceBytes;                           // this warp's slots
+  const int64_t row_bytes = 2 * L;
+  const int64_t pieces = (row_bytes + kStageBytes - 1) / kStageBytes, per_head = B * pieces;
+  const uint32_t last_bytes = (uint32_t)(row_bytes - (pieces - 1) * kStageBytes);
+  const int64_t i0 = (int64_t)blockIdx.x * total_items / gridDim.x;
+  const int n_items = (int)((int64_t)(blockIdx.x + 1) * total_items / gridDim.x - i0);
+  const int64_t h_first = i0 / per_head, h_last = (i0 + n_items - 1) / per_head;
+  if (tid == 0) {
+    sh.cnt[0][0] = sh.cnt[0][1] = sh.cnt[1][0] = sh.cnt[1][1] = 0u;
+    sh.abort = 0u;
+  }
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sh.full[warp][s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // The samples of the first head and of the next one (a range spans at most two
+  // heads unless heads are small) go out before the ring fills the memory queues.
+  uint4 q0[kSampleUnits], q1[kSampleUnits];
+  load_sample(x + h_first * stride_h, L, stride_b, N, q0);
+  if (h_last > h_first) load_sample(x + (h_first + 1) * stride_h, L, stride_b, N, q1);
+  __syncthreads();                                   // barriers initialised
+
+  // The bytes of this warp's slice of an item whose piece holds `bytes`.
+  auto slice_of = [&](uint32_t bytes) {
+    const int64_t r = (int64_t)bytes - (int64_t)warp * kSliceBytes;
+    return (uint32_t)(r <= 0 ? 0 : (r < kSliceBytes ? r : kSliceBytes));
+  };
+  // Producer state (lane 0 of each warp): the next item to load, as (row b, head h)
+  // and the bytes left in its row from it on.
+  int64_t qb = i0 % per_head / pieces, qh = h_first, qrem = row_bytes - (i0 % per_head % pieces) * kStageBytes;
+  const uint8_t* q_src = reinterpret_cast<const uint8_t*>(x + qb * stride_b + qh * stride_h) + (row_bytes - qrem);
+  int q_next = 0;
+  auto produce = [&]() {                             // lane 0: this warp's slice of item q_next
+    const int slot = q_next % kStages;
+    const uint32_t bytes = slice_of((uint32_t)min(qrem, (int64_t)kStageBytes));
+    const uint32_t bar = smem_u32(&sh.full[warp][slot]);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the warp's reads of the slot came first
+    mbar_expect_tx(bar, bytes);                      // (a zero-byte slice completes the phase at once)
+    if (bytes) bulk_g2s(smem_u32(ring + slot * kSliceBytes), q_src + warp * kSliceBytes, bytes, bar);
+    ++q_next;
+    if (qrem > kStageBytes) {
+      qrem -= kStageBytes;
+      q_src += kStageBytes;
+    } else {
+      qrem = row_bytes;
+      if (++qb == B) { qb = 0; ++qh; }
+      q_src = reinterpret_cast<const uint8_t*>(x + qb * stride_b + qh * stride_h);
     }
   };
-  // high-byte histogram, one atomic per distinct bin and warp step (the sample
-  // concentrates in a few bins, so per-lane atomics would mostly collide)
-  const int lane = tid & 31;
-  for_keys([&](uint32_t key, bool valid) {
-    const uint32_t bin = valid ? (key >> 8) : 256u;
-    const uint32_t m = __match_any_sync(0xffffffffu, bin);
-    if (valid && lane == __ffs(m) - 1) atomicAdd(&whist[warp][bin], (uint32_t)__popc(m));
-  });
-  __syncthreads();
-  for (int i = tid; i < 256; i += kSampleThreads) {
-    uint32_t c = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) c += whist[w][i];
-    hist[0][i] = c;
+  if (lane == 0)
+    for (int s = 0; s < kStages && s < n_items; ++s) produce();
+  // Thresholds of the first two heads in one search, while the ring fills.
+  Thresholds th[2];
+  {
+    const SampleExt e[2] = {sample_extremes(q0), h_last > h_first ? sample_extremes(q1) : sample_extremes(q0)};
+    select_tails(e, rank, sh, th);
   }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t total = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) total += hist[0][8 * lane + j];
-    total = __reduce_add_sync(0xffffffffu, total);
-    const double want = 3.0 * (double)total * (double)span / (double)N + 4.0;
-    const uint32_t r = want >= (double)total ? total : (uint32_t)want;
-    uint32_t b_lo = 256u, b_hi = 0u, r_lo = 1u, r_hi = 1u;
-    if (r > 0 && r < total) {
-      select_bin(hist[0], r, false, b_lo, r_lo);
-      select_bin(hist[0], r, true, b_hi, r_hi);
-    }                                            // else too few samples: count everything
-    if (lane == 0) { sel[0] = b_lo; sel[1] = b_hi; sel[2] = r_lo; sel[3] = r_hi; }
-  }
-  __syncthreads();
-  const uint32_t s0 = sel[0], s1 = sel[1];
-  for_keys([&](uint32_t key, bool valid) {
-    if (valid && (key >> 8) == s0) atomicAdd(&hist[1][key & 0xffu], 1u);
-    if (valid && (key >> 8) == s1) atomicAdd(&hist[2][key & 0xffu], 1u);
-  });
-  __syncthreads();
-  if (warp == 0) {
-    TailInfo ti{0xffffu, 0x10000u, 0u, 0u};
-    if (s0 < 256u) {
-      uint32_t k_lo, k_hi, rk;
-      select_bin(hist[1], sel[2], false, k_lo, rk);
-      select_bin(hist[2], sel[3], true, k_hi, rk);
-      const uint32_t lo = (s0 << 8) | k_lo, hi = (s1 << 8) | k_hi;
-      if (lo + 1u < hi) { ti.key_lo = lo; ti.key_hi = hi; }
+
+  // Consumer state (every thread): the head of the current item, the items left in
+  // that head, and the item's piece index in its row.  Head h_first + i stages its
+  // keys in buffer i & 1; a head change needs no barrier unless the CTA meets a
+  // third head (small heads), whose buffer must first be flushed.
+  int64_t ph = h_first, left = per_head - i0 % per_head;
+  int64_t pc = i0 % per_head % pieces;
+  int64_t cur = -1;
+  int buf = 0;
+  uint32_t key_lo = 0, key_hi = 0, mid2 = 0, vlo2 = 0, vhi2 = 0;
+  bool skip = true;
+  for (int j = 0; j < n_items; ++j) {
+    if (ph != cur) {
+      buf = (int)((ph - h_first) & 1);
+      if (ph > h_first + 1) {                         // a third head or later
+        flush_tails(loc, sh, buf, tails + (ph - 2), lists + (ph - 2) * 2 * kListCap);
+        uint4 q[kSampleUnits];
+        load_sample(x + ph * stride_h, L, stride_b, N, q);
+        const SampleExt e[2] = {sample_extremes(q), sample_extremes(q)};
+        Thresholds t2[2];
+        select_tails(e, rank, sh, t2);
+        if (buf) th[1] = t2[0]; else th[0] = t2[0];
+      }
+      const Thresholds t = buf ? th[1] : th[0];
+      key_lo = t.lo;
+      key_hi = t.hi;
+      skip = t.degenerate;
+      if (skip && tid == 0) tails[ph].flag = 1u;
+      const float v_lo = key_value(key_lo), v_hi = key_value(key_hi);
+      vlo2 = (__float_as_uint(v_lo) >> 16) * 0x10001u;
+      vhi2 = (__float_as_uint(v_hi) >> 16) * 0x10001u;
+      // a bf16 pair strictly between the thresholds: stands in for bytes past a short piece
+      mid2 = (__float_as_uint(key_value(key_lo + 1u)) >> 16) * 0x10001u;
+      cur = ph;
     }
-    if (lane == 0) tails[h] = ti;
+    const int slot = j % kStages;
+    const bool ok = warp_all(wait_bar(smem_u32(&sh.full[warp][slot]), (uint32_t)((j / kStages) & 1), &sh.abort, nullptr));
+    const uint32_t bytes = slice_of(pc == pieces - 1 ? last_bytes : (uint32_t)kStageBytes);
+    const uint8_t* slot_base = ring + slot * kSliceBytes;
+    if (ok && !skip && bytes != 0u) {
+      const uint8_t* st = slot_base + 16 * lane;
+      // bf16 min / max of each of the lane's groups; the groups past a short slice
+      // read as values strictly between the thresholds
+      uint32_t gmn[kGroupsPerStage], gmx[kGroupsPerStage];
+      if (bytes == (uint32_t)kSliceBytes) {
+#pragma unroll
+        for (int k = 0; k < kGroupsPerStage; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(st + 16 * 32 * k);
+          gmn[k] = bmin2(bmin2(v.x, v.y), bmin2(v.z, v.w));
+          gmx[k] = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kGroupsPerStage; ++k) {
+          gmn[k] = gmx[k] = mid2;
+          if (16u * (uint32_t)(lane + 32 * k) < bytes) {
+            const uint4 v = *reinterpret_cast<const uint4*>(st + 16 * 32 * k);
+            gmn[k] = bmin2(bmin2(v.x, v.y), bmin2(v.z, v.w));
+            gmx[k] = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+          }
+        }
+      }
+      const uint32_t tmn = bmin2(bmin2(bmin2(gmn[0], gmn[1]), bmin2(gmn[2], gmn[3])),
+                                 bmin2(bmin2(gmn[4], gmn[5]), bmin2(gmn[6], gmn[7])));
+      const uint32_t tmx = bmax2(bmax2(bmax2(gmx[0], gmx[1]), bmax2(gmx[2], gmx[3])),
+                                 bmax2(bmax2(gmx[4], gmx[5]), bmax2(gmx[6], gmx[7])));
+      // packed IEEE compares: a value at or beyond a threshold's value may be a tail key
+      const bool flagged = (ble2(tmn, vlo2) | bge2(tmx, vhi2)) != 0u;
+      // rare: the warp's flagged lanes, four at a time, hand their eight groups each
+      // to the 32 lanes, which locate the candidates and run the exact key test
+      uint32_t pending = __ballot_sync(0xffffffffu, flagged);
+      while (pending != 0u) {
+        int src = 32;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int l = pending ? __ffs(pending) - 1 : 32;
+          if (pending) pending &= pending - 1u;
+          if ((lane >> 3) == r) src = l;
+        }
+        const int k = lane & 7;
+        if (src < 32 && 16u * (uint32_t)(src + 32 * k) < bytes) {
+          const uint4 g = *reinterpret_cast<const uint4*>(slot_base + 16 * (src + 32 * k));
+          const uint32_t w[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if ((ble2(w[i], vlo2) | bge2(w[i], vhi2)) == 0u) continue;
+            const uint32_t k2 = bf16x2_keys(w[i]);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {            // the exact test, on keys
+              const uint32_t key = half ? k2 >> 16 : k2 & 0xffffu;
+              if (key <= key_lo) stage_key(loc, sh, buf, 0, key);
+              else if (key >= key_hi) stage_key(loc, sh, buf, 1, key);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();                                    // the warp is done with the slot: refill it
+    if (lane == 0 && q_next < n_items && !*reinterpret_cast<volatile uint32_t*>(&sh.abort)) produce();
+    if (++pc == pieces) pc = 0;
+    if (--left == 0) { ++ph; left = per_head; }
   }
+  if (lane == 0 && *reinterpret_cast<volatile uint32_t*>(&sh.abort)) {
+    // gave up: the heads of this range are counted in full; the warp's copies still
+    // in flight (its last slots filled) get one more bounded wait before the CTA exits
+    for (int64_t h = h_first; h <= h_last; ++h) tails[h].flag = 1u;
+    uint32_t no_abort = 0u;
+    for (int jj = q_next > kStages ? q_next - kStages : 0; jj < q_next; ++jj)
+      wait_bar(smem_u32(&sh.full[warp][jj % kStages]), (uint32_t)((jj / kStages) & 1), &no_abort, nullptr);
+  }
+  // the last two heads' staged keys
+  if (cur > h_first) flush_tails(loc, sh, buf ^ 1, tails + (cur - 1), lists + (cur - 1) * 2 * kListCap);
+  if (cur >= 0) flush_tails(loc, sh, buf, tails + cur, lists + cur * 2 * kListCap);
 }
 
 // A window: its exact width hi - lo as the unevaluated fp32 sum ws + we (the
@@ -421,7 +557,8 @@ __device__ __forceinline__ Cand make_cand(uint32_t lo_key, uint32_t hi_key) {
 
 // Orders windows by exact width, then by start key: rounding is monotonic, so a
 // smaller rounded difference means a smaller exact one, and equal rounded
-// differences are ordered by their errors.
+// differences are ordered by their errors.  Two windows equal in both have the
+// same ends, so the order among them does not matter.
 __device__ __forceinline__ bool cand_less(const Cand& a, const Cand& b) {
   return a.ws < b.ws || (a.ws == b.ws && (a.we < b.we || (a.we == b.we && a.lo_key < b.lo_key)));
 }
@@ -430,146 +567,182 @@ __device__ __forceinline__ bool tot_less(float a, float b) {
   return a < b || (a == b && signbit(a) && !signbit(b));
 }
 
-__global__ void __launch_bounds__(kWinThreads, 1)
-window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long long t,
-              float* __restrict__ min_io, float* __restrict__ max_io, TailInfo* __restrict__ tails, int mode,
-              const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int vec) {
-  pdl_wait();
-  pdl_launch_dependents();
-  // mode 0: tail counts (few windows); mode 1: the heads flagged by mode 0 are
-  // counted here in full and searched again, other heads return at once;
-  // mode 2: full counts from the histogram kernel, no tail state.
-  __shared__ unsigned long long base_s[kWinThreads + 1];
-  __shared__ unsigned long long warp_tot[kWinThreads / 32];
-  __shared__ Cand warp_best[kWinThreads / 32];
-  __shared__ unsigned long long count_lo_s;
-  const int h = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t* ch = counts + (int64_t)h * kBins;
-  if (mode == 1 && tails[h].flag == 0u) return;
-  if (mode == 1) {
-    // Full count of this head (rare): global atomics, one per distinct key and warp step.
-    const uint16_t* xh = x + (int64_t)h * stride_h;
-    const int64_t units = vec ? (int64_t)N / 8 : (int64_t)N;
-    const int nk = vec ? 8 : 1;
-    for (int64_t u0 = 0; u0 < units; u0 += kWinThreads) {
-      const int64_t u = u0 + tid;
-      const bool valid = u < units;
-      uint32_t keys[8];
+__device__ __forceinline__ Cand warp_min_cand(Cand best) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) keys[i] = 0x10000u;
-      if (valid) {
-        const int64_t n = u * nk, b = n / L, l = n - b * L;
-        if (vec) {
-          const uint4 q = *reinterpret_cast<const uint4*>(xh + b * stride_b + l);
-          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t k2 = bf16x2_keys(w[i]);
-            keys[2 * i] = k2 & 0xffffu;
-            keys[2 * i + 1] = k2 >> 16;
-          }
-        } else {
-          keys[0] = bf16x2_keys(xh[b * stride_b + l]) & 0xffffu;
-        }
-      }
-      for (int i = 0; i < nk; ++i) {
-        const uint32_t m = __match_any_sync(0xffffffffu, keys[i]);
-        if (keys[i] < 0x10000u && lane == __ffs(m) - 1) atomicAdd(&ch[keys[i]], (uint32_t)__popc(m));
-      }
-    }
-    __syncthreads();
+  for (int o = 16; o > 0; o >>= 1) {
+    Cand other;
+    other.ws = __shfl_xor_sync(0xffffffffu, best.ws, o);
+    other.we = __shfl_xor_sync(0xffffffffu, best.we, o);
+    other.lo_key = __shfl_xor_sync(0xffffffffu, best.lo_key, o);
+    other.hi_key = __shfl_xor_sync(0xffffffffu, best.hi_key, o);
+    if (cand_less(other, best)) best = other;
   }
-  const uint32_t key_lo = mode == 0 ? tails[h].key_lo : 0xffffu;   // read before thread 0 clears it
-  const uint32_t key_hi = mode == 0 ? tails[h].key_hi : 0u;
-  // in mode 0 the bins strictly between the tails were never counted: skip reading them
-  const uint32_t my_first = (uint32_t)tid * kBinsPerThread, my_last = my_first + kBinsPerThread - 1;
-  const bool skip = mode == 0 && key_lo < 0xffffu && my_first > key_lo && my_last < key_hi;
+  return best;
+}
 
-  // 64 consecutive bins per thread (re-read later from L2 rather than held in registers).
-  const uint4* src = reinterpret_cast<const uint4*>(ch + tid * kBinsPerThread);
-  unsigned long long sum = 0;
-  uint32_t any = 0;
-#pragma unroll 4
-  for (int i = 0; i < kBinsPerThread / 4 && !skip; ++i) {
-    const uint4 q = src[i];
-    sum += (unsigned long long)q.x + q.y + q.z + q.w;
-    any |= q.x | q.y | q.z | q.w;
-  }
-
-  // Block-wide exclusive scan of the per-thread sums.
-  unsigned long long incl = sum;
+// Block-wide exclusive prefix of one value per thread (kWinThreads threads).
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T* warp_tot, T& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    const T y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
   if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    unsigned long long wv = warp_tot[lane];
-    unsigned long long wi = wv;
+    const T wv = warp_tot[lane];
+    T wi = wv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xffffffffu, wi, o);
+      const T y = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += y;
     }
     warp_tot[lane] = wi - wv;                      // exclusive prefix of warp totals
+    if (lane == 31) warp_tot[32] = wi;
   }
   __syncthreads();
-  unsigned long long base = warp_tot[warp] + incl - sum;
+  total = warp_tot[32];
+  return warp_tot[warp] + incl - v;
+}
+
+// Narrowest window of a head from its two tail lists (n_lo and n_hi keys, each at
+// least span = N - t + 1): the listed keys, sorted, are the n_lo smallest and the
+// n_hi largest values of the head, so window i (i < span) starts at listed rank i
+// and ends at listed rank n - span + i (n = n_lo + n_hi).  A counting sort in
+// shared memory gives the ranks: 16-bit counters of the 65536 keys (thread t owns
+// keys [64 t, 64 t + 64), its 32 words padded by 4 so that 16-byte reads of eight
+// threads hit distinct banks), turned in place into exclusive prefix sums, then
+// every listed key takes its rank with one atomic increment of its key's slot.
+constexpr int kPadWords = 36;       // words per thread's 64 counters, padded
+__device__ __forceinline__ uint32_t padded_word(uint32_t key) { return (key >> 1) + 4u * (key >> 6); }
+
+__device__ Cand search_lists(const uint16_t* __restrict__ list, uint32_t n_lo, uint32_t n_hi, uint32_t span,
+                             uint8_t* dyn, uint32_t* warp_tot) {
+  const int tid = threadIdx.x;
+  uint32_t* bins = reinterpret_cast<uint32_t*>(dyn);
+  uint16_t* start_tab = reinterpret_cast<uint16_t*>(dyn + kWinThreads * kPadWords * 4);
+  uint16_t* end_tab = start_tab + span;
+  for (int i = tid; i < kWinThreads * kPadWords / 4; i += kWinThreads)
+    reinterpret_cast<uint4*>(bins)[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  auto bump = [&](uint32_t key) {       // returns the slot's value before the increment
+    const uint32_t sh = (key & 1u) << 4;
+    return (atomicAdd(&bins[padded_word(key)], 1u << sh) >> sh) & 0xffffu;
+  };
+  for (uint32_t i = tid; i < n_lo; i += kWinThreads) bump(list[i]);
+  for (uint32_t i = tid; i < n_hi; i += kWinThreads) bump(list[kListCap + i]);
+  __syncthreads();
+  uint4* own = reinterpret_cast<uint4*>(bins + tid * kPadWords);
+  uint32_t sum = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint4 q = own[w];
+    sum += (q.x & 0xffffu) + (q.x >> 16) + (q.y & 0xffffu) + (q.y >> 16) + (q.z & 0xffffu) + (q.z >> 16) +
+           (q.w & 0xffffu) + (q.w >> 16);
+  }
+  uint32_t n;
+  uint32_t run = block_exclusive_scan<uint32_t>(sum, warp_tot, n);
+  // counters -> exclusive prefix sums (ranks of each key's first copy); n < 65536
+  auto pre = [&](uint32_t w) {
+    const uint32_t lo = run;
+    run += w & 0xffffu;
+    const uint32_t hi = run;
+    run += w >> 16;
+    return lo | (hi << 16);
+  };
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint4 q = own[w];
+    uint4 r;
+    r.x = pre(q.x);
+    r.y = pre(q.y);
+    r.z = pre(q.z);
+    r.w = pre(q.w);
+    own[w] = r;
+  }
+  __syncthreads();
+  const uint32_t e0 = n - span;                      // rank of the first window's end
+  auto place = [&](uint32_t key) {
+    const uint32_t rank = bump(key);
+    if (rank < span) start_tab[rank] = (uint16_t)key;
+    if (rank >= e0) end_tab[rank - e0] = (uint16_t)key;
+  };
+  for (uint32_t i = tid; i < n_lo; i += kWinThreads) place(list[i]);
+  for (uint32_t i = tid; i < n_hi; i += kWinThreads) place(list[kListCap + i]);
+  __syncthreads();
+  Cand best{__int_as_float(0x7f800000), 0.f, 0xffffffffu, 0xffffffffu};
+  for (uint32_t i = tid; i < span; i += kWinThreads) {
+    const Cand cd = make_cand(start_tab[i], end_tab[i]);
+    if (cand_less(cd, best)) best = cd;
+  }
+  return best;
+}
+
+// Full count of head h into its u32 table (global atomics, one per distinct key
+// and warp step): the rare fallback of the tail-list path.
+__device__ void count_head_full(uint32_t* __restrict__ ch, const uint16_t* __restrict__ xh, unsigned long long N,
+                                int64_t L, int64_t stride_b) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t units = (int64_t)N / 8;
+  for (int64_t u0 = 0; u0 < units; u0 += kWinThreads) {
+    const int64_t u = u0 + tid;
+    uint32_t keys[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) keys[i] = 0x10000u;
+    if (u < units) {
+      const int64_t n = u * 8, b = n / L, l = n - b * L;
+      const uint4 q = *reinterpret_cast<const uint4*>(xh + b * stride_b + l);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t k2 = bf16x2_keys(w[i]);
+        keys[2 * i] = k2 & 0xffffu;
+        keys[2 * i + 1] = k2 >> 16;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t m = __match_any_sync(0xffffffffu, keys[i]);
+      if (keys[i] < 0x10000u && lane == __ffs(m) - 1) atomicAdd(&ch[keys[i]], (uint32_t)__popc(m));
+    }
+  }
+  __syncthreads();
+}
+
+// Narrowest window of a head from its full u32 key table ch (N values, windows of
+// t); zeroes the table's occupied words on the way out.
+__device__ Cand search_counts(uint32_t* __restrict__ ch, unsigned long long N, unsigned long long t, uint8_t* dyn,
+                              unsigned long long* base_s, unsigned long long* warp_tot) {
+  const int tid = threadIdx.x;
+  // 64 consecutive bins per thread (re-read later from L2 rather than held in registers)
+  const uint4* src = reinterpret_cast<const uint4*>(ch + tid * kBinsPerThread);
+  unsigned long long sum = 0;
+  uint32_t any = 0;
+#pragma unroll 4
+  for (int i = 0; i < kBinsPerThread / 4; ++i) {
+    const uint4 q = src[i];
+    sum += (unsigned long long)q.x + q.y + q.z + q.w;
+    any |= q.x | q.y | q.z | q.w;
+  }
+  unsigned long long total;
+  const unsigned long long base = block_exclusive_scan<unsigned long long>(sum, warp_tot, total);
   base_s[tid] = base;
   if (tid == kWinThreads - 1) base_s[kWinThreads] = base + sum;
   __syncthreads();
-  bool search = true;
-  if (mode == 0) {
-    // Only keys <= key_lo and >= key_hi were counted: the N - total uncounted values
-    // sit between them, so one virtual bin key_lo + 1 of that size gives every
-    // counted bin its true position.  The windows are exact if each tail holds at
-    // least N - t + 1 values; otherwise flag the head for the full pass.
-    const unsigned long long total = base_s[kWinThreads];
-    const unsigned long long span = N - t + 1;
-    if (key_lo < 0xffffu) {
-      const uint32_t vb = key_lo + 1u;
-      const int owner = (int)(vb / kBinsPerThread);
-      const unsigned long long M = N - total;
-      if (tid == owner) {
-        unsigned long long below = base;
-        for (uint32_t i = (uint32_t)owner * kBinsPerThread; i < vb; ++i) below += ch[i];
-        count_lo_s = below;
-        if (M != 0) {
-          ch[vb] += (uint32_t)M;            // read back by this thread only
-          sum += M;
-          any = 1u;
-        }
-      }
-      if (tid > owner) base += M;
-      __syncthreads();
-      const unsigned long long count_lo = count_lo_s, count_hi = total - count_lo;
-      search = count_lo >= span && count_hi >= span;
-    }
-    if (tid == 0) {
-      tails[h].key_lo = 0u;
-      tails[h].key_hi = 0u;
-      if (!search) tails[h].flag = 1u;
-    }
-  } else if (mode == 1 && tid == 0) {
-    tails[h].flag = 0u;
-  }
 
   Cand best{__int_as_float(0x7f800000), 0.f, 0xffffffffu, 0xffffffffu};
   unsigned long long P = base;
-  if (!search) {
-    // thin tails: the full pass decides this head
-  } else if (N - t + 1 <= (unsigned long long)kCandCap) {
-    // Few window starts (ratio near 1).  Table the first position of every value
-    // that can start a window, start_tab[position] = its bin, and the bin of every
-    // position a window can end at, end_tab[position - (t - 1)]; then window i runs
-    // from start_tab[i] to end_tab[i], and all of them are checked in parallel.
-    extern __shared__ uint32_t tab[];
+  if (N - t + 1 <= (unsigned long long)kCandCap) {
+    // Few window starts.  Table the first position of every value that can start
+    // a window, start_tab[position] = its bin, and the bin of every position a
+    // window can end at, end_tab[position - (t - 1)]; then window i runs from
+    // start_tab[i] to end_tab[i], and all of them are checked in parallel.
     const uint32_t span = (uint32_t)(N - t + 1);
-    uint32_t* start_tab = tab;
-    uint32_t* end_tab = tab + span;
+    uint32_t* start_tab = reinterpret_cast<uint32_t*>(dyn);
+    uint32_t* end_tab = start_tab + span;
     for (uint32_t i = tid; i < span; i += kWinThreads) start_tab[i] = 0xffffffffu;
     __syncthreads();
     unsigned long long pos = base;
@@ -631,42 +804,74 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
       P += cnt;
     }
   }
-
-  // Block argmin (width, then start key).
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Cand other;
-    other.ws = __shfl_xor_sync(0xffffffffu, best.ws, o);
-    other.we = __shfl_xor_sync(0xffffffffu, best.we, o);
-    other.lo_key = __shfl_xor_sync(0xffffffffu, best.lo_key, o);
-    other.hi_key = __shfl_xor_sync(0xffffffffu, best.hi_key, o);
-    if (cand_less(other, best)) best = other;
-  }
-  if (lane == 0) warp_best[warp] = best;
-  __syncthreads();                                  // also: every read of ch[] is done
-  if (warp == 0) {
-    best = warp_best[lane];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      Cand other;
-      other.ws = __shfl_xor_sync(0xffffffffu, best.ws, o);
-      other.we = __shfl_xor_sync(0xffffffffu, best.we, o);
-      other.lo_key = __shfl_xor_sync(0xffffffffu, best.lo_key, o);
-      other.hi_key = __shfl_xor_sync(0xffffffffu, best.hi_key, o);
-      if (cand_less(other, best)) best = other;
-    }
-    if (lane == 0 && best.lo_key != 0xffffffffu) {
-      const float lo = key_value(best.lo_key), hi = key_value(best.hi_key);
-      if (tot_less(lo, min_io[h])) min_io[h] = lo;
-      if (tot_less(max_io[h], hi)) max_io[h] = hi;
-    }
-  }
-  // Leave the workspace zero-filled for the next call (only occupied bins are written).
+  __syncthreads();                                  // every read of ch[] is done
+  // Leave the table zero-filled for the next call (only occupied words are written).
   if (any != 0) {
     uint4* dst = reinterpret_cast<uint4*>(ch + tid * kBinsPerThread);
     for (int i = 0; i < kBinsPerThread / 4; ++i) {
       const uint4 q = dst[i];
       if (q.x | q.y | q.z | q.w) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  return best;
+}
+
+// One CTA per head.  lists != nullptr: the tail-list path (a head that cannot be
+// decided from its lists is counted in full here); otherwise the u32 table holds
+// the head's full counts from hist_kernel.
+__global__ void __launch_bounds__(kWinThreads, 1)
+window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long long t,
+              float* __restrict__ min_io, float* __restrict__ max_io, TailInfo* __restrict__ tails,
+              uint16_t* __restrict__ lists, const uint16_t* __restrict__ x, int64_t L, int64_t stride_b,
+              int64_t stride_h) {
+  pdl_wait();
+  pdl_launch_dependents();
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ unsigned long long base_s[kWinThreads + 1];
+  __shared__ unsigned long long warp_tot[33];
+  __shared__ uint32_t warp_tot32[33];
+  __shared__ Cand warp_best[kWinThreads / 32];
+  const int h = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* ch = counts + (int64_t)h * kBins;
+  const unsigned long long span = N - t + 1;
+  Cand best;
+  bool full = lists == nullptr;
+  if (lists != nullptr) {
+    const TailInfo ti = tails[h];
+    __syncthreads();
+    if (tid == 0) tails[h] = TailInfo{0u, 0u, 0u, 0u};
+    const bool decided = ti.flag == 0u && ti.n_lo >= span && ti.n_hi >= span && ti.n_lo <= (uint32_t)kListCap &&
+                         ti.n_hi <= (uint32_t)kListCap;
+    uint16_t* list = lists + (int64_t)h * 2 * kListCap;
+    if (decided) {
+      best = search_lists(list, ti.n_lo, ti.n_hi, (uint32_t)span, dyn, warp_tot32);
+    } else {
+      count_head_full(ch, x + (int64_t)h * stride_h, N, L, stride_b);
+      full = true;
+    }
+    // Zero the list entries the pass wrote (whole 16-byte groups), so the workspace
+    // is all zero again, whatever head count the next call lays it out for.
+    __syncthreads();
+#pragma unroll
+    for (int side = 0; side < 2; ++side) {
+      const uint32_t n = min(side ? ti.n_hi : ti.n_lo, (uint32_t)kListCap);
+      uint4* dst = reinterpret_cast<uint4*>(list + side * kListCap);
+      for (uint32_t i = tid; i < (n + 7) / 8; i += kWinThreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (full) best = search_counts(ch, N, t, dyn, base_s, warp_tot);
+
+  // Block argmin (width, then start key).
+  best = warp_min_cand(best);
+  if (lane == 0) warp_best[warp] = best;
+  __syncthreads();
+  if (warp == 0) {
+    best = warp_min_cand(warp_best[lane]);
+    if (lane == 0 && best.lo_key != 0xffffffffu) {
+      const float lo = key_value(best.lo_key), hi = key_value(best.hi_key);
+      if (tot_less(lo, min_io[h])) min_io[h] = lo;
+      if (tot_less(max_io[h], hi)) max_io[h] = hi;
     }
   }
 }
@@ -676,8 +881,13 @@ window_kernel(uint32_t* __restrict__ counts, unsigned long long N, unsigned long
 
 using namespace fa3;
 
+namespace {
+size_t counts_bytes(int H) { return (size_t)H * kBins * sizeof(uint32_t); }
+size_t tails_bytes(int H) { return (size_t)H * sizeof(TailInfo); }
+}  // namespace
+
 FA3_API size_t fa3_calibrate_workspace_size(int H) {
-  return H > 0 ? (size_t)H * kBins * sizeof(uint32_t) + (size_t)H * sizeof(TailInfo) : 0;
+  return H > 0 ? counts_bytes(H) + tails_bytes(H) + (size_t)H * 2 * kListCap * sizeof(uint16_t) : 0;
 }
 
 FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L, int64_t stride_b,
@@ -691,65 +901,69 @@ FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L
   if (H > 65535) return FA3_ERANGE;
   if (!workspace || workspace_bytes < fa3_calibrate_workspace_size(H) || !aligned16(workspace))
     return FA3_EWORKSPACE;
-  int st = check_device(nullptr);
+  int sms = 0;
+  int st = check_device(&sms);
   if (st != FA3_OK) return st;
+  if (sms <= 0) sms = 148;
   // FA3量化 step 2: target_num = int(ratio * N), float64 product, truncation; at least 1.
   int64_t t = (int64_t)(ratio * (double)N);
   if (t < 1) t = 1;
   if (t > N) t = N;
   const int vec = (L % 8 == 0) && aligned16(x) && (stride_b % 8 == 0) && (stride_h % 8 == 0);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int smem = kBins * 2;   // 128 KB of 16-bit bins
-  if (cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return FA3_ECUDA;
-  const int chunks_per_head = (int)((N + kChunk - 1) / kChunk);
-  const int64_t total_chunks = (int64_t)chunks_per_head * H;
-  if (total_chunks > (int64_t)1 << 30) return FA3_ERANGE;
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess || sms <= 0) sms = 148;
-  {
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  }
-  const unsigned grid = (unsigned)(total_chunks < sms ? total_chunks : sms);
   uint32_t* counts = static_cast<uint32_t*>(workspace);
-  TailInfo* tails = reinterpret_cast<TailInfo*>(counts + (size_t)H * kBins);
+  TailInfo* tails = reinterpret_cast<TailInfo*>(static_cast<uint8_t*>(workspace) + counts_bytes(H));
+  uint16_t* lists = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + counts_bytes(H) + tails_bytes(H));
   const unsigned long long span = (unsigned long long)(N - t + 1);
-  const bool fast = span <= (unsigned long long)kCandCap;
-  const int wsmem = fast ? (int)(2 * span * sizeof(uint32_t)) : 0;   // start and end tables
-  if (wsmem > 48 * 1024 &&
-      cudaFuncSetAttribute(window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem) != cudaSuccess)
-    return FA3_ECUDA;
-  if (fast) {
-    // tails only, then a full pass over the heads whose tails turned out too thin
-    if (launch_pdl(tail_kernel, dim3(H), dim3(kSampleThreads), 0, s, x, L, stride_b, stride_h, N, span, vec, tails) !=
+  // Tail lists when both can be expected well inside their capacity: with S
+  // sampled keys, r = int(3 S (N - t + 1) / N + 4) sampled keys lie in each tail,
+  // which then holds about N r / S values; r must stay well below the thread
+  // count for the thresholds to track the sample's order statistics.
+  constexpr double kS = 8.0 * kSampleGroups;
+  const double r_want = 3.0 * kS * (double)span / (double)N + 4.0;
+  const uint32_t rank = r_want >= kS ? (uint32_t)kS : (uint32_t)r_want;
+  const bool use_lists = vec && rank <= (uint32_t)kMaxRank && (double)N * rank / kS <= 0.5 * kListCap;
+  if (use_lists) {
+    const int64_t pieces = (2 * L + kStageBytes - 1) / kStageBytes;
+    const int64_t total_items = pieces * B * H;
+    const unsigned grid = (unsigned)(total_items < sms ? total_items : sms);
+    if (cudaFuncSetAttribute(tail_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStreamSmem) !=
         cudaSuccess)
       return FA3_ECUDA;
+    // padded counters and tables of the list search; the same bytes hold the u32
+    // tables of a head that falls back to its full count (8 * span fits)
+    const int wsmem = (int)(kWinThreads * kPadWords * 4 + 4 * span);
+    if (cudaFuncSetAttribute(window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem) != cudaSuccess)
+      return FA3_ECUDA;
     timing_begin(s);
-    const int64_t per_cta = (int64_t)kTailThreads * kTailGroups;
-    const int64_t xb = (L / 8 + per_cta - 1) / per_cta, rows = B * (int64_t)H;
-    if (vec && xb <= 0x7fffffff && rows <= 65535) {
-      if (launch_pdl(tail_count_kernel, dim3((unsigned)xb, (unsigned)rows), dim3(kTailThreads), 0, s, x, L,
-                     stride_b, stride_h, H, counts, static_cast<const TailInfo*>(tails)) != cudaSuccess)
-        return FA3_ECUDA;
-    } else {
-      if (launch_pdl(hist_kernel, dim3(grid), dim3(kHistThreads), smem, s, x, L, stride_b, stride_h, N,
-                     chunks_per_head, (int)total_chunks, counts, vec, static_cast<const TailInfo*>(tails)) != cudaSuccess)
-        return FA3_ECUDA;
-    }
-    timing_end(s);
-    for (int mode = 0; mode < 2; ++mode)
-      if (launch_pdl(window_kernel, dim3(H), dim3(kWinThreads), wsmem, s, counts, (unsigned long long)N,
-                     (unsigned long long)t, min_io, max_io, tails, mode, x, L, stride_b, stride_h, vec) != cudaSuccess)
-        return FA3_ECUDA;
-  } else {
-    timing_begin(s);
-    if (launch_pdl(hist_kernel, dim3(grid), dim3(kHistThreads), smem, s, x, L, stride_b, stride_h, N,
-                   chunks_per_head, (int)total_chunks, counts, vec, static_cast<const TailInfo*>(nullptr)) != cudaSuccess)
+    if (launch_pdl(tail_stream_kernel, dim3(grid), dim3(kStreamThreads), kStreamSmem, s, x, L, stride_b, stride_h,
+                   B, (unsigned long long)N, rank, total_items, tails, lists) != cudaSuccess)
       return FA3_ECUDA;
     timing_end(s);
     if (launch_pdl(window_kernel, dim3(H), dim3(kWinThreads), wsmem, s, counts, (unsigned long long)N,
-                   (unsigned long long)t, min_io, max_io, tails, 2, x, L, stride_b, stride_h, vec) != cudaSuccess)
+                   (unsigned long long)t, min_io, max_io, tails, lists, x, L, stride_b,
+                   stride_h) != cudaSuccess)
+      return FA3_ECUDA;
+  } else {
+    const int smem = kBins * 2;   // 128 KB of 16-bit bins
+    if (cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return FA3_ECUDA;
+    const int chunks_per_head = (int)((N + kChunk - 1) / kChunk);
+    const int64_t total_chunks = (int64_t)chunks_per_head * H;
+    if (total_chunks > (int64_t)1 << 30) return FA3_ERANGE;
+    const unsigned grid = (unsigned)(total_chunks < sms ? total_chunks : sms);
+    const int wsmem = span <= (unsigned long long)kCandCap ? (int)(8 * span) : 0;   // start and end tables
+    if (wsmem > 48 * 1024 &&
+        cudaFuncSetAttribute(window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem) != cudaSuccess)
+      return FA3_ECUDA;
+    timing_begin(s);
+    if (launch_pdl(hist_kernel, dim3(grid), dim3(kHistThreads), smem, s, x, L, stride_b, stride_h, N,
+                   chunks_per_head, (int)total_chunks, counts, vec) != cudaSuccess)
+      return FA3_ECUDA;
+    timing_end(s);
+    if (launch_pdl(window_kernel, dim3(H), dim3(kWinThreads), wsmem, s, counts, (unsigned long long)N,
+                   (unsigned long long)t, min_io, max_io, tails, static_cast<uint16_t*>(nullptr), x, L,
+                   stride_b, stride_h) != cudaSuccess)
       return FA3_ECUDA;
   }
   return cuda_status(cudaGetLastError());

@@ -30,7 +30,7 @@ def test_status_strings_and_version(L):
 
 def test_calibrate_validation(L):
     ws = L.fa3_calibrate_workspace_size(4)
-    assert ws == 4 * 65536 * 4 + 4 * 16
+    assert ws == 4 * 65536 * 4 + 4 * 16 + 4 * 2 * 16384 * 2   # key counts, tail state, tail-key lists
     args = lambda **k: dict(dict(x=FAKE, B=2, H=4, L=64, sb=256, sh=64, ratio=0.9999, mn=FAKE, mx=FAKE,
                                  ws=FAKE, wsb=ws), **k)
     call = lambda a: L.fa3_calibrate_perhead(a["x"], a["B"], a["H"], a["L"], a["sb"], a["sh"], a["ratio"],

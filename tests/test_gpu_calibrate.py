@@ -160,30 +160,31 @@ def test_full_size_calibration_all_heads_four_batches():
     assert np.array_equal(_bits(sc), _bits(O.qparams(omn, omx)))
 
 
-def _sampled_units(units, n_samples=512):
-    # the strided sample the tail thresholds are drawn from (16-byte groups or values)
+def _sampled_units(units, n_samples=2048):
+    # the strided sample the tail thresholds are drawn from (16-byte groups)
     return sorted({g * units // n_samples for g in range(n_samples)})
 
 
 @pytest.mark.parametrize("vec", [True, False])
 def test_thin_tails_fall_back_to_full_count(vec):
-    # Plant one extreme value into sampled units of head 0 (25 groups of 8 values, or
-    # 40 single values, more than the sample's tail rank of 16 or 5): the sample's
-    # tail order statistic then falls on that value, whose count (200 or 40) is below
-    # the 1574 smallest values a window can start from, so the tail-only count must
-    # be rejected and the head counted again in full.  Head 1 is left as is.
+    # Plant one extreme value into the first 60 sampled groups of head 0 (480 values,
+    # one group in each of 60 sampling threads, more than the sample rank of 53): the
+    # low threshold then falls on that value, whose count (480) is below the 1574
+    # smallest values a window can start from, so the tail lists must be rejected and
+    # the head counted again in full.  Head 1 is left as is.  With an odd row stride
+    # (vec False) the input takes the histogram path instead; the result is the same
+    # either way.
     F = fa3()
     rng = np.random.default_rng(11)
     H, N = 2, 4 * 2048 * 192
     ratio = 0.999                                  # N - target_num + 1 = 1574 window starts
     x = W.bf16_round(rng.standard_normal((H, N)).astype(np.float32))
-    per, n_plant = (8, 25) if vec else (1, 40)
-    for u in _sampled_units(N // per)[:n_plant]:
-        x[0, u * per:u * per + per] = -600.0
+    for u in _sampled_units(N // 8)[:60]:
+        x[0, u * 8:u * 8 + 8] = -600.0
     if vec:
         xd = bf16_dev(x)
     else:
-        pad = np.zeros((H, N + 1), np.float32)     # odd row stride: the scalar path
+        pad = np.zeros((H, N + 1), np.float32)     # odd row stride: the histogram path
         pad[:, :N] = x
         xd = bf16_dev(pad)[:, :N]
     omn, omx = O.calibrate([x.reshape(1, H, 1, N)], ratio)
@@ -194,6 +195,63 @@ def test_thin_tails_fall_back_to_full_count(vec):
         torch.cuda.synchronize()
         assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn))
         assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx))
+
+
+def test_tail_list_path_every_branch():
+    # One (H, N) batch at ratio 0.9999 (158 window starts, sample rank 8), one head
+    # per branch of the tail-list path:
+    #   0  ordinary Student-t head: decided from its lists;
+    #   1  6000 copies of -50 inside one 64 KB piece of the row: one CTA stages most
+    #      of a list, still decided from the lists;
+    #   2  20000 copies of -50 at the start of the row: the low list overflows its
+    #      capacity and the head is counted in full;
+    #   3  a constant head: the sample's thresholds meet (degenerate), full count;
+    #   4  negative values only, with a high tail of one repeated value;
+    #   5  12000 copies of -50 inside one piece: more than one CTA may stage for a
+    #      head, so the head is counted in full.
+    F = fa3()
+    rng = np.random.default_rng(12)
+    H, N = 6, 4 * 2048 * 192
+    ratio = 0.9999
+    x = (rng.standard_t(3, (H, N)) * 2.0).astype(np.float32)
+    x[1, 3 * 16384:3 * 16384 + 6000] = -50.0
+    x[2, :20000] = -50.0
+    x[3] = 1.5
+    x[4] = -np.abs(x[4]) - 1.0
+    x[4, rng.choice(N, 3000, replace=False)] = -0.5
+    x[5, 5 * 16384:5 * 16384 + 12000] = -50.0
+    x = W.bf16_round(x)
+    for lo, n in ((3 * 16384, 6000), (5 * 16384, 12000)):
+        assert sum(1 for u in _sampled_units(N // 8) if lo <= 8 * u < lo + n) >= 8
+    omn, omx = O.calibrate([x.reshape(1, H, 1, N)], ratio)
+    xd = bf16_dev(x)
+    for _ in range(2):
+        mn = torch.full((H,), float("inf"), device="cuda")
+        mx = torch.full((H,), float("-inf"), device="cuda")
+        F.calibrate_perhead(xd, ratio, mn, mx)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn)), (mn.cpu().numpy(), omn)
+        assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx)), (mx.cpu().numpy(), omx)
+
+
+def test_workspace_reused_across_head_counts():
+    # One caller-owned workspace, sized for the largest H, serves calls with other
+    # head counts and both paths (tail lists at ratio 0.9999, the full histogram at
+    # 0.5); the per-H layout moves, so every call must leave it all zero.
+    F = fa3()
+    rng = np.random.default_rng(13)
+    ws = torch.zeros(F.calibrate_workspace_size(8), dtype=torch.uint8, device="cuda")
+    for H, ratio in ((8, 0.9999), (3, 0.9999), (5, 0.5), (6, 0.9999), (2, 0.5)):
+        x = W.bf16_round((rng.standard_t(3, (2, H, 256, 128)) * rng.uniform(0.1, 10, (1, H, 1, 1)))
+                         .astype(np.float32))
+        mn = torch.full((H,), float("inf"), device="cuda")
+        mx = torch.full((H,), float("-inf"), device="cuda")
+        F.calibrate_perhead(bf16_dev(x), ratio, mn, mx, workspace=ws)
+        omn, omx = O.calibrate([x], ratio)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(mn.cpu().numpy()), _bits(omn)), (H, ratio)
+        assert np.array_equal(_bits(mx.cpu().numpy()), _bits(omx)), (H, ratio)
+        assert int(torch.count_nonzero(ws)) == 0, (H, ratio)
 
 
 def test_range_merge_matches_step_3_in_any_split():
