@@ -14,14 +14,15 @@
 // Tail-list path (few windows: N - target_num + 1 small, e.g. the pages' ratio
 // 0.9999).  Every window then starts among the N - t + 1 smallest values and
 // ends among as many largest, so only the two tails of a head matter.
-//   tail_stream_kernel  one persistent CTA per SM walks a contiguous range of
-//             64 KB pieces of the input (head-major); each warp streams its 4 KB
-//             slice of every piece with bulk copies through its own 3-slot ring.
-//             The CTA draws each of its heads' tail thresholds from a fixed sample
-//             of the head (every CTA that meets the head draws the same ones),
-//             rules out most values with packed bf16 min/max tests, and appends the
-//             keys beyond the thresholds to two per-head lists (staged in shared
-//             memory, one global reservation per head and CTA).
+//   tail_pick_kernel  per head: tail thresholds from a fixed sample of the head
+//             (16 runs of 2 KB), the r-th smallest of the sampling threads' minima
+//             and the r-th largest of their maxima.
+//   tail_stream_kernel  one persistent CTA per SM takes every G-th 64 KB piece of
+//             the input; each warp streams its 4 KB slice of every piece with bulk
+//             copies through its own 3-slot ring, rules out most values with packed
+//             bf16 min/max tests, and stages the keys beyond its head's thresholds
+//             (tagged with their piece) until the CTA moves them into two per-head
+//             lists.
 //   window_kernel  per head: counts the listed keys into a shared-memory
 //             histogram, prefix sums give each listed key its rank, and the
 //             windows i = 0 .. N - t pair the i-th smallest listed key with the
@@ -67,20 +68,20 @@ constexpr int kStages = 3;          // ring depth (per warp: each warp streams i
 constexpr int kSliceBytes = kStageBytes / kStreamWarps;              // a warp's 4 KB share of a piece
 constexpr int kGroupsPerStage = kStageBytes / 16 / kStreamThreads;   // 8 groups of 8 values per lane
 constexpr int kListCap = 16384;     // tail keys per list and head in the workspace
-constexpr int kStageCap = 4096;     // tail keys per list a CTA stages for one head
 constexpr int kSampleGroups = 2048; // strided 16-byte groups per head for the tail thresholds
 constexpr int kMaxRank = 64;        // largest sample rank the tail thresholds are drawn at
-// ring, then two staging buffers (two heads) of two lists each
-constexpr size_t kStreamSmem = (size_t)kStages * kStageBytes + 4 * kStageCap * sizeof(uint16_t);
+// ring, then the staged keys (kStagedCap words)
+constexpr size_t kStreamSmem = (size_t)kStages * kStageBytes + 8192 * sizeof(uint32_t);
 static_assert(kGroupsPerStage == 8, "the per-thread min / max tree below takes eight groups");
 
 // Per-head state of the tail-list path, in the workspace after the counters:
 // n_lo / n_hi: keys appended to the low / high list (may exceed kListCap: then
-// the lists are incomplete); flag: the head's sample was degenerate, or one CTA
-// met more than kStageCap keys of one list (the head is then counted in full).
-// The window kernel reads and re-zeroes it.
+// the lists are incomplete); flag: the head's sample was degenerate, or a bounded
+// wait gave up (the head is then counted in full); keys: the tail thresholds
+// tail_pick_kernel drew.  The window kernel reads and
+// re-zeroes it.
 struct TailInfo {
-  uint32_t n_lo, n_hi, flag, pad;
+  uint32_t n_lo, n_hi, flag, keys;   // keys: the thresholds, key_lo | key_hi << 16
 };
 
 // Order-preserving 16-bit key of a bf16 value: positive values get the top bit
@@ -222,114 +223,119 @@ hist_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t
 // Shared state of tail_stream_kernel beside its dynamic buffers.
 struct StreamShared {
   uint64_t full[kStreamWarps][kStages];  // a warp's ring slot filled (bulk copy bytes landed)
-  uint32_t part[2][2][kStreamWarps];  // per-warp counts of the threshold search (two heads), double-buffered
-  uint32_t gbase[2];               // global list positions reserved by a flush
-  uint32_t cnt[2][2];              // per staging buffer: keys met for the low / high list (staged: the first kStageCap)
+  uint32_t tag_cnt[128];           // flush: staged keys per tag, then the next free position per tag
+  uint32_t tag_base[128];          // flush: the list position reserved for each tag
+  uint32_t n_staged;               // keys staged since the last flush (may pass the capacity)
   uint32_t abort;                  // a bounded wait gave up: stop using the ring
 };
 
-// One thread's share of a head's sample: kSampleUnits strided 16-byte groups
-// (group g of the head's N / 8 at g * (N / 8) / kSampleGroups; the positions
-// depend only on the head's size, so every CTA that meets the head draws the
-// same sample).
-constexpr int kSampleUnits = kSampleGroups / kStreamThreads;   // 4 groups per thread
-__device__ __forceinline__ void load_sample(const uint16_t* __restrict__ xh, int64_t L, int64_t stride_b,
-                                            unsigned long long N, uint4 (&q)[kSampleUnits]) {
+// Tail thresholds, one CTA per head (tail_pick_kernel).  The sample: kSampleGroups
+// 16-byte groups of the head in 16 runs of 128 consecutive groups (run r starts at
+// group r * (N / 8) / 16, wrapping past the end), so that each run reads whole
+// DRAM pages.  Thread t reads eight groups of run t / 16.  (A small CTA: it can
+// share an SM with the stream kernel's CTA, whose ring loads start meanwhile.)
+constexpr int kPickThreads = 256;
+constexpr int kPickWarps = kPickThreads / 32;
+constexpr int kSampleRuns = 16;
+constexpr int kRunThreads = kPickThreads / kSampleRuns;        // 16 threads per run
+constexpr int kSampleUnits = kSampleGroups / kPickThreads;     // 8 groups per thread
+static_assert(kSampleGroups == kSampleRuns * kRunThreads * kSampleUnits, "sample layout");
+
+// key_lo = the r-th smallest of the threads' sample minima (64 keys each), key_hi
+// = the r-th largest of their maxima (searches over the 16-bit keys, a hex digit
+// per step, counted with ballots).  r threads hold a sampled key at or below
+// key_lo, so at least r of the S sampled keys are; for r well below the thread
+// count it sits near the sample's r-th smallest key.  With p = (N - t + 1) / N and
+// r = 3 S p + 4, the low list (keys <= key_lo) then holds the N - t + 1 smallest
+// values of the head unless the sample over-represents the low tail badly (the
+// window kernel checks and falls back); likewise the high list.  Thresholds that
+// meet mark the head degenerate (flag 1: counted in full).
+__global__ void __launch_bounds__(kPickThreads, 1)
+tail_pick_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h,
+                 unsigned long long N, uint32_t r, TailInfo* __restrict__ tails) {
+  __shared__ uint32_t part[2][kPickWarps][32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, h = blockIdx.x;
+  const uint16_t* xh = x + (int64_t)h * stride_h;
   const unsigned long long units = N / 8;
+  // this thread's groups: run0 + (tid % 16) + 16 j; one division for the first, then
+  // steps of 128 values along the row (and on to the next row, or back to the first)
+  const unsigned long long u0 =
+      ((unsigned long long)(tid / kRunThreads) * units / kSampleRuns + (tid % kRunThreads)) % units;
+  int64_t b = (int64_t)(u0 * 8) / L, l = (int64_t)(u0 * 8) - b * L;
+  const int64_t rows = (int64_t)(N / (unsigned long long)L);
+  uint4 q[kSampleUnits];
 #pragma unroll
   for (int j = 0; j < kSampleUnits; ++j) {
-    const unsigned long long u = (unsigned long long)(threadIdx.x + j * kStreamThreads) * units / kSampleGroups;
-    const int64_t n = (int64_t)u * 8, b = n / L, l = n - b * L;
     q[j] = *reinterpret_cast<const uint4*>(xh + b * stride_b + l);
+    l += 8 * kRunThreads;
+    while (l >= L) {
+      l -= L;
+      if (++b == rows) b = 0;
+    }
   }
-}
-// The smallest and largest key of the thread's sampled values.
-struct SampleExt {
-  uint32_t mn, mx;
-};
-__device__ __forceinline__ SampleExt sample_extremes(const uint4 (&q)[kSampleUnits]) {
-  SampleExt e{0xffffu, 0u};
+  uint32_t mn = 0xffffu, mx = 0u;
 #pragma unroll
   for (int j = 0; j < kSampleUnits; ++j) {
     const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t k2 = bf16x2_keys(w[i]), a = k2 & 0xffffu, c = k2 >> 16;
-      e.mn = min(e.mn, min(a, c));
-      e.mx = max(e.mx, max(a, c));
+      mn = min(mn, min(a, c));
+      mx = max(mx, max(a, c));
     }
   }
-  return e;
-}
-
-// Tail thresholds of two heads at once, block-wide: key_lo = the r-th smallest of
-// the threads' sample minima, key_hi = the r-th largest of their maxima (binary
-// searches over the 16-bit keys, one ballot count per step).  r threads hold a
-// sampled key at or below key_lo, so at least r of the S sampled keys are; for r
-// well below the thread count it sits near the sample's r-th smallest key.  With
-// p = (N - t + 1) / N and r = 3 S p + 4, the low list (keys <= key_lo) then holds
-// the N - t + 1 smallest values of the head unless the sample over-represents the
-// low tail badly (the window kernel checks and falls back); likewise the high
-// list.  Thresholds that meet mark the head degenerate.
-struct Thresholds {
-  uint32_t lo, hi;
-  bool degenerate;
-};
-__device__ void select_tails(const SampleExt (&e)[2], uint32_t r, StreamShared& sh, Thresholds (&t)[2]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t a_lo[2] = {0u, 0u}, b_lo[2] = {0xffffu, 0xffffu}, a_hi[2] = {0u, 0u}, b_hi[2] = {0xffffu, 0xffffu};
+  // radix-16 searches, one hex digit of both keys per step: lane i of each warp
+  // counts the threads whose minimum is at most (prefix, digit i, then all ones),
+  // lane 16 + i those whose maximum is at least (prefix, digit i + 1, then zeros)
+  uint32_t a_lo = 0u, a_hi = 0u;
 #pragma unroll 1
-  for (int it = 0; it < 16; ++it) {
-    uint32_t m_lo[2], m_hi[2];
+  for (int st = 0; st < 4; ++st) {
+    const int shift = 12 - 4 * st;
+    const uint32_t ones = (1u << shift) - 1u;
+    uint32_t mine = 0u;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      m_lo[u] = (a_lo[u] + b_lo[u]) >> 1;
-      m_hi[u] = (a_hi[u] + b_hi[u] + 1u) >> 1;
-      const uint32_t c = (uint32_t)__popc(__ballot_sync(0xffffffffu, e[u].mn <= m_lo[u])) |
-                         ((uint32_t)__popc(__ballot_sync(0xffffffffu, e[u].mx >= m_hi[u])) << 16);
-      if (lane == 0) sh.part[it & 1][u][warp] = c;
+    for (int i = 0; i < 15; ++i) {
+      const uint32_t bl = __ballot_sync(0xffffffffu, mn <= (a_lo | ((uint32_t)i << shift) | ones));
+      const uint32_t bh = __ballot_sync(0xffffffffu, mx >= (a_hi | ((uint32_t)(i + 1) << shift)));
+      if (lane == i) mine = (uint32_t)__popc(bl);
+      if (lane == 16 + i) mine = (uint32_t)__popc(bh);
     }
+    part[st & 1][warp][lane] = mine;
     __syncthreads();
+    uint32_t tot = 0u;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      uint32_t tot = lane < kStreamWarps ? sh.part[it & 1][u][lane] : 0u;
-      tot = __reduce_add_sync(0xffffffffu, tot);
-      if ((tot & 0xffffu) >= r) b_lo[u] = m_lo[u]; else a_lo[u] = m_lo[u] + 1u;
-      if ((tot >> 16) >= r) a_hi[u] = m_hi[u]; else b_hi[u] = m_hi[u] - 1u;
-    }
+    for (int w = 0; w < kPickWarps; ++w) tot += part[st & 1][w][lane];
+    const uint32_t okl = __ballot_sync(0xffffffffu, lane < 15 && tot >= r);
+    const uint32_t okh = __ballot_sync(0xffffffffu, lane >= 16 && lane < 31 && tot >= r);
+    a_lo |= (okl ? (uint32_t)(__ffs(okl) - 1) : 15u) << shift;          // smallest digit reaching r
+    a_hi |= (okh ? (uint32_t)(31 - __clz(okh) - 15) : 0u) << shift;     // largest digit reaching r
   }
-#pragma unroll
-  for (int u = 0; u < 2; ++u) t[u] = Thresholds{a_lo[u], a_hi[u], !(a_lo[u] + 1u < a_hi[u])};
-}
-
-// Stages one tail key (one lane; the keys are rare) in staging buffer `buf`.  Keys
-// past kStageCap are counted, not kept: the flush then flags the head for the
-// full count.
-__device__ __forceinline__ void stage_key(uint16_t* loc, StreamShared& sh, int buf, int side, uint32_t key) {
-  const uint32_t pos = atomicAdd(&sh.cnt[buf][side], 1u);
-  if (pos < (uint32_t)kStageCap) loc[(2 * buf + side) * kStageCap + pos] = (uint16_t)key;
-}
-
-// Moves staging buffer `buf` (one head's keys) into the head's lists (block-wide):
-// one reservation of the full count per list, so the head's count stays exact.
-__device__ void flush_tails(uint16_t* loc, StreamShared& sh, int buf, TailInfo* ti, uint16_t* list) {
-  const int tid = threadIdx.x;
-  __syncthreads();
-  const uint32_t c0 = sh.cnt[buf][0], c1 = sh.cnt[buf][1];
   if (tid == 0) {
-    sh.gbase[0] = c0 ? atomicAdd(&ti->n_lo, c0) : 0u;
-    sh.gbase[1] = c1 ? atomicAdd(&ti->n_hi, c1) : 0u;
-    if (c0 > (uint32_t)kStageCap || c1 > (uint32_t)kStageCap) ti->flag = 1u;
+    tails[h].keys = a_lo | (a_hi << 16);
+    if (!(a_lo + 1u < a_hi)) tails[h].flag = 1u;
   }
-  __syncthreads();
-  const uint32_t g0 = sh.gbase[0], g1 = sh.gbase[1];
-  const uint32_t n0 = min(c0, (uint32_t)kStageCap), n1 = min(c1, (uint32_t)kStageCap);
-  const uint16_t* b = loc + 2 * buf * kStageCap;
-  for (uint32_t i = tid; i < n0 && g0 + i < (uint32_t)kListCap; i += kStreamThreads) list[g0 + i] = b[i];
-  for (uint32_t i = tid; i < n1 && g1 + i < (uint32_t)kListCap; i += kStreamThreads)
-    list[kListCap + g1 + i] = b[kStageCap + i];
-  __syncthreads();
-  if (tid == 0) { sh.cnt[buf][0] = 0u; sh.cnt[buf][1] = 0u; }
+}
+
+// Staged tail keys of a CTA: one list of key | tag << 16, the tag naming the
+// CTA's item (its position k in the CTA's sequence, modulo kTagItems) and the side
+// (low list 0, high list 1): tag = 2 (k mod kTagItems) + side.
+constexpr int kTagItems = 64;                 // items staged between two flushes
+constexpr int kTags = 2 * kTagItems;
+constexpr int kStagedCap = 8192;              // staged keys per CTA between two flushes
+
+// Stages one tail key (one lane; the keys are rare).  Keys past kStagedCap go
+// straight to the head's list, one reservation each.
+__device__ __forceinline__ void stage_key(uint32_t* staged, uint32_t* n_staged, uint32_t tag, uint32_t key,
+                                          TailInfo* ti, uint16_t* list, int side) {
+  const uint32_t pos = atomicAdd(n_staged, 1u);
+  if (pos < (uint32_t)kStagedCap) {
+    staged[pos] = key | (tag << 16);
+  } else {
+    const uint32_t p = atomicAdd(side ? &ti->n_hi : &ti->n_lo, 1u);
+    if (p < (uint32_t)kListCap) list[side * kListCap + p] = (uint16_t)key;
+  }
 }
 
 // Packed bf16 compares, 0xffff per true half (IEEE: -0 == +0).
@@ -345,120 +351,142 @@ __device__ __forceinline__ uint32_t bge2(uint32_t a, uint32_t b) {
 }
 
 // Tail-list pass (16-byte aligned rows).  The input is cut into items of up to
-// kStageBytes of one row, numbered head-major (head, batch row, piece); CTA g
-// takes the contiguous items [g T / G, (g + 1) T / G).  Warp w handles the 4 KB
-// slice w of every item: its lane 0 streams the slices with bulk copies into the
-// warp's own kStages-slot ring (one mbarrier per slot), so warps run independently
-// of one another between head changes (where the whole CTA meets only when it
-// meets a third head).  A bounded wait that gives up flags every head of the CTA
-// for the full count, so the result stays exact.
+// kStageBytes of one row, numbered head-major (head, batch row, piece); CTA g of G
+// takes items g, g + G, g + 2 G, ... (spread over all heads and addresses, so the
+// CTAs finish together).  Warp w handles the 4 KB slice w of every item: its lane
+// 0 streams the slices with bulk copies into the warp's own kStages-slot ring (one
+// mbarrier per slot), so the warps run independently; tail keys are staged with a
+// tag naming their item and side, and every kTagItems items the CTA meets once to
+// move them into the heads' lists.  A bounded wait that gives up flags every head
+// of the CTA for the full count, so the result stays exact.
+struct ItemMap {                    // item i -> (head h, batch row b, piece c)
+  DivU32 per_head, pieces;
+  uint32_t n_pieces, n_per_head;
+};
+__device__ __forceinline__ void item_coords(uint32_t i, const ItemMap& m, uint32_t& h, uint32_t& b, uint32_t& c) {
+  h = divu32(i, m.per_head);
+  const uint32_t r = i - h * m.n_per_head;
+  b = divu32(r, m.pieces);
+  c = r - b * m.n_pieces;
+}
+
+// Moves the CTA's staged keys into the heads' lists (block-wide): counts per tag,
+// one reservation per tag in its head's list, then every key to its place.  Tag t
+// belongs to the CTA's item k0 + t / 2.
+__device__ void flush_staged(const uint32_t* staged, StreamShared& sh, int k0, uint32_t g, uint32_t G,
+                             const ItemMap& m, TailInfo* __restrict__ tails, uint16_t* __restrict__ lists) {
+  const int tid = threadIdx.x;
+  __syncthreads();
+  const uint32_t n = min(sh.n_staged, (uint32_t)kStagedCap);
+  for (uint32_t e = tid; e < n; e += kStreamThreads) atomicAdd(&sh.tag_cnt[staged[e] >> 16], 1u);
+  __syncthreads();
+  if (tid < kTags) {
+    const uint32_t c = sh.tag_cnt[tid];
+    if (c != 0u) {
+      uint32_t h, b, pc;
+      item_coords(g + (uint32_t)(k0 + tid / 2) * G, m, h, b, pc);
+      sh.tag_base[tid] = atomicAdd((tid & 1) ? &tails[h].n_hi : &tails[h].n_lo, c);
+    }
+    sh.tag_cnt[tid] = 0u;
+  }
+  __syncthreads();
+  for (uint32_t e = tid; e < n; e += kStreamThreads) {
+    const uint32_t v = staged[e], t = v >> 16;
+    const uint32_t pos = sh.tag_base[t] + atomicAdd(&sh.tag_cnt[t], 1u);
+    if (pos < (uint32_t)kListCap) {
+      uint32_t h, b, pc;
+      item_coords(g + (uint32_t)(k0 + (int)t / 2) * G, m, h, b, pc);
+      lists[((size_t)h * 2 + (t & 1)) * kListCap + pos] = (uint16_t)(v & 0xffffu);
+    }
+  }
+  __syncthreads();
+  if (tid < kTags) sh.tag_cnt[tid] = 0u;
+  if (tid == 0) sh.n_staged = 0u;
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kStreamThreads, 1)
-tail_stream_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, int64_t stride_h, int64_t B,
-                   unsigned long long N, uint32_t rank, int64_t total_items, TailInfo* __restrict__ tails,
-                   uint16_t* __restrict__ lists) {
+tail_stream_kernel(const uint16_t* __restrict__ x, int64_t stride_b, int64_t stride_h, uint32_t total_items,
+                   ItemMap m, uint32_t last_bytes, TailInfo* __restrict__ tails, uint16_t* __restrict__ lists) {
   extern __shared__ __align__(128) uint8_t sm_stream[];
-  uint16_t* loc = reinterpret_cast<uint16_t*>(sm_stream + kStages * kStageBytes);   // [2][2][kStageCap]
+  uint32_t* staged = reinterpret_cast<uint32_t*>(sm_stream + kStages * kStageBytes);   // [kStagedCap]
   __shared__ StreamShared sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint8_t* ring = sm_stream + warp * kStages * kSliceBytes;                           // this warp's slots
-  const int64_t row_bytes = 2 * L;
-  const int64_t pieces = (row_bytes + kStageBytes - 1) / kStageBytes, per_head = B * pieces;
-  const uint32_t last_bytes = (uint32_t)(row_bytes - (pieces - 1) * kStageBytes);
-  const int64_t i0 = (int64_t)blockIdx.x * total_items / gridDim.x;
-  const int n_items = (int)((int64_t)(blockIdx.x + 1) * total_items / gridDim.x - i0);
-  const int64_t h_first = i0 / per_head, h_last = (i0 + n_items - 1) / per_head;
+  const uint32_t g = blockIdx.x, G = gridDim.x;
+  const int n_items = (int)((total_items - g + G - 1) / G);
+  if (tid < kTags) sh.tag_cnt[tid] = 0u;
   if (tid == 0) {
-    sh.cnt[0][0] = sh.cnt[0][1] = sh.cnt[1][0] = sh.cnt[1][1] = 0u;
+    sh.n_staged = 0u;
     sh.abort = 0u;
   }
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sh.full[warp][s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  __syncwarp();                                      // the warp's barriers are initialised
 
-  pdl_wait();
-  pdl_launch_dependents();
-
-  // The samples of the first head and of the next one (a range spans at most two
-  // heads unless heads are small) go out before the ring fills the memory queues.
-  uint4 q0[kSampleUnits], q1[kSampleUnits];
-  load_sample(x + h_first * stride_h, L, stride_b, N, q0);
-  if (h_last > h_first) load_sample(x + (h_first + 1) * stride_h, L, stride_b, N, q1);
-  __syncthreads();                                   // barriers initialised
-
-  // The bytes of this warp's slice of an item whose piece holds `bytes`.
-  auto slice_of = [&](uint32_t bytes) {
-    const int64_t r = (int64_t)bytes - (int64_t)warp * kSliceBytes;
+  // this warp's slice of item k of the CTA (bytes, source)
+  auto slice = [&](int k, const uint8_t*& src) {
+    uint32_t h, b, c;
+    item_coords(g + (uint32_t)k * G, m, h, b, c);
+    const int32_t r = (int32_t)(c == m.n_pieces - 1 ? last_bytes : (uint32_t)kStageBytes) - warp * kSliceBytes;
+    src = reinterpret_cast<const uint8_t*>(x + (int64_t)b * stride_b + (int64_t)h * stride_h) +
+          (size_t)c * kStageBytes + (size_t)warp * kSliceBytes;
     return (uint32_t)(r <= 0 ? 0 : (r < kSliceBytes ? r : kSliceBytes));
   };
-  // Producer state (lane 0 of each warp): the next item to load, as (row b, head h)
-  // and the bytes left in its row from it on.
-  int64_t qb = i0 % per_head / pieces, qh = h_first, qrem = row_bytes - (i0 % per_head % pieces) * kStageBytes;
-  const uint8_t* q_src = reinterpret_cast<const uint8_t*>(x + qb * stride_b + qh * stride_h) + (row_bytes - qrem);
   int q_next = 0;
   auto produce = [&]() {                             // lane 0: this warp's slice of item q_next
     const int slot = q_next % kStages;
-    const uint32_t bytes = slice_of((uint32_t)min(qrem, (int64_t)kStageBytes));
+    const uint8_t* src;
+    const uint32_t bytes = slice(q_next, src);
     const uint32_t bar = smem_u32(&sh.full[warp][slot]);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the warp's reads of the slot came first
     mbar_expect_tx(bar, bytes);                      // (a zero-byte slice completes the phase at once)
-    if (bytes) bulk_g2s(smem_u32(ring + slot * kSliceBytes), q_src + warp * kSliceBytes, bytes, bar);
+    if (bytes) bulk_g2s(smem_u32(ring + slot * kSliceBytes), src, bytes, bar);
     ++q_next;
-    if (qrem > kStageBytes) {
-      qrem -= kStageBytes;
-      q_src += kStageBytes;
-    } else {
-      qrem = row_bytes;
-      if (++qb == B) { qb = 0; ++qh; }
-      q_src = reinterpret_cast<const uint8_t*>(x + qb * stride_b + qh * stride_h);
-    }
   };
+  // The ring's first loads go out while tail_pick_kernel (the grid this one
+  // depends on) runs: the input is complete by then, because that grid lets this
+  // one start only after its own wait for the work before it.  The workspace is
+  // touched only after the wait below.
   if (lane == 0)
     for (int s = 0; s < kStages && s < n_items; ++s) produce();
-  // Thresholds of the first two heads in one search, while the ring fills.
-  Thresholds th[2];
-  {
-    const SampleExt e[2] = {sample_extremes(q0), h_last > h_first ? sample_extremes(q1) : sample_extremes(q0)};
-    select_tails(e, rank, sh, th);
-  }
+  pdl_wait();
+  pdl_launch_dependents();
+  __syncthreads();                                   // the staging counters are initialised
 
-  // Consumer state (every thread): the head of the current item, the items left in
-  // that head, and the item's piece index in its row.  Head h_first + i stages its
-  // keys in buffer i & 1; a head change needs no barrier unless the CTA meets a
-  // third head (small heads), whose buffer must first be flushed.
-  int64_t ph = h_first, left = per_head - i0 % per_head;
-  int64_t pc = i0 % per_head % pieces;
-  int64_t cur = -1;
-  int buf = 0;
-  uint32_t key_lo = 0, key_hi = 0, mid2 = 0, vlo2 = 0, vhi2 = 0;
-  bool skip = true;
+  // thresholds of item k's head, loaded one item ahead
+  auto head_info = [&](int k, uint32_t& h) {
+    uint32_t b, c;
+    item_coords(g + (uint32_t)k * G, m, h, b, c);
+    return *reinterpret_cast<const uint4*>(&tails[h]);
+  };
+  uint32_t h_next = 0;
+  uint4 ti_next = n_items > 0 ? head_info(0, h_next) : make_uint4(0u, 0u, 1u, 0u);
+  int k0 = 0;                                        // first item of the current tag window
   for (int j = 0; j < n_items; ++j) {
-    if (ph != cur) {
-      buf = (int)((ph - h_first) & 1);
-      if (ph > h_first + 1) {                         // a third head or later
-        flush_tails(loc, sh, buf, tails + (ph - 2), lists + (ph - 2) * 2 * kListCap);
-        uint4 q[kSampleUnits];
-        load_sample(x + ph * stride_h, L, stride_b, N, q);
-        const SampleExt e[2] = {sample_extremes(q), sample_extremes(q)};
-        Thresholds t2[2];
-        select_tails(e, rank, sh, t2);
-        if (buf) th[1] = t2[0]; else th[0] = t2[0];
-      }
-      const Thresholds t = buf ? th[1] : th[0];
-      key_lo = t.lo;
-      key_hi = t.hi;
-      skip = t.degenerate;
-      if (skip && tid == 0) tails[ph].flag = 1u;
-      const float v_lo = key_value(key_lo), v_hi = key_value(key_hi);
-      vlo2 = (__float_as_uint(v_lo) >> 16) * 0x10001u;
-      vhi2 = (__float_as_uint(v_hi) >> 16) * 0x10001u;
-      // a bf16 pair strictly between the thresholds: stands in for bytes past a short piece
-      mid2 = (__float_as_uint(key_value(key_lo + 1u)) >> 16) * 0x10001u;
-      cur = ph;
+    const uint32_t h = h_next;
+    const uint4 ti = ti_next;
+    if (j + 1 < n_items) ti_next = head_info(j + 1, h_next);
+    if (j - k0 == kTagItems) {                       // the tags wrap: move the staged keys out
+      flush_staged(staged, sh, k0, g, G, m, tails, lists);
+      k0 = j;
     }
+    const uint32_t key_lo = ti.w & 0xffffu, key_hi = ti.w >> 16;
+    const bool skip = ti.z != 0u;                    // degenerate head: counted in full
+    const uint32_t vlo2 = (__float_as_uint(key_value(key_lo)) >> 16) * 0x10001u;
+    const uint32_t vhi2 = (__float_as_uint(key_value(key_hi)) >> 16) * 0x10001u;
+    // a bf16 pair strictly between the thresholds: stands in for bytes past a short slice
+    const uint32_t mid2 = (__float_as_uint(key_value(key_lo + 1u)) >> 16) * 0x10001u;
+    const uint32_t tag = 2u * (uint32_t)(j - k0);
+    uint16_t* list = lists + (size_t)h * 2 * kListCap;
     const int slot = j % kStages;
     const bool ok = warp_all(wait_bar(smem_u32(&sh.full[warp][slot]), (uint32_t)((j / kStages) & 1), &sh.abort, nullptr));
-    const uint32_t bytes = slice_of(pc == pieces - 1 ? last_bytes : (uint32_t)kStageBytes);
+    uint32_t hh, hb, hc;
+    item_coords(g + (uint32_t)j * G, m, hh, hb, hc);
+    const int32_t rb = (int32_t)(hc == m.n_pieces - 1 ? last_bytes : (uint32_t)kStageBytes) - warp * kSliceBytes;
+    const uint32_t bytes = (uint32_t)(rb <= 0 ? 0 : (rb < kSliceBytes ? rb : kSliceBytes));
     const uint8_t* slot_base = ring + slot * kSliceBytes;
     if (ok && !skip && bytes != 0u) {
       const uint8_t* st = slot_base + 16 * lane;
@@ -502,8 +530,8 @@ tail_stream_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, 
         }
         const int k = lane & 7;
         if (src < 32 && 16u * (uint32_t)(src + 32 * k) < bytes) {
-          const uint4 g = *reinterpret_cast<const uint4*>(slot_base + 16 * (src + 32 * k));
-          const uint32_t w[4] = {g.x, g.y, g.z, g.w};
+          const uint4 gr = *reinterpret_cast<const uint4*>(slot_base + 16 * (src + 32 * k));
+          const uint32_t w[4] = {gr.x, gr.y, gr.z, gr.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             if ((ble2(w[i], vlo2) | bge2(w[i], vhi2)) == 0u) continue;
@@ -511,8 +539,8 @@ tail_stream_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, 
 #pragma unroll
             for (int half = 0; half < 2; ++half) {            // the exact test, on keys
               const uint32_t key = half ? k2 >> 16 : k2 & 0xffffu;
-              if (key <= key_lo) stage_key(loc, sh, buf, 0, key);
-              else if (key >= key_hi) stage_key(loc, sh, buf, 1, key);
+              if (key <= key_lo) stage_key(staged, &sh.n_staged, tag, key, tails + h, list, 0);
+              else if (key >= key_hi) stage_key(staged, &sh.n_staged, tag + 1u, key, tails + h, list, 1);
             }
           }
         }
@@ -520,20 +548,20 @@ tail_stream_kernel(const uint16_t* __restrict__ x, int64_t L, int64_t stride_b, 
     }
     __syncwarp();                                    // the warp is done with the slot: refill it
     if (lane == 0 && q_next < n_items && !*reinterpret_cast<volatile uint32_t*>(&sh.abort)) produce();
-    if (++pc == pieces) pc = 0;
-    if (--left == 0) { ++ph; left = per_head; }
   }
   if (lane == 0 && *reinterpret_cast<volatile uint32_t*>(&sh.abort)) {
-    // gave up: the heads of this range are counted in full; the warp's copies still
-    // in flight (its last slots filled) get one more bounded wait before the CTA exits
-    for (int64_t h = h_first; h <= h_last; ++h) tails[h].flag = 1u;
+    // gave up: the heads of the CTA's items are counted in full; the warp's copies
+    // still in flight (its last slots filled) get one more bounded wait before exit
+    for (int k = 0; k < n_items; ++k) {
+      uint32_t h, b, c;
+      item_coords(g + (uint32_t)k * G, m, h, b, c);
+      tails[h].flag = 1u;
+    }
     uint32_t no_abort = 0u;
     for (int jj = q_next > kStages ? q_next - kStages : 0; jj < q_next; ++jj)
       wait_bar(smem_u32(&sh.full[warp][jj % kStages]), (uint32_t)((jj / kStages) & 1), &no_abort, nullptr);
   }
-  // the last two heads' staged keys
-  if (cur > h_first) flush_tails(loc, sh, buf ^ 1, tails + (cur - 1), lists + (cur - 1) * 2 * kListCap);
-  if (cur >= 0) flush_tails(loc, sh, buf, tails + cur, lists + cur * 2 * kListCap);
+  flush_staged(staged, sh, k0, g, G, m, tails, lists);
 }
 
 // A window: its exact width hi - lo as the unevaluated fp32 sum ws + we (the
@@ -923,10 +951,16 @@ FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L
   const double r_want = 3.0 * kS * (double)span / (double)N + 4.0;
   const uint32_t rank = r_want >= kS ? (uint32_t)kS : (uint32_t)r_want;
   const bool use_lists = vec && rank <= (uint32_t)kMaxRank && (double)N * rank / kS <= 0.5 * kListCap;
-  if (use_lists) {
-    const int64_t pieces = (2 * L + kStageBytes - 1) / kStageBytes;
-    const int64_t total_items = pieces * B * H;
+  const int64_t pieces = (2 * L + kStageBytes - 1) / kStageBytes;
+  const int64_t total_items = pieces * B * H;
+  if (use_lists && total_items < ((int64_t)1 << 31)) {
     const unsigned grid = (unsigned)(total_items < sms ? total_items : sms);
+    ItemMap m;
+    m.n_pieces = (uint32_t)pieces;
+    m.n_per_head = (uint32_t)(pieces * B);
+    m.pieces = make_divu32(m.n_pieces);
+    m.per_head = make_divu32(m.n_per_head);
+    const uint32_t last_bytes = (uint32_t)(2 * L - (pieces - 1) * kStageBytes);
     if (cudaFuncSetAttribute(tail_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStreamSmem) !=
         cudaSuccess)
       return FA3_ECUDA;
@@ -935,9 +969,16 @@ FA3_API int fa3_calibrate_perhead(const uint16_t* x, int64_t B, int H, int64_t L
     const int wsmem = (int)(kWinThreads * kPadWords * 4 + 4 * span);
     if (cudaFuncSetAttribute(window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wsmem) != cudaSuccess)
       return FA3_ECUDA;
+    // the pick kernel's CTAs share SMs with the stream kernel's, whose ring needs
+    // nearly all of the shared memory: ask for the same carve-out
+    if (cudaFuncSetAttribute(tail_pick_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+      return FA3_ECUDA;
+    if (launch_pdl(tail_pick_kernel, dim3(H), dim3(kPickThreads), 0, s, x, L, stride_b, stride_h,
+                   (unsigned long long)N, rank, tails) != cudaSuccess)
+      return FA3_ECUDA;
     timing_begin(s);
-    if (launch_pdl(tail_stream_kernel, dim3(grid), dim3(kStreamThreads), kStreamSmem, s, x, L, stride_b, stride_h,
-                   B, (unsigned long long)N, rank, total_items, tails, lists) != cudaSuccess)
+    if (launch_pdl(tail_stream_kernel, dim3(grid), dim3(kStreamThreads), kStreamSmem, s, x, stride_b, stride_h,
+                   (uint32_t)total_items, m, last_bytes, tails, lists) != cudaSuccess)
       return FA3_ECUDA;
     timing_end(s);
     if (launch_pdl(window_kernel, dim3(H), dim3(kWinThreads), wsmem, s, counts, (unsigned long long)N,

@@ -160,27 +160,29 @@ def test_full_size_calibration_all_heads_four_batches():
     assert np.array_equal(_bits(sc), _bits(O.qparams(omn, omx)))
 
 
-def _sampled_units(units, n_samples=2048):
-    # the strided sample the tail thresholds are drawn from (16-byte groups)
-    return sorted({g * units // n_samples for g in range(n_samples)})
+def _sample_runs(units, runs=16, run_len=128):
+    # the tail thresholds' sample: 16 runs of 128 consecutive 16-byte groups, run r
+    # from group r * units // 16; sampling thread 16 r + (w % 16) holds group w of run r
+    return [[(r * units // runs + w) % units for w in range(run_len)] for r in range(runs)]
 
 
 @pytest.mark.parametrize("vec", [True, False])
 def test_thin_tails_fall_back_to_full_count(vec):
-    # Plant one extreme value into the first 60 sampled groups of head 0 (480 values,
-    # one group in each of 60 sampling threads, more than the sample rank of 53): the
-    # low threshold then falls on that value, whose count (480) is below the 1574
-    # smallest values a window can start from, so the tail lists must be rejected and
-    # the head counted again in full.  Head 1 is left as is.  With an odd row stride
-    # (vec False) the input takes the histogram path instead; the result is the same
-    # either way.
+    # Plant one extreme value into the first sixteen sampled groups of runs 0..3 of
+    # head 0 (512 values, one group in each of 64 sampling threads, more than the
+    # sample rank of 53): the low threshold then falls on that value, whose count
+    # (512) is below the 1574 smallest values a window can start from, so the tail
+    # lists must be rejected and the head counted again in full.  Head 1 is left
+    # as is.  With an odd row stride (vec False) the input takes the histogram path
+    # instead; the result is the same either way.
     F = fa3()
     rng = np.random.default_rng(11)
     H, N = 2, 4 * 2048 * 192
     ratio = 0.999                                  # N - target_num + 1 = 1574 window starts
     x = W.bf16_round(rng.standard_normal((H, N)).astype(np.float32))
-    for u in _sampled_units(N // 8)[:60]:
-        x[0, u * 8:u * 8 + 8] = -600.0
+    for run in _sample_runs(N // 8)[:4]:
+        for u in run[:16]:
+            x[0, u * 8:u * 8 + 8] = -600.0
     if vec:
         xd = bf16_dev(x)
     else:
@@ -199,30 +201,29 @@ def test_thin_tails_fall_back_to_full_count(vec):
 
 def test_tail_list_path_every_branch():
     # One (H, N) batch at ratio 0.9999 (158 window starts, sample rank 8), one head
-    # per branch of the tail-list path:
+    # per branch of the tail-list path (the low threshold sits near -26 for the
+    # Student-t heads, so every planted -50 lands in the low list):
     #   0  ordinary Student-t head: decided from its lists;
-    #   1  6000 copies of -50 inside one 64 KB piece of the row: one CTA stages most
+    #   1  3000 copies of -50 inside one 64 KB piece of the row: one CTA stages most
     #      of a list, still decided from the lists;
-    #   2  20000 copies of -50 at the start of the row: the low list overflows its
-    #      capacity and the head is counted in full;
+    #   2  20000 copies of -50 spread over the row: no CTA stages too many, but the
+    #      head's low list overflows its capacity, so the head is counted in full;
     #   3  a constant head: the sample's thresholds meet (degenerate), full count;
     #   4  negative values only, with a high tail of one repeated value;
-    #   5  12000 copies of -50 inside one piece: more than one CTA may stage for a
-    #      head, so the head is counted in full.
+    #   5  12000 copies of -50 inside one piece: one CTA meets more keys than it can
+    #      stage, so the head is counted in full.
     F = fa3()
     rng = np.random.default_rng(12)
     H, N = 6, 4 * 2048 * 192
     ratio = 0.9999
     x = (rng.standard_t(3, (H, N)) * 2.0).astype(np.float32)
-    x[1, 3 * 16384:3 * 16384 + 6000] = -50.0
-    x[2, :20000] = -50.0
+    x[1, 3 * 32768 + 100:3 * 32768 + 3100] = -50.0
+    x[2, np.linspace(0, N - 1, 20000).astype(np.int64)] = -50.0
     x[3] = 1.5
     x[4] = -np.abs(x[4]) - 1.0
     x[4, rng.choice(N, 3000, replace=False)] = -0.5
-    x[5, 5 * 16384:5 * 16384 + 12000] = -50.0
+    x[5, 5 * 32768 + 100:5 * 32768 + 12100] = -50.0
     x = W.bf16_round(x)
-    for lo, n in ((3 * 16384, 6000), (5 * 16384, 12000)):
-        assert sum(1 for u in _sampled_units(N // 8) if lo <= 8 * u < lo + n) >= 8
     omn, omx = O.calibrate([x.reshape(1, H, 1, N)], ratio)
     xd = bf16_dev(x)
     for _ in range(2):
