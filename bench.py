@@ -344,11 +344,45 @@ def run_gpu(args):
         return torch.randint(-127, 128, shape, dtype=torch.int8, device=dev, generator=gen)
 
     gB, gHq, gHkv, gD, gT = 16, 64, 8, 128, 4096
-    gk, gv, gq = i8((gB, gT, gHkv, gD)), i8((gB, gT, gHkv, gD)), i8((gB, gHq, gD))
+    # two cache copies used in turn: 2 x 134 MB, more than L2 holds
+    gkv = [(i8((gB, gT, gHkv, gD)), i8((gB, gT, gHkv, gD))) for _ in range(2)]
+    gq = i8((gB, gHq, gD))
     gs1, gs2 = torch.full((gHq,), 0.01, device=dev), torch.full((gHkv,), 0.01, device=dev)
     glens = torch.full((gB,), gT, dtype=torch.int32, device=dev)
-    gqa_ms = timed(lambda: F.decode_attn_gqa(gq, gk, gv, gs1, gs2, gs2, glens, 1 / math.sqrt(128)), 50)
-    del gk, gv
+    gstep = [0]
+
+    def gqa_call():
+        gk, gv = gkv[gstep[0] & 1]
+        gstep[0] += 1
+        F.decode_attn_gqa(gq, gk, gv, gs1, gs2, gs2, glens, 1 / math.sqrt(128))
+
+    gqa_ms = timed(gqa_call, 50)
+    # the same calls replayed from a CUDA graph, as a serving loop issues them: the
+    # GPU time of a call without the host's per-call work
+    gout = torch.empty(gB, gHq, gD, dtype=torch.bfloat16, device=dev)
+    gws = torch.zeros(max(16, F.gqa_workspace_size(gB, gHq, gHkv, gD, gT)), dtype=torch.uint8, device=dev)
+    gst = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(gst):
+        for i in range(3):
+            F.decode_attn_gqa(gq, gkv[i & 1][0], gkv[i & 1][1], gs1, gs2, gs2, glens, 1 / math.sqrt(128),
+                              out=gout, workspace=gws, stream=gst)
+    gst.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gst):
+        for i in range(20):
+            F.decode_attn_gqa(gq, gkv[i & 1][0], gkv[i & 1][1], gs1, gs2, gs2, glens, 1 / math.sqrt(128),
+                              out=gout, workspace=gws, stream=gst)
+    graph.replay()
+    torch.cuda.synchronize()
+    ga, gz = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ga.record()
+    for _ in range(5):
+        graph.replay()
+    gz.record()
+    torch.cuda.synchronize()
+    gqa_graph_ms = ga.elapsed_time(gz) / 100
+    del graph, gkv
     pS = 4096
     pq, pk, pv = i8((1, pS, gHq, gD)), i8((1, pS, gHkv, gD)), i8((1, pS, gHkv, gD))
     pl = torch.full((1,), pS, dtype=torch.int32, device=dev)
@@ -524,9 +558,12 @@ def run_gpu(args):
         "decode_call": {"ms": mla_ms, "kv_gbs": kv_gbs, "tflops": flops_per_step() / (mla_ms / 1e3) / 1e12,
                         "kernels": "query pre-pass + mla_decode_kernel + split-K combine",
                         "timing": "CUDA events around the call, second timed pass"},
-        "gqa_decode": {"workload": "llama70b-gqa b16 hq64 hkv8 d128 ctx4096, int8 q/k/v (one call: decode + combine)",
+        "gqa_decode": {"workload": "llama70b-gqa b16 hq64 hkv8 d128 ctx4096, int8 q/k/v (one call, one kernel; "
+                                   "two cache copies used in turn)",
                        "us_per_call": gqa_ms * 1e3, "kv_gbs": gB * gT * gHkv * gD * 2 / (gqa_ms / 1e3) / 1e9,
-                       "hbm_frac_of_measured": gB * gT * gHkv * gD * 2 / (gqa_ms / 1e3) / 1e9 / hbm},
+                       "hbm_frac_of_measured": gB * gT * gHkv * gD * 2 / (gqa_ms / 1e3) / 1e9 / hbm,
+                       "us_per_call_graph": gqa_graph_ms * 1e3,
+                       "hbm_frac_of_measured_graph": gB * gT * gHkv * gD * 2 / (gqa_graph_ms / 1e3) / 1e9 / hbm},
         "prefill": {"workload": "llama70b-prefill b1 s4096 t4096 hq64 hkv8 d128 causal, int8 q/k/v",
                     "us_per_call": pre_ms * 1e3, "tflops": pre_flop / (pre_ms / 1e3) / 1e12,
                     "frac_of_measured_bf16": pre_flop / (pre_ms / 1e3) / 1e12 / bf16},
@@ -600,12 +637,19 @@ def run_kernel(args):
         unit = ("KV GB/s", Bq * Tq * Hkv * D * 2)
     elif k == "gqa":
         Bq, Hq, Hkv, D, Tq = 16, 64, 8, 128, 4096
-        kc = torch.randint(-127, 128, (Bq, Tq, Hkv, D), dtype=torch.int8, device=dev, generator=g)
-        vc = torch.randint(-127, 128, (Bq, Tq, Hkv, D), dtype=torch.int8, device=dev, generator=g)
+        # two cache copies used in turn (2 x 134 MB: more than L2 holds)
+        kvs = [(torch.randint(-127, 128, (Bq, Tq, Hkv, D), dtype=torch.int8, device=dev, generator=g),
+                torch.randint(-127, 128, (Bq, Tq, Hkv, D), dtype=torch.int8, device=dev, generator=g))
+               for _ in range(2)]
         q8 = torch.randint(-127, 128, (Bq, Hq, D), dtype=torch.int8, device=dev, generator=g)
         s1, s2 = torch.full((Hq,), 0.01, device=dev), torch.full((Hkv,), 0.01, device=dev)
         lens = torch.full((Bq,), Tq, dtype=torch.int32, device=dev)
-        fn = lambda: F.decode_attn_gqa(q8, kc, vc, s1, s2, s2, lens, 1 / math.sqrt(128))
+        step = [0]
+
+        def fn():
+            kc, vc = kvs[step[0] & 1]
+            step[0] += 1
+            F.decode_attn_gqa(q8, kc, vc, s1, s2, s2, lens, 1 / math.sqrt(128))
         unit = ("KV GB/s", Bq * Tq * Hkv * D * 2)
     elif k == "prefill":
         # Llama-3.1-70B-shaped causal prefill: S = T new rows per sequence, 64 / 8 heads

@@ -975,19 +975,6 @@ __global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p) 
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // Number of 2-CTA clusters that can be resident at once (cached per device).
 int max_clusters() {
   static int cached[64] = {0};
@@ -1095,7 +1082,7 @@ int mla_decode(const uint16_t* q, const int8_t* ckv, const uint16_t* krope, cons
   size_t off_ml, off_qlat, off_qrope, off_seg;
   const size_t need = mla_ws_parts(B, Dl, C, &off_ml, &off_qlat, &off_qrope, &off_seg);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FA3_EWORKSPACE;
-  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return FA3_ECUDA;
 
   MlaParams prm;

@@ -65,6 +65,39 @@ def test_fewer_query_heads_per_group():
     assert_attn_close(got, ref, bf16_out=True, what="gqa G=3")
 
 
+def test_runs_shared_between_ctas_and_workspace_reuse():
+    # The tiles of all (b, g) pairs are dealt to one wave of CTAs in runs, equal
+    # runs inside each sequence or runs of equal cost across sequences: pairs
+    # shared by many CTAs (some of whose runs lie past the sequence's length),
+    # runs that end mid-pair, runs holding several whole pairs, and one
+    # zero-filled workspace reused across all of them, zero-filled again after
+    # every call.
+    F = fa3()
+    cases = [
+        (3, 64, 8, 4096, [4096, 70, 2500]),
+        (40, 16, 2, 300, None),
+        (600, 8, 1, 64, None),
+        (7, 24, 8, 1000, [1000, 1, 999, 64, 65, 0, 513]),
+        (40, 64, 8, 2048, None),   # runs of equal cost crossing sequences (an agent lane counts a first unit)
+    ]
+    need = max(F.gqa_workspace_size(B, Hq, Hkv, 128, T) for B, Hq, Hkv, T, _ in cases)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    for B, Hq, Hkv, T, lens in cases:
+        w = W.gqa_llama70b(B=B, T=T)
+        w.Hq, w.Hkv = Hq, Hkv
+        if lens is None:
+            lens = np.random.default_rng(B).integers(1, T + 1, B)
+        inp, args = _case(w, lens=lens)
+        q8, k8, v8, qs, ks, vs, ln = args
+        out = F.decode_attn_gqa(t(q8), t(k8), t(v8), t(qs), t(ks), t(vs), t(ln), w.softmax_scale, workspace=ws)
+        torch.cuda.synchronize()
+        ref = O.gqa_decode(*args[:6], ln, w.softmax_scale)
+        assert_attn_close(out.float().cpu().numpy(), ref, bf16_out=True, what=f"gqa runs B={B} Hkv={Hkv} T={T}")
+        assert not bool(ws.any()), "workspace not left zero-filled"
+
+
 @pytest.mark.slow
 def test_llama70b_full_size():
     F = fa3()

@@ -110,7 +110,7 @@ def _gqa_case(B, T, lens):
     return w, q8, k8, v8, qs, ks, vs, np.asarray(lens, np.int32)
 
 
-@pytest.mark.parametrize("page_size", [16, 64])
+@pytest.mark.parametrize("page_size", [16, 32, 48, 64, 96, 128])
 def test_gqa_paged_ragged(page_size):
     F = fa3()
     w, q8, k8, v8, qs, ks, vs, lens = _gqa_case(4, 300, [1, 37, 300, 129])
@@ -127,7 +127,7 @@ def test_gqa_paged_ragged(page_size):
                        qs, ks, vs, lens, w.softmax_scale)
     assert_attn_close(got, ref, bf16_out=True, what=f"gqa paged {page_size}")
     assert int(err.item()) == 0
-    bt[2, 3] = -1                           # inside lens[2]
+    bt[2, min(3, (int(lens[2]) - 1) // page_size)] = -1     # a page inside lens[2]
     got = F.decode_attn_gqa_paged(_t(q8), _t(k_pool), _t(v_pool), _t(qs), _t(ks), _t(vs), _t(lens), _t(bt),
                                   w.softmax_scale, dev_err=err)
     torch.cuda.synchronize()
