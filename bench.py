@@ -558,7 +558,7 @@ def run_gpu(args):
         "decode_call": {"ms": mla_ms, "kv_gbs": kv_gbs, "tflops": flops_per_step() / (mla_ms / 1e3) / 1e12,
                         "kernels": "query pre-pass + mla_decode_kernel + split-K combine",
                         "timing": "CUDA events around the call, second timed pass"},
-        "gqa_decode": {"workload": "llama70b-gqa b16 hq64 hkv8 d128 ctx4096, int8 q/k/v (one call, one kernel; "
+        "gqa_decode": {"workload": "llama70b-gqa b16 hq64 hkv8 d128 ctx4096, int8 q/k/v (one call: decode + combine; "
                                    "two cache copies used in turn)",
                        "us_per_call": gqa_ms * 1e3, "kv_gbs": gB * gT * gHkv * gD * 2 / (gqa_ms / 1e3) / 1e9,
                        "hbm_frac_of_measured": gB * gT * gHkv * gD * 2 / (gqa_ms / 1e3) / 1e9 / hbm,

@@ -258,14 +258,8 @@ int fa3_decode_attn_mla(const uint16_t* q, const int8_t* ckv, const uint16_t* kr
  * q        int8 [B][Hq][D];  k, v  int8 [B][T_max][Hkv][D].
  * q_scale  float[Hq];  k_scale, v_scale  float[Hkv].
  * lens     int32[B] (as for MLA).   out  bf16 [B][Hq][D].
- * Supported: D = 128, 1 <= Hq / Hkv <= 8; 16-byte aligned rows,
- * B * T_max < 2^31 - 64 (else FA3_ERANGE).
- * workspace  fa3_gqa_workspace_size(B, Hq, Hkv, D, T_max) bytes (0: none
- *            needed), 16-byte aligned: per-(b, g) arrival counters, then the
- *            partials of the (b, g) pairs that several CTAs share.  It must be
- *            zero-filled before its first use (one cudaMemset); every call
- *            leaves it zero-filled again, so a workspace is reused without
- *            clearing, also for other sizes.
+ * Supported: D = 128, 1 <= Hq / Hkv <= 8; 16-byte aligned rows.
+ * workspace  fa3_gqa_workspace_size(B, Hq, Hkv, D, T_max) bytes.
  * ------------------------------------------------------------------------ */
 size_t fa3_gqa_workspace_size(int B, int Hq, int Hkv, int D, int T_max);
 
@@ -328,16 +322,15 @@ int fa3_prefill_attn_gqa(const int8_t* q, const int8_t* k, const int8_t* v,
  * allocation ahead of time, deployments that forbid allocation after start-up).
  *
  * Same arguments and results as fa3_decode_attn_gqa, without the workspace:
- * the workspace is a fixed 8 MiB array in the library's own device memory,
- * which every GPU that loads libfa3.so holds until the process exits.  Sizes
- * whose workspace would need more than 8 MiB (fa3_gqa_workspace_size() >
- * 8 MiB) return FA3_EWORKSPACE; the plan (at most one wave of resident CTAs,
- * two 4 KB partials each) keeps the partials below 4 MiB on GB300, and the
- * counters take 4 bytes per (b, g) pair.
+ * the split-K partials go to a fixed 8 MiB array in the library's own device
+ * memory, which every GPU that loads libfa3.so holds until the process exits.
+ * Sizes whose partials would need more than 8 MiB (fa3_gqa_workspace_size() >
+ * 8 MiB) return FA3_EWORKSPACE; the split plan (at most one wave of resident
+ * CTAs, 4 KB of partials each) keeps every size below 2 MiB on GB300.
  * The first call on each device looks up the array's device address (this
  * may initialise the module on that device): make that first call before any
- * stream capture.  All calls share the one array: it starts zero-filled with
- * the module and every call leaves it zero-filled; calls that overlap on the
+ * stream capture.  All calls share the one array and it keeps the last call's
+ * contents (nothing in it needs to start at zero); calls that overlap on the
  * GPU -- on different streams, or from different host threads -- race on it.
  * ------------------------------------------------------------------------ */
 int fa3_decode_attn_gqa_noalloc(const int8_t* q, const int8_t* k, const int8_t* v,
@@ -391,8 +384,7 @@ int fa3_decode_attn_mla_paged(const uint16_t* q, const int8_t* ckv, const uint16
 
 /* GQA decode over a paged cache (fa3_decode_attn_gqa's arithmetic).
  * k, v   int8 [num_pages][page_size][Hkv][D] pools.
- * Supported: as fa3_decode_attn_gqa, page_size a multiple of 16,
- * num_pages * page_size < 2^31 - 64 (else FA3_ERANGE).
+ * Supported: as fa3_decode_attn_gqa, page_size a multiple of 16.
  * workspace  fa3_gqa_workspace_size(B, Hq, Hkv, D, max_pages * page_size) bytes. */
 int fa3_decode_attn_gqa_paged(const int8_t* q, const int8_t* k, const int8_t* v,
                               const float* q_scale, const float* k_scale, const float* v_scale,

@@ -28,12 +28,6 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   }
   return fn;
 }
-// 2D tiled TMA load (coordinates: innermost first) into this CTA's shared memory.
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar) : "memory");
-}
 
 // ----------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -47,15 +41,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t a) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t tx) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(tx) : "memory");
-}
-// A 2D TMA box fetched into L2 only (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_2d(const void* tm, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tm), "r"(c0), "r"(c1)
-               : "memory");
-}
-// Adds tx bytes to the current phase's expected transactions, without an arrival.
-__device__ __forceinline__ void mbar_expect_only(uint32_t a, uint32_t tx) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(tx) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");

@@ -407,7 +407,7 @@ def decode_attn_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_scale: 
         out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=q.device)
     nbytes = gqa_workspace_size(B, Hq, Hkv, D, T_max)
     if workspace is None:
-        workspace = _workspace("gqa", nbytes, q.device, zero=True, stream=stream)
+        workspace = _workspace("gqa", nbytes, q.device, stream=stream)
     st = lib().fa3_decode_attn_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
                                    _ptr(lens), _ptr(out), B, Hq, Hkv, D, T_max, float(softmax_scale),
                                    _ptr(workspace), 0 if workspace is None else workspace.numel(),
@@ -437,7 +437,7 @@ def decode_attn_gqa_channel(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q
         out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=q.device)
     nbytes = gqa_workspace_size(B, Hq, Hkv, D, T_max)
     if workspace is None:
-        workspace = _workspace("gqa", nbytes, q.device, zero=True, stream=stream)
+        workspace = _workspace("gqa", nbytes, q.device, stream=stream)
     st = lib().fa3_decode_attn_gqa_channel(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(q_offset), _ptr(k_scale),
                                            _ptr(k_offset), _ptr(v_scale), _ptr(v_offset), _ptr(lens), _ptr(out), B,
                                            Hq, Hkv, D, T_max, float(softmax_scale), _ptr(workspace),
@@ -555,7 +555,7 @@ def decode_attn_gqa_paged(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_s
         out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=q.device)
     nbytes = gqa_workspace_size(B, Hq, Hkv, D, max_pages * page_size)
     if workspace is None:
-        workspace = _workspace("gqa", nbytes, q.device, zero=True, stream=stream)
+        workspace = _workspace("gqa", nbytes, q.device, stream=stream)
     st = lib().fa3_decode_attn_gqa_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
                                          _ptr(lens), _ptr(block_table), _ptr(out), B, Hq, Hkv, D, num_pages,
                                          page_size, max_pages, float(softmax_scale), _ptr(workspace),

@@ -63,8 +63,8 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 def test_split_plan_keeps_partials_within_the_fixed_scratch():
-    # Partials take two 4 KB blocks per CTA and the plan never makes more CTAs than
-    # one wave of resident ones; the counters take 4 bytes per (sequence, KV head).
+    # Partials take one 4 KB block per (sequence, KV head, split); the plan never
+    # makes more blocks than one wave of resident CTAs, far below 8 MiB.
     F = fa3()
     for B in (1, 2, 7, 16, 57, 128, 137, 1024):
         for Hkv in (1, 2, 8):
