@@ -319,6 +319,26 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     cal_ms = e0.elapsed_time(e1) / n_cal
+    # the same call replayed from a CUDA graph: its three kernels without the host's per-call work
+    cws = torch.zeros(F.calibrate_workspace_size(H), dtype=torch.uint8, device=dev)
+    cst = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(cst):
+        F.calibrate_perhead(cal_big, 0.9999, cmn, cmx, workspace=cws, stream=cst)
+    cst.synchronize()
+    cgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cgraph, stream=cst):
+        for _ in range(n_cal):
+            F.calibrate_perhead(cal_big, 0.9999, cmn, cmx, workspace=cws, stream=cst)
+    cgraph.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(3):
+        cgraph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    cal_graph_ms = e0.elapsed_time(e1) / (3 * n_cal)
+    del cgraph, cws
     for x in calib_q:
         F.calibrate_perhead(x, 0.9999, qmn, qmx)
     for x in calib_kv:
@@ -569,7 +589,9 @@ def run_gpu(args):
                     "frac_of_measured_bf16": pre_flop / (pre_ms / 1e3) / 1e12 / bf16},
         "calibration": {"workload": "B=4 H=128 S=2048 D=192 bf16, ratio 0.9999, Student-t nu=3 x per-head "
                                     "log-uniform [0.1, 10] sigma", "ms_per_batch": cal_ms,
-                        "gbs": 4 * H * 2048 * 192 * 2 / (cal_ms / 1e3) / 1e9},
+                        "gbs": 4 * H * 2048 * 192 * 2 / (cal_ms / 1e3) / 1e9,
+                        "ms_per_batch_graph": cal_graph_ms,
+                        "hbm_frac_of_measured_graph": 4 * H * 2048 * 192 * 2 / (cal_graph_ms / 1e3) / 1e9 / hbm},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
