@@ -348,17 +348,21 @@ def run_gpu(args):
     del cal_big
 
     # ---- the other attention calls at their workloads' shapes (reported beside the step)
-    def timed(fn, n):
+    def timed(fn, n, rounds=3):
+        # median over `rounds` timed batches of n calls (one batch swings with the host's timing)
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n):
-            fn()
-        z.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(z) / n
+        per = []
+        for _ in range(rounds):
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                fn()
+            z.record(stream)
+            torch.cuda.synchronize()
+            per.append(a.elapsed_time(z) / n)
+        return sorted(per)[len(per) // 2]
 
     def i8(shape):
         return torch.randint(-127, 128, shape, dtype=torch.int8, device=dev, generator=gen)
